@@ -1,0 +1,518 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused q-norm / RoPE / KV-quant / paged-insert step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload stress]
+    python bench.py --impl reference ...      # the CPU oracle on a bounded sample
+
+A step is one pass of the whole fused step (one launch) over one batch: by default
+the "stress" workload, 131072 tokens x 128 q heads (q is 17.2 GB of bf16), FP8 cache
+of 2048 x 64 slots.  Inputs are resident in HBM before the timed region; q is far
+larger than the 129 MB L2, so no flush is needed between steps (q is rewritten in
+place; every step moves the same bytes).  Rank 0 prints one JSON line.
+
+For N > 1 (torchrun, one rank per GPU) every rank runs its own independent batch of
+the same shape (seed offset by rank): weak scaling, no collective on the data path;
+the timed region is bracketed by barriers and the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import dataclasses
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+from synth import configs  # noqa: E402
+
+METRIC = "HBM GB/s (% of warm copy ceiling) and tokens/s, fused qnorm-rope-kv-insert"
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0
+
+
+# ------------------------------------------------------------------ distributed glue
+
+def dist_env():
+    """(rank, world_size, local_rank) from torchrun's environment (1 process: 0, 1, 0)."""
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def rank_workload(wl: configs.Workload, rank: int) -> configs.Workload:
+    """Rank r's independent batch: the same shape, seed offset by 1000 * r."""
+    if rank == 0:
+        return wl
+    name = f"{wl.name}@rank{rank}"
+    configs._POSITIONS.setdefault(name, configs._POSITIONS[wl.name])
+    configs._SLOTS.setdefault(name, configs._SLOTS[wl.name])
+    return dataclasses.replace(wl, name=name, seed=wl.seed + 1000 * rank)
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(value: float, world: int, device=None) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ measurement helpers
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples every 100 ms while running."""
+
+    FIELDS = ("timestamp,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id: str | None):
+        self.bus_id = bus_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        self.out = os.fdopen(fd, "w")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self) -> dict:
+        time.sleep(0.25)
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                if self.bus_id and self.bus_id.lower() not in parts[1].lower():
+                    continue
+                try:
+                    rows.append((float(parts[2]), float(parts[3]), parts[5:9]))
+                except ValueError:
+                    continue
+        os.remove(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for _, _, flags in rows for n, fl in zip(names, flags)
+                          if fl.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def bus_id_of(device_index: int) -> str | None:
+    import torch
+    p = torch.cuda.get_device_properties(device_index)
+    try:
+        return f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}"
+    except AttributeError:
+        return None
+
+
+def copy_ceiling_gbs(dev, nbytes: int) -> float:
+    """Warm device-to-device copy: read + write bytes / time, median of 10 after 3 warm-ups."""
+    import torch
+    a = torch.empty(nbytes // 2, dtype=torch.bfloat16, device=dev)
+    b = torch.empty_like(a)
+    a.fill_(1.0)
+    for _ in range(3):
+        b.copy_(a)
+    torch.cuda.synchronize(dev)
+    times = []
+    for _ in range(10):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        b.copy_(a)
+        e1.record()
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1) / 1e3)
+    del a, b
+    return 2 * nbytes / statistics.median(times) / 1e9
+
+
+# ------------------------------------------------------------------ inputs on the device
+
+class DeviceBatch:
+    """One workload resident in HBM.  q and kv are drawn on the device by a seeded
+    torch generator (N(0,1), the workload's heavy tail, rounded to bf16); positions,
+    slots, the weight and the cos/sin table come from ``synth``."""
+
+    def __init__(self, wl: configs.Workload, dev):
+        import torch
+        self.wl = wl
+        self.dev = dev
+        g = torch.Generator(device=dev)
+        g.manual_seed(wl.seed * 7919 + 17)
+        self.q = self._normal((wl.T, wl.H, 512), g)
+        self.kv = self._normal((wl.T, 512), g)
+        self.positions_np = wl.positions()
+        self.slots_np = wl.slot_mapping()
+        self.w = torch.from_numpy(configs.weight_bits(wl).view(np.int16)).view(torch.bfloat16).to(dev)
+        self.pos = torch.from_numpy(self.positions_np).to(dev)
+        self.slots = torch.from_numpy(self.slots_np).to(dev)
+        self.cs = torch.from_numpy(configs.cos_sin(wl)).to(dev)
+        self.cache = torch.zeros(configs.cache_bytes(wl), dtype=torch.uint8, device=dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.bytes = configs.algorithmic_bytes(wl, self.positions_np, self.slots_np)
+
+    def _normal(self, shape, g):
+        import torch
+        wl = self.wl
+        out = torch.empty(shape, dtype=torch.bfloat16, device=self.dev)
+        flat = out.view(-1)
+        chunk = 1 << 28
+        for i in range(0, flat.numel(), chunk):
+            n = min(chunk, flat.numel() - i)
+            x = torch.randn(n, generator=g, device=self.dev, dtype=torch.float32)
+            if wl.tail_frac > 0:
+                u = torch.rand(n, generator=g, device=self.dev, dtype=torch.float32)
+                x = torch.where(u < wl.tail_frac, x * wl.tail_mult, x)
+            flat[i:i + n] = x.to(torch.bfloat16)
+            del x
+        return out
+
+    def args(self, stream_handle: int):
+        wl = self.wl
+        return (self.q.data_ptr(), self.kv.data_ptr(), self.w.data_ptr(), self.pos.data_ptr(),
+                self.cs.data_ptr(), wl.max_position, self.slots.data_ptr(), self.cache.data_ptr(),
+                wl.num_blocks, wl.block_size, wl.T, wl.H, wl.eps, self.err.data_ptr(), stream_handle)
+
+
+def entry(lib, store: str):
+    return (lib.dsv4_qnorm_rope_kv_quant_insert if store == "fp8"
+            else lib.dsv4_qnorm_rope_kv_bf16_insert)
+
+
+def known_answer_check() -> str:
+    """The tiny workload against the oracle at the parity bar (before and after timing)."""
+    from tests import harness
+    rep = harness.check(configs.TINY)
+    return "pass" if rep.ok else f"FAIL: {rep}"
+
+
+# ------------------------------------------------------------------ end to end
+
+def e2e_run(batch: DeviceBatch, lib, steps: int, chunks: int = 8):
+    """Same metric through the C ABI with host buffers: per step, token chunks of q, kv,
+    positions and slots go host->device from pinned memory, the kernel runs on each chunk,
+    and q plus the cache come back device->host; copies in each direction overlap the
+    kernel of neighbouring chunks on three streams.  Returns (GB/s, h2d, d2h bytes/step)."""
+    import torch
+    wl = batch.wl
+    dev = batch.dev
+    q_h = torch.empty((wl.T, wl.H, 512), dtype=torch.bfloat16, pin_memory=True)
+    kv_h = torch.empty((wl.T, 512), dtype=torch.bfloat16, pin_memory=True)
+    pos_h = torch.from_numpy(batch.positions_np).pin_memory()
+    sl_h = torch.from_numpy(batch.slots_np).pin_memory()
+    cache_h = torch.empty(batch.cache.numel(), dtype=torch.uint8, pin_memory=True)
+    q_h.copy_(batch.q)
+    kv_h.copy_(batch.kv)
+    fn = entry(lib, wl.store)
+    s_in, s_k, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    bounds = np.linspace(0, wl.T, chunks + 1).astype(np.int64)
+    h2d = q_h.numel() * 2 + kv_h.numel() * 2 + pos_h.numel() * 8 + sl_h.numel() * 8
+    d2h = q_h.numel() * 2 + cache_h.numel()
+
+    def step():
+        done_in, done_k = [], []
+        for c in range(chunks):
+            a, b = int(bounds[c]), int(bounds[c + 1])
+            with torch.cuda.stream(s_in):
+                batch.q[a:b].copy_(q_h[a:b], non_blocking=True)
+                batch.kv[a:b].copy_(kv_h[a:b], non_blocking=True)
+                batch.pos[a:b].copy_(pos_h[a:b], non_blocking=True)
+                batch.slots[a:b].copy_(sl_h[a:b], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(s_in)
+                done_in.append(ev)
+            s_k.wait_event(done_in[c])
+            st = fn(batch.q[a:b].data_ptr(), batch.kv[a:b].data_ptr(), batch.w.data_ptr(),
+                    batch.pos[a:b].data_ptr(), batch.cs.data_ptr(), wl.max_position,
+                    batch.slots[a:b].data_ptr(), batch.cache.data_ptr(), wl.num_blocks,
+                    wl.block_size, b - a, wl.H, wl.eps, batch.err.data_ptr(), s_k.cuda_stream)
+            if st != 0:
+                raise RuntimeError(f"launch failed with status {st}")
+            ev = torch.cuda.Event()
+            ev.record(s_k)
+            done_k.append(ev)
+            s_out.wait_event(ev)
+            with torch.cuda.stream(s_out):
+                q_h[a:b].copy_(batch.q[a:b], non_blocking=True)
+        with torch.cuda.stream(s_out):
+            cache_h.copy_(batch.cache, non_blocking=True)
+        # the next step's uploads must not overwrite device q before its download
+        s_in.wait_stream(s_out)
+
+    step()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize(dev)
+    dt = (time.perf_counter() - t0) / steps
+    return batch.bytes / dt / 1e9, h2d, d2h, dt
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+
+class OracleSample:
+    """Tokens [t0, t0 + n) of a workload, generated once on the host, for timing the
+    oracle: all q heads and the KV row of each token, cache writes included."""
+
+    def __init__(self, wl: configs.Workload, n_tokens: int, t0: int = 0):
+        t1 = min(wl.T, t0 + n_tokens)
+        self.wl = wl
+        self.q = configs.q_bits(wl, t0, t1).reshape(t1 - t0, wl.H, 512)
+        self.kv = configs.kv_bits(wl, t0, t1).reshape(t1 - t0, 512)
+        self.pos = wl.positions()[t0:t1]
+        self.sl = wl.slot_mapping()[t0:t1]
+        self.w = configs.weight_bits(wl)
+        self.cs = configs.cos_sin(wl)
+        self.n = t1 - t0
+        self.bytes = (self.n * (2 * wl.H * 1024 + 1024 + 16) + int((self.sl >= 0).sum()) *
+                      (584 if wl.store == "fp8" else 1024) + int(np.unique(self.pos).size) * 256
+                      + 1024)
+
+    def run(self, n_threads: int = 0) -> float:
+        """Seconds for one oracle pass over the sample (on a fresh copy of q)."""
+        import oracle
+        wl = self.wl
+        q = self.q.copy()
+        cache = np.zeros(configs.cache_bytes(wl), np.uint8)
+        start = time.perf_counter()
+        oracle.qnorm_rope_kv_insert(wl.store, q, self.kv, self.w, self.pos, self.cs, self.sl,
+                                    cache, wl.num_blocks, wl.block_size, wl.eps,
+                                    n_threads=n_threads)
+        return time.perf_counter() - start
+
+
+def _sample_tokens_for(wl: configs.Workload, seconds: float) -> int:
+    probe = OracleSample(wl, 16)
+    per_tok = max(probe.run() / probe.n, 1e-7)
+    return int(max(1, min(wl.T, seconds / per_tok)))
+
+
+def cpu_baseline(wl: configs.Workload, seconds: float = 5.0):
+    cores = os.cpu_count() or 1
+    sample = OracleSample(wl, _sample_tokens_for(wl, seconds))
+    dt = sample.run()
+    return {"value": round(sample.bytes / dt / 1e9, 4), "unit": "GB/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"first {sample.n} tokens of {wl.name} ({wl.T}x{wl.H}), all heads + KV "
+                      f"rows, {dt:.1f} s on {cores} threads",
+            "tokens_per_s": round(sample.n / dt, 1)}
+
+
+# ------------------------------------------------------------------ arms
+
+def run_reference(args):
+    """The oracle, as it stands, on the host cores: each step is one pass over a bounded
+    token sample of the workload, sized so warm-up + steps take about two minutes."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    wl = configs.WORKLOADS[args.workload]
+    cores = os.cpu_count() or 1
+    n = _sample_tokens_for(wl, 120.0 / max(1, args.steps + args.warmup))
+    sample = OracleSample(wl, n)
+    times = []
+    for i in range(args.warmup + args.steps):
+        dt = sample.run()
+        if i >= args.warmup:
+            times.append(dt)
+    mean = statistics.mean(times)
+    value = sample.bytes / mean / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(mean * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "store": wl.store,
+                       "step_sample_tokens": sample.n},
+            "tokens_per_s": round(sample.n / mean, 1),
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
+                             "kind": "oracle",
+                             "sample": f"first {sample.n} tokens of {wl.name} per step, all "
+                                       f"heads + KV rows"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+
+    import kv_norm_rope_gb300 as k
+
+    rank, world, local_rank = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    lib = k.lib()
+    wl = rank_workload(configs.WORKLOADS[args.workload], rank)
+
+    kac_before = known_answer_check() if rank == 0 else "skipped"
+    copy_1g = copy_ceiling_gbs(dev, 1 << 30)
+    copy_512m = copy_ceiling_gbs(dev, 1 << 29)
+    batch = DeviceBatch(wl, dev)
+    stream = torch.cuda.current_stream(dev)
+    fn = entry(lib, wl.store)
+    call_args = batch.args(stream.cuda_stream)
+    for _ in range(args.warmup):
+        st = fn(*call_args)
+        if st != 0:
+            raise RuntimeError(f"launch failed: {k.status_string(st)}")
+    torch.cuda.synchronize(dev)
+    if int(batch.err.item()) != 0:
+        raise RuntimeError(f"device error bits {int(batch.err.item())}")
+
+    sampler = ClockSampler(bus_id_of(local_rank)) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        events[2 * i].record(stream)
+        fn(*call_args)
+        events[2 * i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop() if sampler else None
+    per_launch = [events[2 * i].elapsed_time(events[2 * i + 1]) / 1e3 for i in range(args.steps)]
+    region = events[0].elapsed_time(events[-1]) / 1e3
+    t_step = max_over_ranks(region / args.steps, world, dev)
+    total_bytes = sum_over_ranks(float(batch.bytes), world, dev)
+    total_tokens = sum_over_ranks(float(wl.T), world, dev)
+    mean_launch = statistics.mean(per_launch)
+
+    e2e = None
+    if not args.no_e2e:
+        e2e_gbs, h2d, d2h, e2e_dt = e2e_run(batch, lib, args.e2e_steps)
+        e2e_dt = max_over_ranks(e2e_dt, world, dev)
+        e2e = {"value": round(total_bytes / e2e_dt / 1e9, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "tokens_per_s": round(total_tokens / e2e_dt, 1),
+               "chunks": 8, "ms_per_step": round(e2e_dt * 1e3, 3)}
+    kac_after = known_answer_check() if rank == 0 else "skipped"
+    if rank != 0:
+        return 0
+
+    peak, peak_kind = measured_peaks()
+    achieved = batch.bytes / mean_launch / 1e9
+    value = total_bytes / t_step / 1e9
+    plan = k.launch_plan(wl.T, wl.H, torch.cuda.get_device_properties(dev).multi_processor_count,
+                         4)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_step * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": wl.name.split("@")[0], "T": wl.T, "H": wl.H, "store": wl.store,
+                   "num_blocks": wl.num_blocks, "block_size": wl.block_size,
+                   "bytes_per_step": batch.bytes, "l2": "inputs larger than L2 (q 17.2 GB)"
+                   if wl.T * wl.H * 1024 > (1 << 30) else "inputs within L2 size",
+                   "io": "bf16 in; bf16 q, e4m3+ue8m0+bf16 cache out",
+                   "variant": "stream" if plan.variant == k.VARIANT_STREAM else "small",
+                   "parallelism": f"dp{world}" if world > 1 else "single"},
+        "tokens_per_s": round(total_tokens / t_step, 1),
+        "frac_of_copy_ceiling": round(value / world / copy_1g, 4),
+        "frac_of_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
+        "copy_ceiling_gbs": {"1GiB": round(copy_1g, 1), "512MiB": round(copy_512m, 1)},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "launch_ms_mean": round(mean_launch * 1e3, 4),
+                     "launch_ms_median": round(statistics.median(per_launch) * 1e3, 4)},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "wall_s_timed": round(wall, 3),
+        "known_answer": {"before": kac_before, "after": kac_after},
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(configs.WORKLOADS[args.workload], args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(configs.WORKLOADS), default="stress")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=5.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,184 @@
+/*
+ * dsv4kv.h -- C ABI of the fused DeepSeek-V4 attention-input step for GB300
+ * (sm_103a): per token, RMS-normalise every 512-wide query head and rotate its
+ * trailing 64 dims in place; RMS-normalise the token's 512-wide latent KV row
+ * with a learned weight, rotate its trailing 64 dims, and write it into a
+ * paged KV cache, either quantised (448 E4M3 + 7 UE8M0 exponents + 64 bf16)
+ * or as 512 bf16.
+ *
+ * Sources restated here:
+ *  - FlagGems-vllm PR #684, "fused_deepseek_v4_qnorm_rope_kv_rope_quant_insert
+ *    backends": section "T-Head PPU-ZW810E" (the operator rewrites q in place);
+ *    section "Ascend 910B" (a weightless q RMSNorm, 256 bytes of cos/sin per
+ *    position shared by all heads of a token, mixed negative slots that write
+ *    nothing); section 'What "as shipped" would give' (seven per-block
+ *    exponents per token in the FP8 cache).
+ *  - SGLang PR #33358, "DSv4 flashmla norm-rope" (section "Motivation": RMSNorm
+ *    over head_dim 512 with a weight, RoPE on the trailing 64 dims, paged-cache
+ *    store with an FP8-UE8M0 path and a bf16 path; section "Accuracy Tests":
+ *    448 E4M3 bytes, 7 per-64-group exponents, bf16 rope tail).
+ *
+ * Conventions for every entry point:
+ *  - Pointers marked (device) are CUDA device pointers; the caller owns all
+ *    memory.  The library allocates nothing, keeps no state between calls and
+ *    takes no locks.
+ *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = the
+ *    legacy default stream).  A DSV4_OK return means the launch was accepted,
+ *    not that it has finished.
+ *  - Host-side argument checks run before anything is enqueued; a non-OK
+ *    status means nothing was launched and no buffer was touched.
+ *  - Conditions that need device data (a slot or a position out of range) are
+ *    reported by OR-ing DSV4_DEVERR_* bits into *device_error (device int32,
+ *    may be NULL) and skipping the affected writes.  Nothing traps, asserts or
+ *    waits on the device.
+ *  - Preconditions that are not checked: non-negative slots are distinct (if
+ *    two tokens share a slot, which one's row lands is unspecified); q does
+ *    not overlap kv, the cache or the metadata arrays; inputs are finite and
+ *    sum(x^2) of a row stays below 3.4e38.
+ */
+#ifndef DSV4KV_H
+#define DSV4KV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    DSV4_OK = 0,
+    DSV4_ERR_NULL = 1,   /* a required pointer is NULL */
+    DSV4_ERR_SHAPE = 2,  /* a size is out of range */
+    DSV4_ERR_ALIGN = 3,  /* a pointer is not aligned as documented */
+    DSV4_ERR_VALUE = 4,  /* eps negative or not finite; unknown store mode or variant */
+    DSV4_ERR_CUDA = 5    /* the CUDA runtime reported an error while launching */
+} dsv4_status;
+
+enum {
+    DSV4_HEAD_DIM = 512,        /* q head and latent KV width */
+    DSV4_ROPE_DIM = 64,         /* trailing rotated dims 448..511, GPT-J interleaved pairs */
+    DSV4_NOPE_DIM = 448,        /* leading dims quantised to E4M3 on the FP8 path */
+    DSV4_QUANT_BLOCK = 64,      /* elements per UE8M0 exponent */
+    DSV4_NUM_QUANT_BLOCKS = 7,
+    DSV4_FP8_DATA_BYTES = 576,  /* 448 E4M3 + 64 bf16 */
+    DSV4_FP8_SCALE_BYTES = 8,   /* 7 UE8M0 bytes + 1 zero pad byte */
+    DSV4_FP8_SLOT_BYTES = 584,
+    DSV4_BF16_SLOT_BYTES = 1024
+};
+
+/* bits OR-ed into *device_error */
+enum {
+    DSV4_DEVERR_SLOT_RANGE = 1, /* slot_mapping[t] >= num_blocks*block_size: cache row not written */
+    DSV4_DEVERR_POS_RANGE = 2   /* positions[t] < 0 or >= max_position: token not written at all */
+};
+
+/* store modes and launch variants of dsv4_qnorm_rope_kv_insert_variant */
+enum { DSV4_STORE_FP8 = 0, DSV4_STORE_BF16 = 1 };
+enum {
+    DSV4_VARIANT_AUTO = 0,    /* pick from the row count and the SM count (below) */
+    DSV4_VARIANT_SMALL = 1,   /* one row per warp, 2-warp CTAs, one wave: small batches */
+    DSV4_VARIANT_STREAM = 2   /* persistent CTAs sized to the SMs, several rows in flight per warp */
+};
+
+/*
+ * Fused q-norm + RoPE (in place) and KV norm + RoPE + FP8 quant + paged insert.
+ *
+ *  q              (device) bf16 [num_tokens, num_heads, 512], contiguous, read and
+ *                 rewritten in place: q[t,h,:] = bf16( rot( x * r ) ), with
+ *                 x = q[t,h,:], r = 1/sqrt(sum(x^2)/512 + eps), no weight.
+ *                 16-byte aligned.
+ *  kv             (device) bf16 [num_tokens, 512], contiguous, read only. 16-byte aligned.
+ *  kv_norm_weight (device) bf16 [512].  v = x * r * w for the KV row.  16-byte aligned.
+ *  positions      (device) int64 [num_tokens]: row of cos_sin_cache for token t.
+ *  cos_sin_cache  (device) fp32 [max_position, 64]: columns 0..31 = cos of the 32
+ *                 pair angles, 32..63 = their sin.  Pair i = dims (448+2i, 449+2i)
+ *                 turns as (a, b) -> (a*cos - b*sin, b*cos + a*sin).  16-byte aligned.
+ *  slot_mapping   (device) int64 [num_tokens]: slot = block*block_size + offset;
+ *                 a negative slot writes no cache row (q is still rewritten).
+ *  kv_cache       (device) uint8, num_blocks * block_size * 584 bytes.  Block b
+ *                 occupies [b*bs*584, (b+1)*bs*584); inside it, slot offset o has
+ *                   data  at b*bs*584 + o*576         : 448 E4M3 bytes of dims 0..447,
+ *                                                       then dims 448..511 as 64
+ *                                                       little-endian bf16,
+ *                   scale at b*bs*584 + bs*576 + o*8  : UE8M0 bytes e_0..e_6 of the
+ *                                                       seven 64-dim blocks, then 0.
+ *                 e_b = s_b + 127 with s_b the smallest integer such that
+ *                 max|v| over block b <= 448 * 2^s_b (clamped to [-127, 127]; an
+ *                 all-zero block gives e_b = 0); payload = E4M3_rn(v * 2^-s_b).
+ *                 8-byte aligned.  Bytes of slots that are not written keep
+ *                 their previous contents.
+ *  num_blocks, block_size   cache geometry (>= 1 each).
+ *  num_tokens     T >= 0 (T == 0 returns DSV4_OK and launches nothing).
+ *  num_heads      H >= 1.
+ *  eps            >= 0 and finite; added to mean(x^2) inside the root.
+ *  device_error   (device, nullable) int32; DSV4_DEVERR_* bits are OR-ed in.
+ *  stream         cudaStream_t.
+ * Returns a dsv4_status.
+ */
+int dsv4_qnorm_rope_kv_quant_insert(void *q, const void *kv, const void *kv_norm_weight,
+                                    const int64_t *positions, const float *cos_sin_cache,
+                                    int64_t max_position, const int64_t *slot_mapping,
+                                    uint8_t *kv_cache, int64_t num_blocks, int32_t block_size,
+                                    int64_t num_tokens, int32_t num_heads, float eps,
+                                    int32_t *device_error, void *stream);
+
+/*
+ * As above, but the cache holds bf16 rows: kv_cache (device) bf16
+ * [num_blocks, block_size, 512], 16-byte aligned; slot s gets bf16(rot(v))
+ * for all 512 dims (SGLang PR #33358, "Motivation": the kBf16Store path).
+ */
+int dsv4_qnorm_rope_kv_bf16_insert(void *q, const void *kv, const void *kv_norm_weight,
+                                   const int64_t *positions, const float *cos_sin_cache,
+                                   int64_t max_position, const int64_t *slot_mapping,
+                                   void *kv_cache, int64_t num_blocks, int32_t block_size,
+                                   int64_t num_tokens, int32_t num_heads, float eps,
+                                   int32_t *device_error, void *stream);
+
+/*
+ * Either store mode with an explicit launch variant (DSV4_VARIANT_*).  Every
+ * variant computes bit-identical outputs: each token's rows depend only on
+ * that token's inputs (SGLang PR #33358, "Modifications": the grouping of
+ * tokens into blocks does not change a token's bits).  Used by tests that
+ * exercise each variant and by benchmarks.
+ */
+int dsv4_qnorm_rope_kv_insert_variant(int store_mode, int variant, void *q, const void *kv,
+                                      const void *kv_norm_weight, const int64_t *positions,
+                                      const float *cos_sin_cache, int64_t max_position,
+                                      const int64_t *slot_mapping, void *kv_cache,
+                                      int64_t num_blocks, int32_t block_size, int64_t num_tokens,
+                                      int32_t num_heads, float eps, int32_t *device_error,
+                                      void *stream);
+
+/* Launch plan of a call (pure host arithmetic, no CUDA call). */
+typedef struct {
+    int32_t variant;        /* DSV4_VARIANT_SMALL or DSV4_VARIANT_STREAM */
+    int32_t threads;        /* threads per CTA */
+    int64_t ctas;           /* grid size */
+    int32_t rows_per_warp;  /* rows each warp loads together */
+    int64_t rows;           /* num_tokens * (num_heads + 1) work rows */
+} dsv4_plan;
+
+/*
+ * Fill *plan for T tokens, H heads on a GPU with sm_count SMs where
+ * ctas_per_sm CTAs of the streaming kernel fit per SM.  variant AUTO picks
+ * SMALL when the rows would not give every warp slot of the GPU at least a
+ * full group of rows, else STREAM (SGLang PR #33358, "Modifications" item 3:
+ * a grid-starved multi-token layout loses at small N).  Returns a dsv4_status.
+ */
+int dsv4_launch_plan(int64_t num_tokens, int32_t num_heads, int32_t sm_count,
+                     int32_t ctas_per_sm, int32_t variant, dsv4_plan *plan);
+
+/* Bytes of an FP8 cache of num_blocks x block_size slots: num_blocks*block_size*584. */
+size_t dsv4_fp8_cache_bytes(int64_t num_blocks, int32_t block_size);
+/* Bytes of a bf16 cache: num_blocks*block_size*1024. */
+size_t dsv4_bf16_cache_bytes(int64_t num_blocks, int32_t block_size);
+
+/* Static string naming a dsv4_status value ("unknown status" otherwise). */
+const char *dsv4_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSV4KV_H */

@@ -1,0 +1,214 @@
+"""kv_norm_rope_gb300: Python binding of libdsv4kv, the GB300 (sm_103a) library for the
+fused DeepSeek-V4 attention-input step (q RMSNorm + RoPE in place; KV RMSNorm with a
+weight + RoPE + UE8M0/E4M3 quantisation + paged-cache insert).
+
+Argument marshalling only: every step runs in the CUDA kernels of ``csrc/``, reached
+through the C ABI declared in ``include/dsv4kv.h``.  There is no CPU fallback: if the
+shared library is missing and cannot be built, importing the entry points raises.
+PyTorch supplies device memory and the current stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import tempfile
+from concurrent.futures import ThreadPoolExecutor
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_ROOT = os.path.dirname(_HERE)
+_CSRC = os.path.join(_HERE, "csrc")
+_INCLUDE = os.path.join(_ROOT, "include")
+LIB_PATH = os.path.join(_HERE, "libdsv4kv.so")
+_SOURCES = ["qnorm_rope_kv_insert.cu", "api.cpp"]
+_HEADERS = [os.path.join(_INCLUDE, "dsv4kv.h"), os.path.join(_CSRC, "launch.h")]
+NVCC_ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+# status codes and constants (mirrors include/dsv4kv.h)
+OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_VALUE, ERR_CUDA = range(6)
+DEVERR_SLOT_RANGE, DEVERR_POS_RANGE = 1, 2
+STORE_FP8, STORE_BF16 = 0, 1
+VARIANT_AUTO, VARIANT_SMALL, VARIANT_STREAM = 0, 1, 2
+FP8_SLOT_BYTES, BF16_SLOT_BYTES = 584, 1024
+
+EXPORTS = ("dsv4_qnorm_rope_kv_quant_insert", "dsv4_qnorm_rope_kv_bf16_insert",
+           "dsv4_qnorm_rope_kv_insert_variant", "dsv4_launch_plan", "dsv4_fp8_cache_bytes",
+           "dsv4_bf16_cache_bytes", "dsv4_status_string")
+
+
+class Dsv4Error(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+        self.status = status
+
+
+def _nvcc() -> str:
+    cand = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "bin", "nvcc")
+    return cand if os.path.exists(cand) else "nvcc"
+
+
+def _stale() -> bool:
+    if not os.path.exists(LIB_PATH):
+        return True
+    t = os.path.getmtime(LIB_PATH)
+    deps = [os.path.join(_CSRC, s) for s in _SOURCES] + _HEADERS
+    return any(os.path.getmtime(d) > t for d in deps)
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile csrc/ into libdsv4kv.so (in-tree) for sm_103a with nvcc.
+
+    The translation units are compiled in parallel, then linked with the static
+    CUDA runtime, so the library needs only the driver at run time.
+    """
+    if not force and not _stale():
+        return LIB_PATH
+    bdir = tempfile.mkdtemp(prefix="dsv4kv_build_", dir=_HERE)
+    flags = NVCC_ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
+                         "-I", _INCLUDE, "-I", _CSRC]
+    if verbose:
+        flags += ["-Xptxas", "-v"]
+
+    def compile_one(src):
+        obj = os.path.join(bdir, os.path.basename(src) + ".o")
+        subprocess.run([_nvcc()] + flags + ["-c", os.path.join(_CSRC, src), "-o", obj], check=True)
+        return obj
+
+    with ThreadPoolExecutor(len(_SOURCES)) as ex:
+        objs = list(ex.map(compile_one, _SOURCES))
+    tmp = os.path.join(bdir, "libdsv4kv.so")
+    subprocess.run([_nvcc()] + NVCC_ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs,
+                   check=True)
+    os.replace(tmp, LIB_PATH)
+    for f in objs:
+        os.remove(f)
+    os.rmdir(bdir)
+    return LIB_PATH
+
+
+_lib = None
+
+
+def lib():
+    """The loaded libdsv4kv (built first if missing or older than its sources)."""
+    global _lib
+    if _lib is None:
+        path = build()
+        L = ctypes.CDLL(path)
+        vp, i64, i32, f32, c_int = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32,
+                                    ctypes.c_float, ctypes.c_int)
+        common = [vp, vp, vp, vp, vp, i64, vp, vp, i64, i32, i64, i32, f32, vp, vp]
+        L.dsv4_qnorm_rope_kv_quant_insert.argtypes = common
+        L.dsv4_qnorm_rope_kv_quant_insert.restype = c_int
+        L.dsv4_qnorm_rope_kv_bf16_insert.argtypes = common
+        L.dsv4_qnorm_rope_kv_bf16_insert.restype = c_int
+        L.dsv4_qnorm_rope_kv_insert_variant.argtypes = [c_int, c_int] + common
+        L.dsv4_qnorm_rope_kv_insert_variant.restype = c_int
+        L.dsv4_launch_plan.argtypes = [i64, i32, i32, i32, i32, ctypes.POINTER(Plan)]
+        L.dsv4_launch_plan.restype = c_int
+        L.dsv4_fp8_cache_bytes.argtypes = [i64, i32]
+        L.dsv4_fp8_cache_bytes.restype = ctypes.c_size_t
+        L.dsv4_bf16_cache_bytes.argtypes = [i64, i32]
+        L.dsv4_bf16_cache_bytes.restype = ctypes.c_size_t
+        L.dsv4_status_string.argtypes = [c_int]
+        L.dsv4_status_string.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [("variant", ctypes.c_int32), ("threads", ctypes.c_int32), ("ctas", ctypes.c_int64),
+                ("rows_per_warp", ctypes.c_int32), ("rows", ctypes.c_int64)]
+
+
+def status_string(status: int) -> str:
+    return lib().dsv4_status_string(status).decode()
+
+
+def launch_plan(num_tokens: int, num_heads: int, sm_count: int, ctas_per_sm: int,
+                variant: int = VARIANT_AUTO) -> Plan:
+    plan = Plan()
+    st = lib().dsv4_launch_plan(num_tokens, num_heads, sm_count, ctas_per_sm, variant,
+                                ctypes.byref(plan))
+    if st != OK:
+        raise Dsv4Error(st, "dsv4_launch_plan")
+    return plan
+
+
+def fp8_cache_bytes(num_blocks: int, block_size: int) -> int:
+    return int(lib().dsv4_fp8_cache_bytes(num_blocks, block_size))
+
+
+def bf16_cache_bytes(num_blocks: int, block_size: int) -> int:
+    return int(lib().dsv4_bf16_cache_bytes(num_blocks, block_size))
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream_handle(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _shape_args(q, kv, positions, cos_sin_cache):
+    T = int(positions.shape[0])
+    H = int(q.shape[-2]) if q.dim() == 3 else int(q.numel() // max(T, 1) // 512)
+    return T, H, int(cos_sin_cache.shape[0])
+
+
+def insert(store_mode: int, q, kv, kv_norm_weight, positions, cos_sin_cache, slot_mapping,
+           kv_cache, num_blocks: int, block_size: int, eps: float, device_error=None,
+           stream=None, variant: int = VARIANT_AUTO, num_heads: int | None = None) -> None:
+    """Enqueue the fused step on ``stream`` (default: torch's current stream).
+
+    q: bf16 [T, H, 512] (rewritten in place); kv: bf16 [T, 512]; kv_norm_weight: bf16
+    [512]; positions, slot_mapping: int64 [T]; cos_sin_cache: fp32 [max_position, 64];
+    kv_cache: uint8 (FP8, num_blocks*block_size*584 bytes) or bf16 [num_blocks,
+    block_size, 512]; device_error: optional int32 [1].  Raises Dsv4Error on a
+    rejected call.
+    """
+    T, H, max_pos = _shape_args(q, kv, positions, cos_sin_cache)
+    if num_heads is not None:
+        H = num_heads
+    st = lib().dsv4_qnorm_rope_kv_insert_variant(
+        store_mode, variant, _ptr(q), _ptr(kv), _ptr(kv_norm_weight), _ptr(positions),
+        _ptr(cos_sin_cache), max_pos, _ptr(slot_mapping), _ptr(kv_cache), num_blocks,
+        block_size, T, H, eps, _ptr(device_error), _stream_handle(stream))
+    if st != OK:
+        raise Dsv4Error(st, "dsv4_qnorm_rope_kv_insert")
+
+
+def qnorm_rope_kv_quant_insert(q, kv, kv_norm_weight, positions, cos_sin_cache, slot_mapping,
+                               kv_cache, num_blocks, block_size, eps, device_error=None,
+                               stream=None) -> None:
+    """dsv4_qnorm_rope_kv_quant_insert: FP8 (448 E4M3 + 7 UE8M0 + 64 bf16) cache rows."""
+    T, H, max_pos = _shape_args(q, kv, positions, cos_sin_cache)
+    st = lib().dsv4_qnorm_rope_kv_quant_insert(
+        _ptr(q), _ptr(kv), _ptr(kv_norm_weight), _ptr(positions), _ptr(cos_sin_cache), max_pos,
+        _ptr(slot_mapping), _ptr(kv_cache), num_blocks, block_size, T, H, eps,
+        _ptr(device_error), _stream_handle(stream))
+    if st != OK:
+        raise Dsv4Error(st, "dsv4_qnorm_rope_kv_quant_insert")
+
+
+def qnorm_rope_kv_bf16_insert(q, kv, kv_norm_weight, positions, cos_sin_cache, slot_mapping,
+                              kv_cache, num_blocks, block_size, eps, device_error=None,
+                              stream=None) -> None:
+    """dsv4_qnorm_rope_kv_bf16_insert: 512 bf16 cache rows."""
+    T, H, max_pos = _shape_args(q, kv, positions, cos_sin_cache)
+    st = lib().dsv4_qnorm_rope_kv_bf16_insert(
+        _ptr(q), _ptr(kv), _ptr(kv_norm_weight), _ptr(positions), _ptr(cos_sin_cache), max_pos,
+        _ptr(slot_mapping), _ptr(kv_cache), num_blocks, block_size, T, H, eps,
+        _ptr(device_error), _stream_handle(stream))
+    if st != OK:
+        raise Dsv4Error(st, "dsv4_qnorm_rope_kv_bf16_insert")

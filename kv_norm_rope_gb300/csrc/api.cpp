@@ -1,0 +1,216 @@
+// C-ABI layer of libdsv4kv: argument checks, launch planning, status strings.
+// Every check here runs on the host before anything is enqueued, so a rejected
+// call touches no buffer.  See include/dsv4kv.h for the contract.
+
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+
+#include "dsv4kv.h"
+#include "launch.h"
+
+namespace {
+
+bool aligned(const void *p, uintptr_t a)
+{
+    return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+
+// Per-device cache of (SM count, CTAs of the streaming kernel per SM) for the
+// two store modes: immutable properties, filled on first use.
+constexpr int kMaxDevices = 64;
+std::atomic<int32_t> g_sms[kMaxDevices];
+std::atomic<int32_t> g_ctas[kMaxDevices][2];
+
+int device_shape(int store_mode, int32_t *sms, int32_t *ctas)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return DSV4_ERR_CUDA;
+    const bool cached = dev >= 0 && dev < kMaxDevices;
+    if (cached) {
+        *sms = g_sms[dev].load(std::memory_order_relaxed);
+        *ctas = g_ctas[dev][store_mode].load(std::memory_order_relaxed);
+        if (*sms > 0 && *ctas > 0)
+            return DSV4_OK;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+        return DSV4_ERR_CUDA;
+    int c = 0;
+    if (dsv4::stream_ctas_per_sm(store_mode, &c) != DSV4_OK || c < 1)
+        return DSV4_ERR_CUDA;
+    *sms = n;
+    *ctas = c;
+    if (cached) {
+        g_sms[dev].store(n, std::memory_order_relaxed);
+        g_ctas[dev][store_mode].store(c, std::memory_order_relaxed);
+    }
+    return DSV4_OK;
+}
+
+int insert(int store_mode, int variant, void *q, const void *kv, const void *w,
+           const int64_t *positions, const float *cos_sin, int64_t max_position,
+           const int64_t *slot_mapping, void *cache, int64_t num_blocks, int32_t block_size,
+           int64_t num_tokens, int32_t num_heads, float eps, int32_t *device_error, void *stream)
+{
+    if (store_mode != DSV4_STORE_FP8 && store_mode != DSV4_STORE_BF16)
+        return DSV4_ERR_VALUE;
+    if (variant != DSV4_VARIANT_AUTO && variant != DSV4_VARIANT_SMALL &&
+        variant != DSV4_VARIANT_STREAM)
+        return DSV4_ERR_VALUE;
+    if (num_tokens < 0 || num_heads < 1 || num_blocks < 1 || block_size < 1 || max_position < 1)
+        return DSV4_ERR_SHAPE;
+    // every byte offset the kernels form must fit in int64
+    const int64_t lim = INT64_MAX / 4096;
+    if (num_tokens > lim / (int64_t(num_heads) + 1) || num_blocks > lim / block_size ||
+        max_position > lim)
+        return DSV4_ERR_SHAPE;
+    if (!(eps >= 0.0f) || !std::isfinite(eps))
+        return DSV4_ERR_VALUE;
+    if (num_tokens == 0)
+        return DSV4_OK;
+    if (!q || !kv || !w || !positions || !cos_sin || !slot_mapping || !cache)
+        return DSV4_ERR_NULL;
+    const uintptr_t cache_align = store_mode == DSV4_STORE_FP8 ? 8 : 16;
+    if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(w, 16) || !aligned(cos_sin, 16) ||
+        !aligned(cache, cache_align) || !aligned(positions, 8) || !aligned(slot_mapping, 8) ||
+        !aligned(device_error, 4))
+        return DSV4_ERR_ALIGN;
+
+    int32_t sms = 0, ctas = 0;
+    int st = device_shape(store_mode, &sms, &ctas);
+    if (st != DSV4_OK)
+        return st;
+    dsv4_plan plan;
+    st = dsv4_launch_plan(num_tokens, num_heads, sms, ctas, variant, &plan);
+    if (st != DSV4_OK)
+        return st;
+
+    dsv4::LaunchArgs a;
+    a.q = static_cast<uint16_t *>(q);
+    a.kv = static_cast<const uint16_t *>(kv);
+    a.w = static_cast<const uint16_t *>(w);
+    a.pos = positions;
+    a.cs = cos_sin;
+    a.max_pos = max_position;
+    a.slot = slot_mapping;
+    a.cache = static_cast<uint8_t *>(cache);
+    a.num_slots = num_blocks * int64_t(block_size);
+    a.block_size = block_size;
+    a.num_heads = num_heads;
+    a.num_tokens = num_tokens;
+    a.eps = eps;
+    a.err = device_error;
+    return dsv4::launch(store_mode, plan, a, static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+int dsv4_launch_plan(int64_t num_tokens, int32_t num_heads, int32_t sm_count, int32_t ctas_per_sm,
+                     int32_t variant, dsv4_plan *plan)
+{
+    if (!plan)
+        return DSV4_ERR_NULL;
+    if (num_tokens < 0 || num_heads < 1 || sm_count < 1 || ctas_per_sm < 1)
+        return DSV4_ERR_SHAPE;
+    if (num_tokens > (INT64_MAX / 4096) / (int64_t(num_heads) + 1))
+        return DSV4_ERR_SHAPE;
+    const int64_t rows = num_tokens * (int64_t(num_heads) + 1);
+    const int stream_warps = dsv4::kStreamThreads / 32;
+    const int64_t warp_slots = int64_t(sm_count) * ctas_per_sm * stream_warps;
+    if (variant == DSV4_VARIANT_AUTO)
+        variant = rows < warp_slots * dsv4::kStreamRowsPerWarp ? DSV4_VARIANT_SMALL
+                                                               : DSV4_VARIANT_STREAM;
+    plan->rows = rows;
+    if (variant == DSV4_VARIANT_SMALL) {
+        const int warps = dsv4::kSmallThreads / 32;
+        plan->variant = DSV4_VARIANT_SMALL;
+        plan->threads = dsv4::kSmallThreads;
+        plan->rows_per_warp = 1;
+        plan->ctas = rows > 0 ? (rows + warps - 1) / warps : 1;
+        if (plan->ctas > INT32_MAX)
+            return DSV4_ERR_SHAPE;
+    } else if (variant == DSV4_VARIANT_STREAM) {
+        const int64_t groups = (rows + dsv4::kStreamRowsPerWarp - 1) / dsv4::kStreamRowsPerWarp;
+        const int64_t need = (groups + stream_warps - 1) / stream_warps;
+        const int64_t resident = int64_t(sm_count) * ctas_per_sm;
+        plan->variant = DSV4_VARIANT_STREAM;
+        plan->threads = dsv4::kStreamThreads;
+        plan->rows_per_warp = dsv4::kStreamRowsPerWarp;
+        plan->ctas = need < resident ? (need > 0 ? need : 1) : resident;
+    } else {
+        return DSV4_ERR_VALUE;
+    }
+    return DSV4_OK;
+}
+
+int dsv4_qnorm_rope_kv_quant_insert(void *q, const void *kv, const void *kv_norm_weight,
+                                    const int64_t *positions, const float *cos_sin_cache,
+                                    int64_t max_position, const int64_t *slot_mapping,
+                                    uint8_t *kv_cache, int64_t num_blocks, int32_t block_size,
+                                    int64_t num_tokens, int32_t num_heads, float eps,
+                                    int32_t *device_error, void *stream)
+{
+    return insert(DSV4_STORE_FP8, DSV4_VARIANT_AUTO, q, kv, kv_norm_weight, positions,
+                  cos_sin_cache, max_position, slot_mapping, kv_cache, num_blocks, block_size,
+                  num_tokens, num_heads, eps, device_error, stream);
+}
+
+int dsv4_qnorm_rope_kv_bf16_insert(void *q, const void *kv, const void *kv_norm_weight,
+                                   const int64_t *positions, const float *cos_sin_cache,
+                                   int64_t max_position, const int64_t *slot_mapping,
+                                   void *kv_cache, int64_t num_blocks, int32_t block_size,
+                                   int64_t num_tokens, int32_t num_heads, float eps,
+                                   int32_t *device_error, void *stream)
+{
+    return insert(DSV4_STORE_BF16, DSV4_VARIANT_AUTO, q, kv, kv_norm_weight, positions,
+                  cos_sin_cache, max_position, slot_mapping, kv_cache, num_blocks, block_size,
+                  num_tokens, num_heads, eps, device_error, stream);
+}
+
+int dsv4_qnorm_rope_kv_insert_variant(int store_mode, int variant, void *q, const void *kv,
+                                      const void *kv_norm_weight, const int64_t *positions,
+                                      const float *cos_sin_cache, int64_t max_position,
+                                      const int64_t *slot_mapping, void *kv_cache,
+                                      int64_t num_blocks, int32_t block_size, int64_t num_tokens,
+                                      int32_t num_heads, float eps, int32_t *device_error,
+                                      void *stream)
+{
+    return insert(store_mode, variant, q, kv, kv_norm_weight, positions, cos_sin_cache,
+                  max_position, slot_mapping, kv_cache, num_blocks, block_size, num_tokens,
+                  num_heads, eps, device_error, stream);
+}
+
+size_t dsv4_fp8_cache_bytes(int64_t num_blocks, int32_t block_size)
+{
+    if (num_blocks < 1 || block_size < 1)
+        return 0;
+    return size_t(num_blocks) * size_t(block_size) * DSV4_FP8_SLOT_BYTES;
+}
+
+size_t dsv4_bf16_cache_bytes(int64_t num_blocks, int32_t block_size)
+{
+    if (num_blocks < 1 || block_size < 1)
+        return 0;
+    return size_t(num_blocks) * size_t(block_size) * DSV4_BF16_SLOT_BYTES;
+}
+
+const char *dsv4_status_string(int status)
+{
+    switch (status) {
+    case DSV4_OK: return "ok";
+    case DSV4_ERR_NULL: return "null pointer argument";
+    case DSV4_ERR_SHAPE: return "size out of range";
+    case DSV4_ERR_ALIGN: return "misaligned pointer argument";
+    case DSV4_ERR_VALUE: return "invalid value (eps, store mode or variant)";
+    case DSV4_ERR_CUDA: return "CUDA runtime error at launch";
+    default: return "unknown status";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,40 @@
+// Internal interface between the C-ABI layer (api.cpp) and the kernels
+// (qnorm_rope_kv_insert.cu).  Not installed; not part of the ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dsv4kv.h"
+
+namespace dsv4 {
+
+// Rows each warp of the streaming variant loads before it computes any.
+constexpr int kStreamRowsPerWarp = 2;
+constexpr int kStreamThreads = 256;
+constexpr int kSmallThreads = 64;
+
+struct LaunchArgs {
+    uint16_t *q;
+    const uint16_t *kv;
+    const uint16_t *w;
+    const int64_t *pos;
+    const float *cs;
+    int64_t max_pos;
+    const int64_t *slot;
+    uint8_t *cache;
+    int64_t num_slots;
+    int32_t block_size;
+    int32_t num_heads;
+    int64_t num_tokens;
+    float eps;
+    int32_t *err;
+};
+
+// CTAs of the streaming kernel for `store_mode` that fit on one SM.
+int stream_ctas_per_sm(int store_mode, int *ctas_per_sm);
+
+// Enqueue the kernel described by `plan` on `stream`; returns a dsv4_status.
+int launch(int store_mode, const dsv4_plan &plan, const LaunchArgs &args, cudaStream_t stream);
+
+}  // namespace dsv4

@@ -77,9 +77,13 @@ def qnorm_rope_kv_insert(store: str, q: np.ndarray | None, kv: np.ndarray | None
         H = q.shape[-2] if H is None else H
     else:
         H = 0
-    assert cache.dtype == np.uint8 and cache.flags.c_contiguous
     row = FP8_SLOT_BYTES if store == "fp8" else 1024
-    assert cache.size == num_blocks * block_size * row
+    if cache is not None:
+        assert cache.dtype == np.uint8 and cache.flags.c_contiguous
+        assert cache.size == num_blocks * block_size * row
+    else:
+        assert kv is None, "a cache image is needed when kv rows are given"
+
     w = _c(w, np.uint16)
     pos = _c(positions, np.int64)
     cs = _c(cos_sin, np.float32)
@@ -90,7 +94,8 @@ def qnorm_rope_kv_insert(store: str, q: np.ndarray | None, kv: np.ndarray | None
         kvp = kv.ctypes.data
     return int(lib.oracle_qnorm_rope_kv_insert(
         1 if store == "bf16" else 0, q.ctypes.data if q is not None else None, kvp, w.ctypes.data,
-        pos.ctypes.data, cs.ctypes.data, cs.shape[0], sl.ctypes.data, cache.ctypes.data,
+        pos.ctypes.data, cs.ctypes.data, cs.shape[0], sl.ctypes.data,
+        cache.ctypes.data if cache is not None else None,
         num_blocks, block_size, T, H, eps, n_threads))
 
 

@@ -1,0 +1,137 @@
+"""C-ABI tests that need no GPU: the library loads, exports every function the header
+declares, rejects bad arguments on the host before touching CUDA, plans launches as
+documented, and has no CPU fallback."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+import kv_norm_rope_gb300 as k
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "dsv4kv.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dsv4_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declarations_are_exported():
+    names = _declared_functions()
+    assert names == sorted(k.EXPORTS)
+    lib = k.lib()
+    for n in names:
+        assert hasattr(lib, n)
+
+
+def test_status_strings():
+    assert k.status_string(k.OK) == "ok"
+    assert "align" in k.status_string(k.ERR_ALIGN)
+    assert k.status_string(99) == "unknown status"
+
+
+def test_cache_bytes():
+    assert k.fp8_cache_bytes(1024, 64) == 1024 * 64 * 584
+    assert k.bf16_cache_bytes(2048, 64) == 2048 * 64 * 1024
+    assert k.fp8_cache_bytes(0, 64) == 0
+
+
+# fake device pointers: never dereferenced, because every call below is rejected
+# (or returns early) on the host
+A = 1 << 20
+
+
+def _call(store=0, variant=0, q=A, kv=A, w=A, pos=A, cs=A, max_pos=4096, slot=A, cache=A,
+          nb=4, bs=64, T=16, H=8, eps=1e-6, err=None):
+    return k.lib().dsv4_qnorm_rope_kv_insert_variant(store, variant, q, kv, w, pos, cs, max_pos,
+                                                     slot, cache, nb, bs, T, H, eps, err, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(T=-1), k.ERR_SHAPE), (dict(H=0), k.ERR_SHAPE), (dict(nb=0), k.ERR_SHAPE),
+    (dict(bs=0), k.ERR_SHAPE), (dict(max_pos=0), k.ERR_SHAPE),
+    (dict(T=2**62), k.ERR_SHAPE),
+    (dict(eps=-1.0), k.ERR_VALUE), (dict(eps=math.inf), k.ERR_VALUE), (dict(eps=math.nan), k.ERR_VALUE),
+    (dict(store=2), k.ERR_VALUE), (dict(variant=7), k.ERR_VALUE),
+    (dict(q=None), k.ERR_NULL), (dict(kv=None), k.ERR_NULL), (dict(w=None), k.ERR_NULL),
+    (dict(pos=None), k.ERR_NULL), (dict(cs=None), k.ERR_NULL), (dict(slot=None), k.ERR_NULL),
+    (dict(cache=None), k.ERR_NULL),
+    (dict(q=A + 8), k.ERR_ALIGN), (dict(kv=A + 2), k.ERR_ALIGN), (dict(w=A + 4), k.ERR_ALIGN),
+    (dict(cs=A + 8), k.ERR_ALIGN), (dict(pos=A + 4), k.ERR_ALIGN), (dict(slot=A + 1), k.ERR_ALIGN),
+    (dict(cache=A + 4), k.ERR_ALIGN), (dict(store=1, cache=A + 8), k.ERR_ALIGN),
+    (dict(err=A + 2), k.ERR_ALIGN),
+])
+def test_host_validation(kw, status):
+    assert _call(**kw) == status
+
+
+def test_fp8_cache_needs_only_8_byte_alignment():
+    # 8-byte aligned FP8 cache passes validation; with no T it returns before CUDA
+    assert _call(cache=A + 8, T=0) == k.OK
+
+
+def test_zero_tokens_is_a_no_op():
+    assert _call(T=0, q=None, kv=None, w=None, pos=None, cs=None, slot=None, cache=None) == k.OK
+
+
+def test_public_entries_validate_like_the_variant_entry():
+    lib = k.lib()
+    assert lib.dsv4_qnorm_rope_kv_quant_insert(A, A, A, A, A, 4096, A, A, 4, 64, -1, 8, 1e-6,
+                                               None, None) == k.ERR_SHAPE
+    assert lib.dsv4_qnorm_rope_kv_bf16_insert(A, A, A, A, A, 4096, A, A + 8, 4, 64, 5, 8, 1e-6,
+                                              None, None) == k.ERR_ALIGN
+
+
+def test_no_cpu_fallback_without_a_gpu():
+    """A valid call on a machine without a GPU must fail loudly, not compute on the host."""
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; covered by the GPU tests")
+    assert _call() == k.ERR_CUDA
+    with pytest.raises(k.Dsv4Error):
+        k.insert(k.STORE_FP8, torch.zeros(16, 8, 512, dtype=torch.bfloat16),
+                 torch.zeros(16, 512, dtype=torch.bfloat16), torch.zeros(512, dtype=torch.bfloat16),
+                 torch.zeros(16, dtype=torch.int64), torch.zeros(4096, 64),
+                 torch.zeros(16, dtype=torch.int64), torch.zeros(4 * 64 * 584, dtype=torch.uint8),
+                 4, 64, 1e-6, stream=0)
+
+
+def test_launch_plan_small_and_stream():
+    # 16 tokens x 9 rows = 144 rows: one row per warp, 2-warp CTAs
+    p = k.launch_plan(16, 8, 152, 4)
+    assert (p.variant, p.threads, p.rows_per_warp, p.rows, p.ctas) == (k.VARIANT_SMALL, 64, 1, 144, 72)
+    # 131072 x 129 rows: persistent grid, 4 CTAs on each of 152 SMs
+    p = k.launch_plan(131072, 128, 152, 4)
+    assert (p.variant, p.threads, p.ctas, p.rows) == (k.VARIANT_STREAM, 256, 608, 131072 * 129)
+    # the crossover: rows below warp slots x rows per warp go SMALL
+    slots = 152 * 4 * 8 * 2
+    assert k.launch_plan(slots // 65 - 1, 64, 152, 4).variant == k.VARIANT_SMALL
+    assert k.launch_plan(slots // 65 + 1, 64, 152, 4).variant == k.VARIANT_STREAM
+    # forced variants
+    assert k.launch_plan(131072, 128, 152, 4, k.VARIANT_SMALL).ctas == 131072 * 129 // 2
+    p = k.launch_plan(3, 1, 152, 4, k.VARIANT_STREAM)
+    assert p.ctas == 1 and p.rows == 6
+    p = k.launch_plan(0, 1, 152, 4)
+    assert p.ctas >= 1 and p.rows == 0
+
+
+def test_launch_plan_rejects():
+    for args in [(-1, 8, 152, 4), (16, 0, 152, 4), (16, 8, 0, 4), (16, 8, 152, 0)]:
+        with pytest.raises(k.Dsv4Error):
+            k.launch_plan(*args)
+    with pytest.raises(k.Dsv4Error):
+        k.launch_plan(16, 8, 152, 4, 9)
+    plan = k.Plan()
+    assert k.lib().dsv4_launch_plan(16, 8, 152, 4, 0, None) == k.ERR_NULL
+    del plan
+
+
+def test_library_has_no_oracle_dependency():
+    """The CUDA library links nothing from the oracle or the input generator."""
+    data = open(k.LIB_PATH, "rb").read()
+    assert b"oracle_" not in data and b"synth_" not in data
+    assert ctypes.CDLL(k.LIB_PATH)
