@@ -86,6 +86,34 @@ def barrier(world: int):
 
 # ------------------------------------------------------------------ measurement helpers
 
+KERNEL_SOURCES = ("kv_norm_rope_gb300/csrc/qnorm_rope_kv_insert.cu", "kv_norm_rope_gb300/csrc/launch.h")
+
+
+def kernel_fingerprint() -> str:
+    """16 hex digits identifying the kernel sources (sha256 over their sha256s)."""
+    import hashlib
+    digests = "".join(hashlib.sha256(open(os.path.join(ROOT, f), "rb").read()).hexdigest()
+                      for f in KERNEL_SOURCES)
+    return hashlib.sha256(digests.encode()).hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM read + write bytes per launch from the committed ncu summary of this
+    workload, or None when there is none or the kernel changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"qnorm_rope_kv_insert_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    fp = traffic = None
+    for line in text.splitlines():
+        if "Kernel sources fingerprint" in line and "`" in line:
+            fp = line.split("`")[1]
+        if line.startswith("traffic_bytes_per_launch:"):
+            traffic = int(line.split(":")[1])
+    return traffic if fp == kernel_fingerprint() else None
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -474,7 +502,8 @@ def run_ours(args):
         "frac_of_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
         "copy_ceiling_gbs": {"1GiB": round(copy_1g, 1), "512MiB": round(copy_512m, 1)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
-                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": profiled_traffic(wl.name.split("@")[0]),
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "launch_ms_mean": round(mean_launch * 1e3, 4),
