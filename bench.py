@@ -210,14 +210,21 @@ def copy_ceiling_gbs(dev, nbytes: int) -> float:
 
 # ------------------------------------------------------------------ inputs on the device
 
+OPS = ("fused", "prenorm", "kv_only")
+
+
 class DeviceBatch:
     """One workload resident in HBM.  q and kv are drawn on the device by a seeded
     torch generator (N(0,1), the workload's heavy tail, rounded to bf16); positions,
-    slots, the weight and the cos/sin table come from ``synth``."""
+    slots, the weight and the cos/sin table come from ``synth``.  ``op`` "kv_only"
+    holds no q."""
 
-    def __init__(self, wl: configs.Workload, dev):
+    def __init__(self, wl: configs.Workload, dev, op: str = "fused"):
         import torch
+        if op == "kv_only":
+            wl = dataclasses.replace(wl, H=0)
         self.wl = wl
+        self.op = op
         self.dev = dev
         g = torch.Generator(device=dev)
         g.manual_seed(wl.seed * 7919 + 17)
@@ -232,6 +239,8 @@ class DeviceBatch:
         self.cache = torch.zeros(configs.cache_bytes(wl), dtype=torch.uint8, device=dev)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         self.bytes = configs.algorithmic_bytes(wl, self.positions_np, self.slots_np)
+        if op == "prenorm":
+            self.bytes -= 1024  # no weight read
 
     def _normal(self, shape, g):
         import torch
@@ -249,11 +258,28 @@ class DeviceBatch:
             del x
         return out
 
-    def args(self, stream_handle: int):
+    def call(self, lib, stream_handle: int):
+        """(C-ABI function, argument tuple) of one step of this batch's op."""
         wl = self.wl
-        return (self.q.data_ptr(), self.kv.data_ptr(), self.w.data_ptr(), self.pos.data_ptr(),
-                self.cs.data_ptr(), wl.max_position, self.slots.data_ptr(), self.cache.data_ptr(),
-                wl.num_blocks, wl.block_size, wl.T, wl.H, wl.eps, self.err.data_ptr(), stream_handle)
+        if self.op == "kv_only":
+            return lib.dsv4_kv_norm_rope_insert, (
+                0 if wl.store == "fp8" else 1, self.kv.data_ptr(), self.w.data_ptr(),
+                self.pos.data_ptr(), self.cs.data_ptr(), wl.max_position, self.slots.data_ptr(),
+                self.cache.data_ptr(), wl.num_blocks, wl.block_size, wl.T, wl.eps,
+                self.err.data_ptr(), stream_handle)
+        if self.op == "prenorm":
+            if wl.store != "fp8":
+                raise ValueError("the pre-normalised entry stores FP8 rows")
+            return lib.dsv4_qnorm_rope_kv_rope_quant_insert, (
+                self.q.data_ptr(), self.kv.data_ptr(), self.pos.data_ptr(), self.cs.data_ptr(),
+                wl.max_position, self.slots.data_ptr(), self.cache.data_ptr(), wl.num_blocks,
+                wl.block_size, wl.T, wl.H, wl.eps, self.err.data_ptr(), stream_handle)
+        fn = (lib.dsv4_qnorm_rope_kv_quant_insert if wl.store == "fp8"
+              else lib.dsv4_qnorm_rope_kv_bf16_insert)
+        return fn, (self.q.data_ptr(), self.kv.data_ptr(), self.w.data_ptr(), self.pos.data_ptr(),
+                    self.cs.data_ptr(), wl.max_position, self.slots.data_ptr(),
+                    self.cache.data_ptr(), wl.num_blocks, wl.block_size, wl.T, wl.H, wl.eps,
+                    self.err.data_ptr(), stream_handle)
 
 
 def entry(lib, store: str):
@@ -434,10 +460,10 @@ def run_ours(args):
     kac_before = known_answer_check() if rank == 0 else "skipped"
     copy_1g = copy_ceiling_gbs(dev, 1 << 30)
     copy_512m = copy_ceiling_gbs(dev, 1 << 29)
-    batch = DeviceBatch(wl, dev)
+    batch = DeviceBatch(wl, dev, args.op)
+    wl = batch.wl
     stream = torch.cuda.current_stream(dev)
-    fn = entry(lib, wl.store)
-    call_args = batch.args(stream.cuda_stream)
+    fn, call_args = batch.call(lib, stream.cuda_stream)
     for _ in range(args.warmup):
         st = fn(*call_args)
         if st != 0:
@@ -449,11 +475,17 @@ def run_ours(args):
     sampler = ClockSampler(bus_id_of(local_rank)) if rank == 0 else None
     if sampler:
         sampler.start()
+    # a step that moves less than 4x the L2 gets the L2 flushed (a 256 MB write)
+    # before its launch, outside the launch's event pair
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if batch.bytes < 4 * (129 << 20) \
+        else None
     events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
     barrier(world)
     torch.cuda.synchronize(dev)
     wall0 = time.perf_counter()
     for i in range(args.steps):
+        if flush is not None:
+            flush.fill_(i & 0xFF)
         events[2 * i].record(stream)
         fn(*call_args)
         events[2 * i + 1].record(stream)
@@ -463,13 +495,14 @@ def run_ours(args):
     clocks = sampler.stop() if sampler else None
     per_launch = [events[2 * i].elapsed_time(events[2 * i + 1]) / 1e3 for i in range(args.steps)]
     region = events[0].elapsed_time(events[-1]) / 1e3
-    t_step = max_over_ranks(region / args.steps, world, dev)
+    step_s = statistics.mean(per_launch) if flush is not None else region / args.steps
+    t_step = max_over_ranks(step_s, world, dev)
     total_bytes = sum_over_ranks(float(batch.bytes), world, dev)
     total_tokens = sum_over_ranks(float(wl.T), world, dev)
     mean_launch = statistics.mean(per_launch)
 
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and args.op == "fused":
         e2e_gbs, h2d, d2h, e2e_dt = e2e_run(batch, lib, args.e2e_steps)
         e2e_dt = max_over_ranks(e2e_dt, world, dev)
         e2e = {"value": round(total_bytes / e2e_dt / 1e9, 2), "unit": "GB/s",
@@ -490,10 +523,12 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_step * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": wl.name.split("@")[0], "T": wl.T, "H": wl.H, "store": wl.store,
+        "config": {"workload": wl.name.split("@")[0], "op": args.op, "T": wl.T, "H": wl.H,
+                   "store": wl.store,
                    "num_blocks": wl.num_blocks, "block_size": wl.block_size,
-                   "bytes_per_step": batch.bytes, "l2": "inputs larger than L2 (q 17.2 GB)"
-                   if wl.T * wl.H * 1024 > (1 << 30) else "inputs within L2 size",
+                   "bytes_per_step": batch.bytes,
+                   "l2": "flushed before every launch (256 MB write)" if flush is not None
+                   else f"inputs larger than L2 ({batch.bytes / 1e9:.2f} GB per step)",
                    "io": "bf16 in; bf16 q, e4m3+ue8m0+bf16 cache out",
                    "variant": "stream" if plan.variant == k.VARIANT_STREAM else "small",
                    "parallelism": f"dp{world}" if world > 1 else "single"},
@@ -503,19 +538,22 @@ def run_ours(args):
         "copy_ceiling_gbs": {"1GiB": round(copy_1g, 1), "512MiB": round(copy_512m, 1)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": profiled_traffic(wl.name.split("@")[0]),
+                     "traffic": profiled_traffic(wl.name.split("@")[0])
+                     if args.op == "fused" else None,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "launch_ms_mean": round(mean_launch * 1e3, 4),
                      "launch_ms_median": round(statistics.median(per_launch) * 1e3, 4)},
         "gpu_launches": args.steps,
+        "ms_per_step_note": "mean launch time (L2 flushed between launches)" if flush is not None
+        else "timed region / steps",
         "clocks": clocks,
         "wall_s_timed": round(wall, 3),
         "known_answer": {"before": kac_before, "after": kac_after},
     }
     if e2e is not None:
         line["e2e"] = e2e
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and args.op == "fused":
         line["cpu_baseline"] = cpu_baseline(configs.WORKLOADS[args.workload], args.cpu_seconds)
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -531,6 +569,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(configs.WORKLOADS), default="stress")
+    ap.add_argument("--op", choices=OPS, default="fused",
+                    help="fused (default); prenorm: KV arrives normalised; kv_only: no q")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -150,6 +150,45 @@ int dsv4_qnorm_rope_kv_insert_variant(int store_mode, int variant, void *q, cons
                                       int32_t num_heads, float eps, int32_t *device_error,
                                       void *stream);
 
+/*
+ * The operator with the KV row already normalised (FlagGems-vllm PR #684: the
+ * operator is q-norm + RoPE and KV RoPE + quant + insert; its eager baseline in
+ * section "Ascend 910B" normalises q only).  As dsv4_qnorm_rope_kv_quant_insert,
+ * except the KV row gets no RMSNorm and no weight: v = kv[t,:], rotated,
+ * quantised and inserted.  eps applies to the q heads only.
+ */
+int dsv4_qnorm_rope_kv_rope_quant_insert(void *q, const void *kv, const int64_t *positions,
+                                         const float *cos_sin_cache, int64_t max_position,
+                                         const int64_t *slot_mapping, uint8_t *kv_cache,
+                                         int64_t num_blocks, int32_t block_size,
+                                         int64_t num_tokens, int32_t num_heads, float eps,
+                                         int32_t *device_error, void *stream);
+
+/*
+ * KV rows only, no q (SGLang PR #33358, "Motivation": fused_norm_rope_flashmla,
+ * RMSNorm over 512 with a weight, RoPE on the trailing 64 dims, paged store):
+ * store_mode DSV4_STORE_FP8 (kv_cache uint8, FP8 layout above, 8-byte aligned) or
+ * DSV4_STORE_BF16 (kv_cache bf16 [num_blocks, block_size, 512], 16-byte aligned).
+ * Other arguments as in dsv4_qnorm_rope_kv_quant_insert.
+ */
+int dsv4_kv_norm_rope_insert(int store_mode, const void *kv, const void *kv_norm_weight,
+                             const int64_t *positions, const float *cos_sin_cache,
+                             int64_t max_position, const int64_t *slot_mapping, void *kv_cache,
+                             int64_t num_blocks, int32_t block_size, int64_t num_tokens,
+                             float eps, int32_t *device_error, void *stream);
+
+/*
+ * The general form behind all of the above: any store mode and launch variant;
+ * kv_norm 1 normalises the KV row with kv_norm_weight, 0 takes it as already
+ * normalised (kv_norm_weight may then be NULL); num_heads >= 0, and q may be
+ * NULL when num_heads is 0.
+ */
+int dsv4_insert_ex(int store_mode, int variant, int kv_norm, void *q, const void *kv,
+                   const void *kv_norm_weight, const int64_t *positions,
+                   const float *cos_sin_cache, int64_t max_position, const int64_t *slot_mapping,
+                   void *kv_cache, int64_t num_blocks, int32_t block_size, int64_t num_tokens,
+                   int32_t num_heads, float eps, int32_t *device_error, void *stream);
+
 /* Launch plan of a call (pure host arithmetic, no CUDA call). */
 typedef struct {
     int32_t variant;        /* DSV4_VARIANT_SMALL or DSV4_VARIANT_STREAM */

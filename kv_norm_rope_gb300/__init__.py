@@ -32,8 +32,9 @@ VARIANT_AUTO, VARIANT_SMALL, VARIANT_STREAM = 0, 1, 2
 FP8_SLOT_BYTES, BF16_SLOT_BYTES = 584, 1024
 
 EXPORTS = ("dsv4_qnorm_rope_kv_quant_insert", "dsv4_qnorm_rope_kv_bf16_insert",
-           "dsv4_qnorm_rope_kv_insert_variant", "dsv4_launch_plan", "dsv4_fp8_cache_bytes",
-           "dsv4_bf16_cache_bytes", "dsv4_status_string")
+           "dsv4_qnorm_rope_kv_insert_variant", "dsv4_qnorm_rope_kv_rope_quant_insert",
+           "dsv4_kv_norm_rope_insert", "dsv4_insert_ex", "dsv4_launch_plan",
+           "dsv4_fp8_cache_bytes", "dsv4_bf16_cache_bytes", "dsv4_status_string")
 
 
 class Dsv4Error(RuntimeError):
@@ -104,6 +105,14 @@ def lib():
         L.dsv4_qnorm_rope_kv_bf16_insert.restype = c_int
         L.dsv4_qnorm_rope_kv_insert_variant.argtypes = [c_int, c_int] + common
         L.dsv4_qnorm_rope_kv_insert_variant.restype = c_int
+        L.dsv4_insert_ex.argtypes = [c_int, c_int, c_int] + common
+        L.dsv4_insert_ex.restype = c_int
+        L.dsv4_qnorm_rope_kv_rope_quant_insert.argtypes = [vp, vp, vp, vp, i64, vp, vp, i64, i32,
+                                                           i64, i32, f32, vp, vp]
+        L.dsv4_qnorm_rope_kv_rope_quant_insert.restype = c_int
+        L.dsv4_kv_norm_rope_insert.argtypes = [c_int, vp, vp, vp, vp, i64, vp, vp, i64, i32, i64,
+                                               f32, vp, vp]
+        L.dsv4_kv_norm_rope_insert.restype = c_int
         L.dsv4_launch_plan.argtypes = [i64, i32, i32, i32, i32, ctypes.POINTER(Plan)]
         L.dsv4_launch_plan.restype = c_int
         L.dsv4_fp8_cache_bytes.argtypes = [i64, i32]
@@ -162,30 +171,61 @@ def _stream_handle(stream) -> int | None:
 
 def _shape_args(q, kv, positions, cos_sin_cache):
     T = int(positions.shape[0])
-    H = int(q.shape[-2]) if q.dim() == 3 else int(q.numel() // max(T, 1) // 512)
+    if q is None:
+        H = 0
+    else:
+        H = int(q.shape[-2]) if q.dim() == 3 else int(q.numel() // max(T, 1) // 512)
     return T, H, int(cos_sin_cache.shape[0])
 
 
 def insert(store_mode: int, q, kv, kv_norm_weight, positions, cos_sin_cache, slot_mapping,
            kv_cache, num_blocks: int, block_size: int, eps: float, device_error=None,
-           stream=None, variant: int = VARIANT_AUTO, num_heads: int | None = None) -> None:
+           stream=None, variant: int = VARIANT_AUTO, num_heads: int | None = None,
+           kv_norm: bool = True) -> None:
     """Enqueue the fused step on ``stream`` (default: torch's current stream).
 
-    q: bf16 [T, H, 512] (rewritten in place); kv: bf16 [T, 512]; kv_norm_weight: bf16
-    [512]; positions, slot_mapping: int64 [T]; cos_sin_cache: fp32 [max_position, 64];
-    kv_cache: uint8 (FP8, num_blocks*block_size*584 bytes) or bf16 [num_blocks,
-    block_size, 512]; device_error: optional int32 [1].  Raises Dsv4Error on a
-    rejected call.
+    q: bf16 [T, H, 512] (rewritten in place; None for KV rows only); kv: bf16 [T, 512];
+    kv_norm_weight: bf16 [512] (unused, may be None, when ``kv_norm`` is False: the KV
+    rows then arrive normalised); positions, slot_mapping: int64 [T]; cos_sin_cache:
+    fp32 [max_position, 64]; kv_cache: uint8 (FP8, num_blocks*block_size*584 bytes) or
+    bf16 [num_blocks, block_size, 512]; device_error: optional int32 [1].  Raises
+    Dsv4Error on a rejected call.  Goes through dsv4_insert_ex.
     """
     T, H, max_pos = _shape_args(q, kv, positions, cos_sin_cache)
     if num_heads is not None:
         H = num_heads
-    st = lib().dsv4_qnorm_rope_kv_insert_variant(
-        store_mode, variant, _ptr(q), _ptr(kv), _ptr(kv_norm_weight), _ptr(positions),
-        _ptr(cos_sin_cache), max_pos, _ptr(slot_mapping), _ptr(kv_cache), num_blocks,
-        block_size, T, H, eps, _ptr(device_error), _stream_handle(stream))
+    st = lib().dsv4_insert_ex(
+        store_mode, variant, 1 if kv_norm else 0, _ptr(q), _ptr(kv), _ptr(kv_norm_weight),
+        _ptr(positions), _ptr(cos_sin_cache), max_pos, _ptr(slot_mapping), _ptr(kv_cache),
+        num_blocks, block_size, T, H, eps, _ptr(device_error), _stream_handle(stream))
     if st != OK:
-        raise Dsv4Error(st, "dsv4_qnorm_rope_kv_insert")
+        raise Dsv4Error(st, "dsv4_insert_ex")
+
+
+def qnorm_rope_kv_rope_quant_insert(q, kv, positions, cos_sin_cache, slot_mapping, kv_cache,
+                                    num_blocks, block_size, eps, device_error=None,
+                                    stream=None) -> None:
+    """dsv4_qnorm_rope_kv_rope_quant_insert: KV rows arrive normalised (rope + FP8 only)."""
+    T, H, max_pos = _shape_args(q, kv, positions, cos_sin_cache)
+    st = lib().dsv4_qnorm_rope_kv_rope_quant_insert(
+        _ptr(q), _ptr(kv), _ptr(positions), _ptr(cos_sin_cache), max_pos, _ptr(slot_mapping),
+        _ptr(kv_cache), num_blocks, block_size, T, H, eps, _ptr(device_error),
+        _stream_handle(stream))
+    if st != OK:
+        raise Dsv4Error(st, "dsv4_qnorm_rope_kv_rope_quant_insert")
+
+
+def kv_norm_rope_insert(store_mode: int, kv, kv_norm_weight, positions, cos_sin_cache,
+                        slot_mapping, kv_cache, num_blocks, block_size, eps, device_error=None,
+                        stream=None) -> None:
+    """dsv4_kv_norm_rope_insert: KV rows only (norm with weight, rope, FP8 or bf16 store)."""
+    T, _, max_pos = _shape_args(None, kv, positions, cos_sin_cache)
+    st = lib().dsv4_kv_norm_rope_insert(
+        store_mode, _ptr(kv), _ptr(kv_norm_weight), _ptr(positions), _ptr(cos_sin_cache),
+        max_pos, _ptr(slot_mapping), _ptr(kv_cache), num_blocks, block_size, T, eps,
+        _ptr(device_error), _stream_handle(stream))
+    if st != OK:
+        raise Dsv4Error(st, "dsv4_kv_norm_rope_insert")
 
 
 def qnorm_rope_kv_quant_insert(q, kv, kv_norm_weight, positions, cos_sin_cache, slot_mapping,

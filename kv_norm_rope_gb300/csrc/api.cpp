@@ -51,17 +51,24 @@ int device_shape(int store_mode, int32_t *sms, int32_t *ctas)
     return DSV4_OK;
 }
 
-int insert(int store_mode, int variant, void *q, const void *kv, const void *w,
+// flags of insert()
+constexpr int kKvNorm = 1;  // normalise the KV row with the weight
+constexpr int kNoQ = 2;     // num_heads may be 0 (KV rows only)
+
+int insert(int store_mode, int variant, int flags, void *q, const void *kv, const void *w,
            const int64_t *positions, const float *cos_sin, int64_t max_position,
            const int64_t *slot_mapping, void *cache, int64_t num_blocks, int32_t block_size,
            int64_t num_tokens, int32_t num_heads, float eps, int32_t *device_error, void *stream)
 {
+    const bool kv_norm = (flags & kKvNorm) != 0;
     if (store_mode != DSV4_STORE_FP8 && store_mode != DSV4_STORE_BF16)
         return DSV4_ERR_VALUE;
     if (variant != DSV4_VARIANT_AUTO && variant != DSV4_VARIANT_SMALL &&
         variant != DSV4_VARIANT_STREAM)
         return DSV4_ERR_VALUE;
-    if (num_tokens < 0 || num_heads < 1 || num_blocks < 1 || block_size < 1 || max_position < 1)
+    const int32_t min_heads = (flags & kNoQ) ? 0 : 1;
+    if (num_tokens < 0 || num_heads < min_heads || num_blocks < 1 || block_size < 1 ||
+        max_position < 1)
         return DSV4_ERR_SHAPE;
     // every byte offset the kernels form must fit in int64
     const int64_t lim = INT64_MAX / 4096;
@@ -72,7 +79,8 @@ int insert(int store_mode, int variant, void *q, const void *kv, const void *w,
         return DSV4_ERR_VALUE;
     if (num_tokens == 0)
         return DSV4_OK;
-    if (!q || !kv || !w || !positions || !cos_sin || !slot_mapping || !cache)
+    if ((num_heads > 0 && !q) || !kv || (kv_norm && !w) || !positions || !cos_sin ||
+        !slot_mapping || !cache)
         return DSV4_ERR_NULL;
     const uintptr_t cache_align = store_mode == DSV4_STORE_FP8 ? 8 : 16;
     if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(w, 16) || !aligned(cos_sin, 16) ||
@@ -104,6 +112,7 @@ int insert(int store_mode, int variant, void *q, const void *kv, const void *w,
     a.num_tokens = num_tokens;
     a.eps = eps;
     a.err = device_error;
+    a.kv_norm = kv_norm;
     return dsv4::launch(store_mode, plan, a, static_cast<cudaStream_t>(stream));
 }
 
@@ -116,7 +125,7 @@ int dsv4_launch_plan(int64_t num_tokens, int32_t num_heads, int32_t sm_count, in
 {
     if (!plan)
         return DSV4_ERR_NULL;
-    if (num_tokens < 0 || num_heads < 1 || sm_count < 1 || ctas_per_sm < 1)
+    if (num_tokens < 0 || num_heads < 0 || sm_count < 1 || ctas_per_sm < 1)
         return DSV4_ERR_SHAPE;
     if (num_tokens > (INT64_MAX / 4096) / (int64_t(num_heads) + 1))
         return DSV4_ERR_SHAPE;
@@ -156,7 +165,7 @@ int dsv4_qnorm_rope_kv_quant_insert(void *q, const void *kv, const void *kv_norm
                                     int64_t num_tokens, int32_t num_heads, float eps,
                                     int32_t *device_error, void *stream)
 {
-    return insert(DSV4_STORE_FP8, DSV4_VARIANT_AUTO, q, kv, kv_norm_weight, positions,
+    return insert(DSV4_STORE_FP8, DSV4_VARIANT_AUTO, kKvNorm, q, kv, kv_norm_weight, positions,
                   cos_sin_cache, max_position, slot_mapping, kv_cache, num_blocks, block_size,
                   num_tokens, num_heads, eps, device_error, stream);
 }
@@ -168,7 +177,7 @@ int dsv4_qnorm_rope_kv_bf16_insert(void *q, const void *kv, const void *kv_norm_
                                    int64_t num_tokens, int32_t num_heads, float eps,
                                    int32_t *device_error, void *stream)
 {
-    return insert(DSV4_STORE_BF16, DSV4_VARIANT_AUTO, q, kv, kv_norm_weight, positions,
+    return insert(DSV4_STORE_BF16, DSV4_VARIANT_AUTO, kKvNorm, q, kv, kv_norm_weight, positions,
                   cos_sin_cache, max_position, slot_mapping, kv_cache, num_blocks, block_size,
                   num_tokens, num_heads, eps, device_error, stream);
 }
@@ -181,9 +190,45 @@ int dsv4_qnorm_rope_kv_insert_variant(int store_mode, int variant, void *q, cons
                                       int32_t num_heads, float eps, int32_t *device_error,
                                       void *stream)
 {
-    return insert(store_mode, variant, q, kv, kv_norm_weight, positions, cos_sin_cache,
+    return insert(store_mode, variant, kKvNorm, q, kv, kv_norm_weight, positions, cos_sin_cache,
                   max_position, slot_mapping, kv_cache, num_blocks, block_size, num_tokens,
                   num_heads, eps, device_error, stream);
+}
+
+int dsv4_qnorm_rope_kv_rope_quant_insert(void *q, const void *kv, const int64_t *positions,
+                                         const float *cos_sin_cache, int64_t max_position,
+                                         const int64_t *slot_mapping, uint8_t *kv_cache,
+                                         int64_t num_blocks, int32_t block_size,
+                                         int64_t num_tokens, int32_t num_heads, float eps,
+                                         int32_t *device_error, void *stream)
+{
+    return insert(DSV4_STORE_FP8, DSV4_VARIANT_AUTO, 0, q, kv, nullptr, positions,
+                  cos_sin_cache, max_position, slot_mapping, kv_cache, num_blocks, block_size,
+                  num_tokens, num_heads, eps, device_error, stream);
+}
+
+int dsv4_kv_norm_rope_insert(int store_mode, const void *kv, const void *kv_norm_weight,
+                             const int64_t *positions, const float *cos_sin_cache,
+                             int64_t max_position, const int64_t *slot_mapping, void *kv_cache,
+                             int64_t num_blocks, int32_t block_size, int64_t num_tokens,
+                             float eps, int32_t *device_error, void *stream)
+{
+    return insert(store_mode, DSV4_VARIANT_AUTO, kKvNorm | kNoQ, nullptr, kv, kv_norm_weight,
+                  positions, cos_sin_cache, max_position, slot_mapping, kv_cache, num_blocks,
+                  block_size, num_tokens, 0, eps, device_error, stream);
+}
+
+int dsv4_insert_ex(int store_mode, int variant, int kv_norm, void *q, const void *kv,
+                   const void *kv_norm_weight, const int64_t *positions,
+                   const float *cos_sin_cache, int64_t max_position, const int64_t *slot_mapping,
+                   void *kv_cache, int64_t num_blocks, int32_t block_size, int64_t num_tokens,
+                   int32_t num_heads, float eps, int32_t *device_error, void *stream)
+{
+    if (kv_norm != 0 && kv_norm != 1)
+        return DSV4_ERR_VALUE;
+    return insert(store_mode, variant, (kv_norm ? kKvNorm : 0) | kNoQ, q, kv, kv_norm_weight,
+                  positions, cos_sin_cache, max_position, slot_mapping, kv_cache, num_blocks,
+                  block_size, num_tokens, num_heads, eps, device_error, stream);
 }
 
 size_t dsv4_fp8_cache_bytes(int64_t num_blocks, int32_t block_size)

@@ -10,7 +10,7 @@
 namespace dsv4 {
 
 // Rows each warp of the streaming variant loads before it computes any.
-constexpr int kStreamRowsPerWarp = 2;
+constexpr int kStreamRowsPerWarp = 3;
 constexpr int kStreamThreads = 256;
 constexpr int kSmallThreads = 64;
 
@@ -29,6 +29,7 @@ struct LaunchArgs {
     int64_t num_tokens;
     float eps;
     int32_t *err;
+    bool kv_norm;  // false: the KV rows arrive normalised (no norm, no weight)
 };
 
 // CTAs of the streaming kernel for `store_mode` that fit on one SM.

@@ -295,12 +295,23 @@ __device__ __forceinline__ void flag_error(int32_t *err, int bit)
 // v = x * r * w for the lane's 16 dims of the KV row, then the rotation of
 // the rope dims (lanes 24..31).  Deterministic: calling it twice on the same
 // data gives the same bits.
-template <bool kSmemW>
+template <bool kSmemW, bool kKvNorm>
 __device__ __forceinline__ void kv_values(const KParams &p, int lane, uint4 xa, uint4 xb,
                                           float4 cv, float4 sv, const uint4 *w_smem, float *v)
 {
     widen8(xa, v);
     widen8(xb, v + 8);
+    if (!kKvNorm) {
+        // the row arrives normalised: v = x (exact), only the rope dims turn
+        if (lane >= 24) {
+            float u[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                u[k] = v[8 + k];
+            rope8_scaled(u, cv, sv, 1.0f, v + 8);
+        }
+        return;
+    }
     float ss = 0.0f;
 #pragma unroll
     for (int k = 0; k < 16; ++k)
@@ -329,8 +340,9 @@ __device__ __forceinline__ void kv_values(const KParams &p, int lane, uint4 xa, 
     }
 }
 
-// The KV row of token t: v = x*r*w, rotate, store into the paged cache.
-template <int kStore, bool kSmemW>
+// The KV row of token t: v = x*r*w (or v = x when the row arrives normalised),
+// rotate, store into the paged cache.
+template <int kStore, bool kSmemW, bool kKvNorm>
 __device__ __forceinline__ void kv_row(const KParams &p, int lane, int64_t t, const uint4 *w_smem)
 {
     const int64_t pos = __ldg(p.pos + t);
@@ -358,7 +370,7 @@ __device__ __forceinline__ void kv_row(const KParams &p, int lane, int64_t t, co
         sv = __ldg(reinterpret_cast<const float4 *>(cs + DSV4_ROPE_DIM / 2));
     }
     float v[16];
-    kv_values<kSmemW>(p, lane, xa, xb, cv, sv, w_smem, v);
+    kv_values<kSmemW, kKvNorm>(p, lane, xa, xb, cv, sv, w_smem, v);
 
     if (kStore == DSV4_STORE_BF16) {
         uint16_t *row = reinterpret_cast<uint16_t *>(p.cache) + slot * kHead;
@@ -379,14 +391,15 @@ __device__ __forceinline__ void kv_row(const KParams &p, int lane, int64_t t, co
     }
     ScaleGuess g0 = ue8m0_guess(group8_max(am0));
     ScaleGuess g1 = ue8m0_guess(group8_max(am1));  // lanes 24..31: amax 0, never near
-    if (__any_sync(kFull, g0.near || g1.near)) {
+    // with no norm, v = x exactly and the guess is already exact
+    if (kKvNorm && __any_sync(kFull, g0.near || g1.near)) {
         const int bumps = exact_scale_bumps(p, lane, t, g0.e, g0.near, g1.e, g1.near);
         if (g0.near)
             g0.s = clamp_s(g0.e - 8 + (bumps & 1));
         if (g1.near)
             g1.s = clamp_s(g1.e - 8 + ((bumps >> 1) & 1));
         // recompute v (same bits) instead of keeping it live across the call
-        kv_values<kSmemW>(p, lane, __ldg(reinterpret_cast<const uint4 *>(src) + lane),
+        kv_values<kSmemW, kKvNorm>(p, lane, __ldg(reinterpret_cast<const uint4 *>(src) + lane),
                           __ldg(reinterpret_cast<const uint4 *>(src) + 32 + lane), cv, sv,
                           w_smem, v);
     }
@@ -425,13 +438,13 @@ __device__ __forceinline__ void kv_row(const KParams &p, int lane, int64_t t, co
 // Work items, handed out round-robin over all warps of the grid:
 //   items [0, T)            : the KV row of token t = item
 //   items [T, T + ceil(TH/R)): R consecutive q rows (memory order) each
-template <int kStore, int kRows, bool kSmemW>
-__global__ void __launch_bounds__(256, 4) qnorm_rope_kv_insert_kernel(const KParams p)
+template <int kStore, int kRows, bool kSmemW, bool kKvNorm>
+__global__ void __launch_bounds__(256, 3) qnorm_rope_kv_insert_kernel(const KParams p)
 {
     __shared__ uint4 w_smem[kSmemW ? 64 : 1];
     const int lane = threadIdx.x & 31;
     const int warps_per_cta = blockDim.x >> 5;
-    if (kSmemW) {
+    if (kSmemW && kKvNorm) {
         for (int i = threadIdx.x; i < 64; i += blockDim.x)
             w_smem[i] = __ldg(reinterpret_cast<const uint4 *>(p.w) + i);
         __syncthreads();
@@ -445,7 +458,7 @@ __global__ void __launch_bounds__(256, 4) qnorm_rope_kv_insert_kernel(const KPar
     for (int64_t it = int64_t(blockIdx.x) * warps_per_cta + (threadIdx.x >> 5); it < items;
          it += stride) {
         if (it < T) {
-            kv_row<kStore, kSmemW>(p, lane, it, w_smem);
+            kv_row<kStore, kSmemW, kKvNorm>(p, lane, it, w_smem);
             continue;
         }
         const int64_t r0 = (it - T) * kRows;
@@ -518,23 +531,35 @@ __global__ void __launch_bounds__(256, 4) qnorm_rope_kv_insert_kernel(const KPar
     }
 }
 
-template <int kStore>
+template <int kStore, bool kKvNorm>
 struct Kernels {
-    static constexpr auto small = qnorm_rope_kv_insert_kernel<kStore, 1, false>;
-    static constexpr auto stream = qnorm_rope_kv_insert_kernel<kStore, kStreamRowsPerWarp, true>;
+    static constexpr auto small = qnorm_rope_kv_insert_kernel<kStore, 1, false, kKvNorm>;
+    static constexpr auto stream =
+        qnorm_rope_kv_insert_kernel<kStore, kStreamRowsPerWarp, true, kKvNorm>;
 };
+
+template <int kStore, bool kKvNorm>
+void launch_one(bool small, dim3 grid, dim3 block, cudaStream_t stream, const KParams &p)
+{
+    if (small)
+        Kernels<kStore, kKvNorm>::small<<<grid, block, 0, stream>>>(p);
+    else
+        Kernels<kStore, kKvNorm>::stream<<<grid, block, 0, stream>>>(p);
+}
 
 }  // namespace
 
 int stream_ctas_per_sm(int store_mode, int *ctas_per_sm)
 {
+    // the normalising FP8 kernel is the largest; every streaming kernel shares
+    // its launch bounds, so its occupancy is the one used for all of them
     cudaError_t e;
     if (store_mode == DSV4_STORE_BF16)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, Kernels<DSV4_STORE_BF16>::stream,
-                                                          kStreamThreads, 0);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            ctas_per_sm, Kernels<DSV4_STORE_BF16, true>::stream, kStreamThreads, 0);
     else
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, Kernels<DSV4_STORE_FP8>::stream,
-                                                          kStreamThreads, 0);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            ctas_per_sm, Kernels<DSV4_STORE_FP8, true>::stream, kStreamThreads, 0);
     return e == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
 }
 
@@ -558,15 +583,15 @@ int launch(int store_mode, const dsv4_plan &plan, const LaunchArgs &a, cudaStrea
     const dim3 grid(unsigned(plan.ctas)), block(unsigned(plan.threads));
     const bool small = plan.variant == DSV4_VARIANT_SMALL;
     if (store_mode == DSV4_STORE_BF16) {
-        if (small)
-            Kernels<DSV4_STORE_BF16>::small<<<grid, block, 0, stream>>>(p);
+        if (a.kv_norm)
+            launch_one<DSV4_STORE_BF16, true>(small, grid, block, stream, p);
         else
-            Kernels<DSV4_STORE_BF16>::stream<<<grid, block, 0, stream>>>(p);
+            launch_one<DSV4_STORE_BF16, false>(small, grid, block, stream, p);
     } else {
-        if (small)
-            Kernels<DSV4_STORE_FP8>::small<<<grid, block, 0, stream>>>(p);
+        if (a.kv_norm)
+            launch_one<DSV4_STORE_FP8, true>(small, grid, block, stream, p);
         else
-            Kernels<DSV4_STORE_FP8>::stream<<<grid, block, 0, stream>>>(p);
+            launch_one<DSV4_STORE_FP8, false>(small, grid, block, stream, p);
     }
     return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
 }

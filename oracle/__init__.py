@@ -44,11 +44,13 @@ def _load():
     if _lib is None:
         lib = ctypes.CDLL(build())
         vp, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float
-        lib.oracle_qnorm_rope_kv_insert.argtypes = [ctypes.c_int, vp, vp, vp, vp, vp, i64, vp, vp,
+        lib.oracle_qnorm_rope_kv_insert.argtypes = [ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, vp,
+                                                    i64, vp, vp,
                                                     i64, i32, i64, i32, f32, ctypes.c_int]
         lib.oracle_qnorm_rope_kv_insert.restype = i32
         lib.oracle_q_values.argtypes = [vp, vp, f32, vp]
         lib.oracle_kv_values.argtypes = [vp, vp, vp, f32, vp]
+        lib.oracle_kv_rope_values.argtypes = [vp, vp, vp]
         lib.oracle_fp8_slot.argtypes = [vp, vp, vp]
         for name in ("oracle_bf16_rne_array", "oracle_e4m3_rne_array",
                      "oracle_bf16_value_array", "oracle_ue8m0_exponent_array"):
@@ -67,9 +69,11 @@ def _c(a: np.ndarray, dtype) -> np.ndarray:
 def qnorm_rope_kv_insert(store: str, q: np.ndarray | None, kv: np.ndarray | None, w: np.ndarray,
                          positions: np.ndarray, cos_sin: np.ndarray, slot_mapping: np.ndarray,
                          cache: np.ndarray, num_blocks: int, block_size: int, eps: float,
-                         H: int | None = None, n_threads: int = 0) -> int:
+                         H: int | None = None, n_threads: int = 0, kv_norm: bool = True) -> int:
     """Run the oracle.  ``q`` (uint16 bf16 bits [T,H,512], or None) and ``cache``
-    (uint8, poisoned pre-image) are modified in place.  Returns the error bits."""
+    (uint8, poisoned pre-image) are modified in place.  ``kv_norm`` False takes the
+    KV rows as already normalised (rotation only; ``w`` and ``eps`` unused for
+    them).  Returns the error bits."""
     lib = _load()
     T = int(positions.shape[0])
     if q is not None:
@@ -84,7 +88,7 @@ def qnorm_rope_kv_insert(store: str, q: np.ndarray | None, kv: np.ndarray | None
     else:
         assert kv is None, "a cache image is needed when kv rows are given"
 
-    w = _c(w, np.uint16)
+    w = _c(np.zeros(512, np.uint16) if w is None else w, np.uint16)
     pos = _c(positions, np.int64)
     cs = _c(cos_sin, np.float32)
     sl = _c(slot_mapping, np.int64)
@@ -93,7 +97,8 @@ def qnorm_rope_kv_insert(store: str, q: np.ndarray | None, kv: np.ndarray | None
         kv = _c(kv, np.uint16)
         kvp = kv.ctypes.data
     return int(lib.oracle_qnorm_rope_kv_insert(
-        1 if store == "bf16" else 0, q.ctypes.data if q is not None else None, kvp, w.ctypes.data,
+        1 if store == "bf16" else 0, 1 if kv_norm else 0,
+        q.ctypes.data if q is not None else None, kvp, w.ctypes.data,
         pos.ctypes.data, cs.ctypes.data, cs.shape[0], sl.ctypes.data,
         cache.ctypes.data if cache is not None else None,
         num_blocks, block_size, T, H, eps, n_threads))
@@ -111,10 +116,19 @@ def q_values(x: np.ndarray, cs_row: np.ndarray, eps: float) -> np.ndarray:
 def kv_values(x: np.ndarray, w: np.ndarray, cs_row: np.ndarray, eps: float) -> np.ndarray:
     """fp64 normalised, weighted, rotated KV row (before rounding/quantisation)."""
     x = _c(x, np.uint16)
-    w = _c(w, np.uint16)
+    w = _c(np.zeros(512, np.uint16) if w is None else w, np.uint16)
     cs = _c(cs_row, np.float32)
     out = np.empty(512, dtype=np.float64)
     _load().oracle_kv_values(x.ctypes.data, w.ctypes.data, cs.ctypes.data, eps, out.ctypes.data)
+    return out
+
+
+def kv_rope_values(x: np.ndarray, cs_row: np.ndarray) -> np.ndarray:
+    """fp64 rotated KV row that arrives normalised (no norm, no weight)."""
+    x = _c(x, np.uint16)
+    cs = _c(cs_row, np.float32)
+    out = np.empty(512, dtype=np.float64)
+    _load().oracle_kv_rope_values(x.ctypes.data, cs.ctypes.data, out.ctypes.data)
     return out
 
 

@@ -41,6 +41,11 @@
  *       and benchmark fixes": build the power of two exactly, never via exp2).
  *   bf16 store ([SG] "Motivation", kBf16Store): bf16(v) for all 512 dims.
  *   slot_mapping[t] < 0: no cache write; q is still rewritten.
+ *   KV already normalised (kv_norm = 0): v = x, rotated as above, with no
+ *       norm and no weight.  The [FG] operator's name (qnorm + rope, kv rope +
+ *       quant + insert) and its eager baseline in "Ascend 910B" (a weightless
+ *       RMSNorm of q, RoPE, the FP8 encoder, a scatter into the cache) apply no
+ *       norm to KV.
  */
 #include <math.h>
 #include <pthread.h>
@@ -208,6 +213,14 @@ void oracle_q_values(const uint16_t *x, const float *cs, float eps, double *y)
     rotate_tail(y, cs);
 }
 
+/* KV row that arrives normalised: only rotated, before rounding or quantisation */
+void oracle_kv_rope_values(const uint16_t *x, const float *cs, double *v)
+{
+    for (int d = 0; d < HEAD; ++d)
+        v[d] = oracle_bf16_value(x[d]);
+    rotate_tail(v, cs);
+}
+
 /* normalised, weighted and rotated KV row, before rounding or quantisation */
 void oracle_kv_values(const uint16_t *x, const uint16_t *w, const float *cs, float eps, double *v)
 {
@@ -249,6 +262,7 @@ void oracle_fp8_slot(const double *v, uint8_t *data, uint8_t *scale)
 
 typedef struct {
     int store_bf16;
+    int kv_norm;
     uint16_t *q;
     const uint16_t *kv, *w;
     const int64_t *pos;
@@ -291,7 +305,10 @@ static void *run_tokens(void *arg)
             j->err |= ERR_SLOT_RANGE;
             continue;
         }
-        oracle_kv_values(j->kv + t * HEAD, j->w, cs, j->eps, y);
+        if (j->kv_norm)
+            oracle_kv_values(j->kv + t * HEAD, j->w, cs, j->eps, y);
+        else
+            oracle_kv_rope_values(j->kv + t * HEAD, cs, y);
         int64_t blk = slot / j->bs, off = slot % j->bs;
         if (j->store_bf16) {
             uint8_t *row = j->cache + slot * (int64_t)(HEAD * 2);
@@ -308,12 +325,13 @@ static void *run_tokens(void *arg)
 
 /*
  * Whole-batch oracle.  q [T,H,512] bf16 is rewritten in place (H may be 0);
- * kv [T,512] (NULL: no cache writes); cache is the poisoned pre-image, of
+ * kv [T,512] (NULL: no cache writes), normalised with w when kv_norm is 1,
+ * taken as already normalised when 0; cache is the poisoned pre-image, of
  * num_blocks*block_size*584 bytes (FP8) or num_blocks*block_size*1024 (bf16).
  * Returns the OR of ERR_* bits.  Tokens are independent, so threads split
  * them into contiguous ranges; the result does not depend on the split.
  */
-int32_t oracle_qnorm_rope_kv_insert(int store_bf16, uint16_t *q, const uint16_t *kv,
+int32_t oracle_qnorm_rope_kv_insert(int store_bf16, int kv_norm, uint16_t *q, const uint16_t *kv,
                                     const uint16_t *w, const int64_t *positions,
                                     const float *cos_sin, int64_t max_position,
                                     const int64_t *slot_mapping, uint8_t *cache,
@@ -335,7 +353,7 @@ int32_t oracle_qnorm_rope_kv_insert(int store_bf16, uint16_t *q, const uint16_t 
         int64_t a = i * per, b = a + per;
         if (a > T) a = T;
         if (b > T) b = T;
-        jobs[i] = (job_t){store_bf16, q, kv, w, positions, cos_sin, max_position, slot_mapping,
+        jobs[i] = (job_t){store_bf16, kv_norm, q, kv, w, positions, cos_sin, max_position, slot_mapping,
                           cache, num_blocks, block_size, a, b, H, eps, 0};
     }
     for (int i = 1; i < n_threads; ++i)

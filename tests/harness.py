@@ -50,7 +50,7 @@ class GpuResult:
 
 
 def run_gpu(inp: Inputs, variant: int = 0, q_tokens: np.ndarray | None = None,
-            store: str | None = None, device: str = "cuda:0") -> GpuResult:
+            store: str | None = None, device: str = "cuda:0", kv_norm: bool = True) -> GpuResult:
     import torch
 
     import kv_norm_rope_gb300 as k
@@ -66,9 +66,9 @@ def run_gpu(inp: Inputs, variant: int = 0, q_tokens: np.ndarray | None = None,
     cs = torch.from_numpy(inp.cos_sin).to(dev)
     cache = torch.from_numpy(inp.poison).to(dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    k.insert(k.STORE_FP8 if store == "fp8" else k.STORE_BF16, q, kv, w, pos, cs, sl, cache,
-             wl.num_blocks, wl.block_size, wl.eps, device_error=err, variant=variant,
-             num_heads=wl.H)
+    k.insert(k.STORE_FP8 if store == "fp8" else k.STORE_BF16, q if wl.H > 0 else None, kv, w,
+             pos, cs, sl, cache, wl.num_blocks, wl.block_size, wl.eps, device_error=err,
+             variant=variant, num_heads=wl.H, kv_norm=kv_norm)
     torch.cuda.synchronize(dev)
     if q_tokens is None:
         q_tokens = np.arange(wl.T, dtype=np.int64)
@@ -91,7 +91,7 @@ def sample_tokens(T: int, n: int, seed: int) -> np.ndarray:
 
 
 def run_oracle(inp: Inputs, q_tokens: np.ndarray | None = None, store: str | None = None,
-               n_threads: int = 0):
+               n_threads: int = 0, kv_norm: bool = True):
     """(q rows of q_tokens after the step, cache image, error bits) from the oracle."""
     wl = inp.wl
     store = store or wl.store
@@ -99,10 +99,12 @@ def run_oracle(inp: Inputs, q_tokens: np.ndarray | None = None, store: str | Non
     # KV rows of every token: the whole cache image
     err = oracle.qnorm_rope_kv_insert(store, None, inp.kv, inp.w, inp.positions, inp.cos_sin,
                                       inp.slots, cache, wl.num_blocks, wl.block_size, wl.eps,
-                                      n_threads=n_threads)
+                                      n_threads=n_threads, kv_norm=kv_norm)
     if q_tokens is None:
         q_tokens = np.arange(wl.T, dtype=np.int64)
     q = np.ascontiguousarray(inp.q[q_tokens])
+    if wl.H == 0:
+        return q, cache, err
     no_slots = np.full(q_tokens.size, -1, dtype=np.int64)
     err |= oracle.qnorm_rope_kv_insert(store, q, None, inp.w, inp.positions[q_tokens], inp.cos_sin,
                                        no_slots, None, wl.num_blocks, wl.block_size, wl.eps,
@@ -132,12 +134,12 @@ def compare_results(inp: Inputs, gpu: GpuResult, ref_q: np.ndarray, ref_cache: n
 
 
 def check(wl: Workload, variant: int = 0, n_sample: int | None = None, inp: Inputs | None = None,
-          store: str | None = None) -> compare.Report:
+          store: str | None = None, kv_norm: bool = True) -> compare.Report:
     """Full round trip for one workload; q compared on all tokens or on a sample."""
     inp = make_inputs(wl) if inp is None else inp
     q_tokens = None if n_sample is None else sample_tokens(wl.T, n_sample, wl.seed + 5)
-    gpu = run_gpu(inp, variant, q_tokens, store)
-    ref_q, ref_cache, ref_err = run_oracle(inp, gpu.q_tokens, store)
+    gpu = run_gpu(inp, variant, q_tokens, store, kv_norm=kv_norm)
+    ref_q, ref_cache, ref_err = run_oracle(inp, gpu.q_tokens, store, kv_norm=kv_norm)
     rep = compare_results(inp, gpu, ref_q, ref_cache, store)
     if gpu.err != ref_err:
         rep.fail(f"device error bits {gpu.err} != oracle {ref_err}")

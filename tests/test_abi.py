@@ -108,7 +108,7 @@ def test_launch_plan_small_and_stream():
     p = k.launch_plan(131072, 128, 152, 4)
     assert (p.variant, p.threads, p.ctas, p.rows) == (k.VARIANT_STREAM, 256, 608, 131072 * 129)
     # the crossover: rows below warp slots x rows per warp go SMALL
-    slots = 152 * 4 * 8 * 2
+    slots = 152 * 4 * 8 * p.rows_per_warp
     assert k.launch_plan(slots // 65 - 1, 64, 152, 4).variant == k.VARIANT_SMALL
     assert k.launch_plan(slots // 65 + 1, 64, 152, 4).variant == k.VARIANT_STREAM
     # forced variants
@@ -120,7 +120,7 @@ def test_launch_plan_small_and_stream():
 
 
 def test_launch_plan_rejects():
-    for args in [(-1, 8, 152, 4), (16, 0, 152, 4), (16, 8, 0, 4), (16, 8, 152, 0)]:
+    for args in [(-1, 8, 152, 4), (16, -1, 152, 4), (16, 8, 0, 4), (16, 8, 152, 0)]:
         with pytest.raises(k.Dsv4Error):
             k.launch_plan(*args)
     with pytest.raises(k.Dsv4Error):
@@ -135,3 +135,44 @@ def test_library_has_no_oracle_dependency():
     data = open(k.LIB_PATH, "rb").read()
     assert b"oracle_" not in data and b"synth_" not in data
     assert ctypes.CDLL(k.LIB_PATH)
+
+
+def test_launch_plan_kv_rows_only():
+    p = k.launch_plan(1000, 0, 152, 4)
+    assert p.rows == 1000 and p.variant == k.VARIANT_SMALL and p.ctas == 500
+
+
+def _ex(kv_norm=1, store=0, variant=0, q=A, kv=A, w=A, pos=A, cs=A, max_pos=4096, slot=A,
+        cache=A, nb=4, bs=64, T=16, H=8, eps=1e-6, err=None):
+    return k.lib().dsv4_insert_ex(store, variant, kv_norm, q, kv, w, pos, cs, max_pos, slot, cache,
+                                  nb, bs, T, H, eps, err, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(kv_norm=2), k.ERR_VALUE), (dict(H=-1), k.ERR_SHAPE),
+    (dict(q=None), k.ERR_NULL), (dict(w=None), k.ERR_NULL), (dict(kv=None), k.ERR_NULL),
+    (dict(kv_norm=0, w=None, T=0), k.OK), (dict(H=0, q=None, T=0), k.OK),
+    (dict(kv_norm=0, w=A + 8), k.ERR_ALIGN),
+])
+def test_ex_validation(kw, status):
+    assert _ex(**kw) == status
+
+
+def test_kv_only_and_prenormalised_entries_validate():
+    lib = k.lib()
+    # KV rows only: no q argument at all; weight required
+    assert lib.dsv4_kv_norm_rope_insert(0, A, None, A, A, 4096, A, A, 4, 64, 16, 1e-6, None,
+                                        None) == k.ERR_NULL
+    assert lib.dsv4_kv_norm_rope_insert(5, A, A, A, A, 4096, A, A, 4, 64, 16, 1e-6, None,
+                                        None) == k.ERR_VALUE
+    assert lib.dsv4_kv_norm_rope_insert(1, A, A, A, A, 4096, A, A + 8, 4, 64, 16, 1e-6, None,
+                                        None) == k.ERR_ALIGN
+    assert lib.dsv4_kv_norm_rope_insert(0, A, A, A, A, 4096, A, A, 4, 64, 0, 1e-6, None,
+                                        None) == k.OK
+    # KV arrives normalised: no weight argument; q still required (H >= 1)
+    assert lib.dsv4_qnorm_rope_kv_rope_quant_insert(A, A, A, A, 4096, A, A, 4, 64, 16, 0, 1e-6,
+                                                    None, None) == k.ERR_SHAPE
+    assert lib.dsv4_qnorm_rope_kv_rope_quant_insert(None, A, A, A, 4096, A, A, 4, 64, 16, 8, 1e-6,
+                                                    None, None) == k.ERR_NULL
+    assert lib.dsv4_qnorm_rope_kv_rope_quant_insert(A, A, A, A, 4096, A, A, 4, 64, 0, 8, 1e-6,
+                                                    None, None) == k.OK

@@ -302,3 +302,47 @@ def test_thread_split_does_not_change_bits():
         outs.append((qq, cache))
     for qq, cache in outs[1:]:
         assert np.array_equal(qq, outs[0][0]) and np.array_equal(cache, outs[0][1])
+
+
+@pytest.mark.parametrize("case", CASES["prenormalised_kv_cases"], ids=lambda c: c["name"])
+def test_golden_prenormalised_kv_rows(case):
+    """KV rows that arrive normalised: rotation and quantisation only."""
+    x = _expand_values(case["kv"])
+    v = oracle.kv_rope_values(x, _table(case["cos_sin"]))
+    data, scale = oracle.fp8_slot(v)
+    assert np.array_equal(data, _expand_bytes(case["fp8_data"], 576))
+    assert np.array_equal(scale, _expand_bytes(case["fp8_scale"], 8))
+    if "bf16_row" in case:
+        assert np.array_equal(oracle.bf16_rne(v), _expand_bf16_row(case["bf16_row"]))
+
+
+def test_prenormalised_driver_ignores_weight_and_eps():
+    """Through the batch driver (KV only, no q): the weight and eps do not enter the
+    KV rows when they arrive normalised, and a row of exact RMS 1 with w = 1 and
+    eps = 0 gives the same image with or without the norm."""
+    h3, x_h3, w1 = _rows_for("H3_quarter_turn_kv")
+    pn2 = next(c for c in CASES["prenormalised_kv_cases"] if c["name"] == "PN2_not_renormalised")
+    x_pn2 = _expand_values(pn2["kv"])
+    table = np.stack([F32_IDENTITY, F32_QUARTER])
+    poison = synth.poison_bytes(4 * 584, seed=9)
+    kv = np.stack([x_h3, x_pn2])
+    pos = np.array([1, 0], np.int64)
+    slots = np.array([3, 1], np.int64)
+    w_odd = synth.normal_bf16(512, 3, 3, mean=1.0, std=0.5)
+    for w, eps in [(w1, 0.0), (w_odd, 0.25)]:
+        cache = poison.copy()
+        err = oracle.qnorm_rope_kv_insert("fp8", None, kv, w, pos, table, slots, cache, 1, 4, eps,
+                                          kv_norm=False)
+        assert err == 0
+        expect = poison.copy()
+        expect[576 * 3:576 * 4] = _expand_bytes(h3["fp8_data"], 576)
+        expect[2304 + 24:2304 + 32] = _expand_bytes(h3["fp8_scale"], 8)
+        expect[576:1152] = _expand_bytes(pn2["fp8_data"], 576)
+        expect[2304 + 8:2304 + 16] = _expand_bytes(pn2["fp8_scale"], 8)
+        assert np.array_equal(cache, expect)
+    # with the norm on, the RMS-1 row is unchanged and the 2.0 row becomes 1.0 (= H1)
+    cache = poison.copy()
+    oracle.qnorm_rope_kv_insert("fp8", None, kv, w1, pos, table, slots, cache, 1, 4, 0.0)
+    h1 = next(c for c in CASES["kv_cases"] if c["name"] == "H1_constant_row")
+    assert np.array_equal(cache[576 * 3:576 * 4], _expand_bytes(h3["fp8_data"], 576))
+    assert np.array_equal(cache[576:1152], _expand_bytes(h1["fp8_data"], 576))

@@ -246,3 +246,83 @@ def test_runs_on_a_side_stream():
                             .reshape(wl.T, wl.H, 512), cache.cpu().numpy(), 0)
     rep = harness.compare_results(inp, gpu, ref_q, ref_cache)
     assert rep.ok, str(rep)
+
+
+# ---------------------------------------------------------------- KV arriving normalised / KV only
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("store", ["fp8", "bf16"])
+def test_prenormalised_kv(store, variant):
+    """The FlagGems operator form: q-norm + rope, KV rope + quant + insert (no KV norm)."""
+    for T, H in [(17, 8), (1000, 64), (333, 1)]:
+        rep = harness.check(configs.generic(T, H, store=store, seed=2000 + T), variant,
+                            kv_norm=False)
+        assert rep.ok, str(rep)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("store", ["fp8", "bf16"])
+def test_kv_rows_only(store, variant):
+    """The SGLang fused_norm_rope_flashmla form: KV rows only, no q."""
+    for T in (1, 64, 2048, 5000):
+        rep = harness.check(configs.generic(T, 0, store=store, seed=3000 + T), variant)
+        assert rep.ok, str(rep)
+
+
+@pytest.mark.parametrize("case", GOLDEN["prenormalised_kv_cases"], ids=lambda c: c["name"])
+def test_golden_prenormalised_rows_on_gpu(case):
+    ident = np.array([1.0] * 32 + [0.0] * 32, np.float32)
+    quarter = np.array([0.0] * 32 + [1.0] * 32, np.float32)
+    x = _row(case["kv"])
+    pos = 0 if case["cos_sin"] == "identity" else 1
+    wl = configs.Workload("golden_pn_" + case["name"], 2, 1, "fp8", 2, 1, 4, 0, eps=0.0)
+    inp = harness.Inputs(wl, np.ascontiguousarray(np.stack([x[None]] * 2)), np.stack([x] * 2),
+                         np.zeros(512, np.uint16), np.full(2, pos, np.int64),
+                         np.array([3, 1], np.int64), np.stack([ident, quarter]),
+                         synth.poison_bytes(4 * 584, seed=4))
+    for v in VARIANTS:
+        gpu = harness.run_gpu(inp, v, kv_norm=False)
+        expect = inp.poison.copy()
+        for slot in (3, 1):
+            expect[576 * slot:576 * slot + 576] = _bytes(case["fp8_data"], 576)
+            expect[2304 + 8 * slot:2304 + 8 * slot + 8] = _bytes(case["fp8_scale"], 8)
+        assert np.array_equal(gpu.cache, expect)
+
+
+@pytest.mark.parametrize("name", ["prefill", "stress"])
+def test_full_size_kv_only_and_prenormalised(name):
+    wl = configs.WORKLOADS[name]
+    kv_wl = configs.Workload(wl.name + "_kvonly", wl.T, 0, wl.store, wl.max_position,
+                             wl.num_blocks, wl.block_size, wl.seed, wl.tail_frac, wl.tail_mult)
+    configs._POSITIONS[kv_wl.name] = configs._POSITIONS[wl.name]
+    configs._SLOTS[kv_wl.name] = configs._SLOTS[wl.name]
+    rep = harness.check(kv_wl, k.VARIANT_AUTO)
+    assert rep.ok, str(rep)
+    if name == "prefill":
+        rep = harness.check(wl, k.VARIANT_AUTO, n_sample=1024, kv_norm=False)
+        assert rep.ok, str(rep)
+
+
+def test_public_entries_match_ex():
+    """dsv4_qnorm_rope_kv_rope_quant_insert and dsv4_kv_norm_rope_insert give the same
+    bytes as the general entry with the corresponding flags."""
+    wl = configs.generic(700, 16, seed=41)
+    inp = harness.make_inputs(wl)
+    dev = torch.device("cuda:0")
+    t = lambda a: torch.from_numpy(a).to(dev)
+    q = t(inp.q.view(np.int16)).view(torch.bfloat16)
+    kv = t(inp.kv.view(np.int16)).view(torch.bfloat16)
+    w = t(inp.w.view(np.int16)).view(torch.bfloat16)
+    cache = t(inp.poison)
+    k.qnorm_rope_kv_rope_quant_insert(q, kv, t(inp.positions), t(inp.cos_sin), t(inp.slots), cache,
+                                      wl.num_blocks, wl.block_size, wl.eps)
+    torch.cuda.synchronize()
+    ref = harness.run_gpu(inp, kv_norm=False)
+    assert np.array_equal(cache.cpu().numpy(), ref.cache)
+    assert np.array_equal(q.cpu().view(torch.int16).numpy().view(np.uint16), ref.q)
+    cache2 = t(inp.poison)
+    k.kv_norm_rope_insert(k.STORE_FP8, kv, w, t(inp.positions), t(inp.cos_sin), t(inp.slots),
+                          cache2, wl.num_blocks, wl.block_size, wl.eps)
+    torch.cuda.synchronize()
+    ref2 = harness.run_gpu(inp)
+    assert np.array_equal(cache2.cpu().numpy(), ref2.cache)
