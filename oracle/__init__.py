@@ -55,6 +55,9 @@ def _load():
         for name in ("oracle_bf16_rne_array", "oracle_e4m3_rne_array",
                      "oracle_bf16_value_array", "oracle_ue8m0_exponent_array"):
             getattr(lib, name).argtypes = [vp, vp, i64]
+        lib.oracle_e4m3_value_array.argtypes = [vp, vp, i64]
+        lib.oracle_dequant_gather.argtypes = [vp, i64, i32, vp, i64, vp]
+        lib.oracle_dequant_gather.restype = i32
         lib.oracle_ue8m0_exponent.argtypes = [ctypes.c_double]
         lib.oracle_ue8m0_exponent.restype = ctypes.c_int
         _lib = lib
@@ -167,3 +170,21 @@ def ue8m0_exponent(amax: np.ndarray) -> np.ndarray:
     out = np.empty(a.shape, dtype=np.int32)
     _load().oracle_ue8m0_exponent_array(a.ctypes.data, out.ctypes.data, a.size)
     return out
+
+
+def e4m3_value(codes: np.ndarray) -> np.ndarray:
+    c = _c(codes, np.uint8)
+    out = np.empty(c.shape, dtype=np.float64)
+    _load().oracle_e4m3_value_array(c.ctypes.data, out.ctypes.data, c.size)
+    return out
+
+
+def dequant_gather(cache: np.ndarray, num_blocks: int, block_size: int, slots: np.ndarray):
+    """(bf16 bits [n, 512], error bits): rows of an FP8 cache read back out."""
+    cache = _c(cache, np.uint8)
+    assert cache.size == num_blocks * block_size * FP8_SLOT_BYTES
+    sl = _c(slots, np.int64)
+    out = np.empty((sl.size, 512), dtype=np.uint16)
+    err = _load().oracle_dequant_gather(cache.ctypes.data, num_blocks, block_size, sl.ctypes.data,
+                                        sl.size, out.ctypes.data)
+    return out, int(err)

@@ -367,6 +367,61 @@ int32_t oracle_qnorm_rope_kv_insert(int store_bf16, int kv_norm, uint16_t *q, co
     return err;
 }
 
+/* ------------------------------------------- reading the FP8 cache back out */
+
+/* exact value of an E4M3 ("fn") code: bias 7, subnormals m * 2^-9, 0x7F/0xFF NaN */
+double oracle_e4m3_value(uint8_t code)
+{
+    int sign = code >> 7;
+    int ef = (code >> 3) & 0xF;
+    int m = code & 7;
+    double mag;
+    if (ef == 15 && m == 7)
+        mag = NAN;
+    else if (ef == 0)
+        mag = ldexp((double)m, -9);
+    else
+        mag = ldexp((double)(8 + m), ef - 10); /* (1 + m/8) * 2^(ef-7) */
+    return sign ? -mag : mag;
+}
+
+/*
+ * Dequantise-and-gather: out[n, :] (bf16 [n_rows, 512]) = the row stored at
+ * slots[n] of an FP8 cache (layout of oracle_fp8_slot), dims 0..447 as
+ * bf16(E4M3 value * 2^(e_b - 127)), dims 448..511 copied.  A negative slot
+ * gives a zero row (the sparse-attention gather of 1Cat-vLLM PR #1280,
+ * "Purpose" item 2, writes zeros for unused slots); a slot past the cache
+ * also gives a zero row and sets ERR_SLOT_RANGE.  The reader of the cache
+ * (same PR, item 5: dequantize_and_gather_k_cache).
+ */
+int32_t oracle_dequant_gather(const uint8_t *cache, int64_t num_blocks, int32_t block_size,
+                              const int64_t *slots, int64_t n_rows, uint16_t *out)
+{
+    int32_t err = 0;
+    const int64_t num_slots = num_blocks * (int64_t)block_size;
+    for (int64_t n = 0; n < n_rows; ++n) {
+        uint16_t *row = out + n * HEAD;
+        int64_t slot = slots[n];
+        if (slot < 0 || slot >= num_slots) {
+            if (slot >= num_slots)
+                err |= ERR_SLOT_RANGE;
+            memset(row, 0, HEAD * sizeof(uint16_t));
+            continue;
+        }
+        int64_t blk = slot / block_size, off = slot % block_size;
+        const uint8_t *base = cache + blk * (int64_t)block_size * FP8_SLOT_BYTES;
+        const uint8_t *data = base + off * FP8_DATA_BYTES;
+        const uint8_t *scale = base + (int64_t)block_size * FP8_DATA_BYTES + off * FP8_SCALE_BYTES;
+        for (int d = 0; d < NOPE; ++d)
+            row[d] = oracle_bf16_rne(ldexp(oracle_e4m3_value(data[d]), (int)scale[d / QBLK] - 127));
+        for (int d = NOPE; d < HEAD; ++d) {
+            const uint8_t *p = data + NOPE + 2 * (d - NOPE);
+            row[d] = (uint16_t)(p[0] | (p[1] << 8));
+        }
+    }
+    return err;
+}
+
 /* ------------------------------------------------- array forms for the tests */
 
 void oracle_bf16_rne_array(const double *x, uint16_t *out, int64_t n)
@@ -385,6 +440,12 @@ void oracle_bf16_value_array(const uint16_t *b, double *out, int64_t n)
 {
     for (int64_t i = 0; i < n; ++i)
         out[i] = oracle_bf16_value(b[i]);
+}
+
+void oracle_e4m3_value_array(const uint8_t *c, double *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = oracle_e4m3_value(c[i]);
 }
 
 void oracle_ue8m0_exponent_array(const double *amax, int32_t *out, int64_t n)

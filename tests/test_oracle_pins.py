@@ -346,3 +346,65 @@ def test_prenormalised_driver_ignores_weight_and_eps():
     h1 = next(c for c in CASES["kv_cases"] if c["name"] == "H1_constant_row")
     assert np.array_equal(cache[576 * 3:576 * 4], _expand_bytes(h3["fp8_data"], 576))
     assert np.array_equal(cache[576:1152], _expand_bytes(h1["fp8_data"], 576))
+
+
+# ---------------------------------------------------------------- reading the cache back
+
+def test_e4m3_decode_matches_torch_for_every_code():
+    import torch
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = oracle.e4m3_value(codes)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+    assert np.array_equal(np.signbit(got[ok]), np.signbit(ref[ok]))
+
+
+@pytest.mark.parametrize("case", CASES["gather_cases"], ids=lambda c: c["name"])
+def test_golden_gather_rows(case):
+    src = next(c for c in CASES["kv_cases"] if c["name"] == case["of"])
+    cache = np.zeros(584, np.uint8)
+    cache[:576] = _expand_bytes(src["fp8_data"], 576)
+    cache[576:584] = _expand_bytes(src["fp8_scale"], 8)
+    out, err = oracle.dequant_gather(cache, 1, 1, np.array([0, -1, 0], np.int64))
+    assert err == 0
+    assert np.array_equal(out[0], _expand_bf16_row(case["row"]))
+    assert np.array_equal(out[2], out[0]) and np.all(out[1] == 0)
+
+
+def test_gather_round_trip_bound():
+    """gather(insert(x)) is within half an E4M3 step (times the block scale) of the
+    exact v on the quantised dims, and equals bf16(v) on the rope dims."""
+    from synth import configs
+    wl = configs.generic(300, 1, seed=61, tail_frac=0.02, tail_mult=100.0)
+    kv = configs.kv_bits(wl).reshape(wl.T, 512)
+    w = configs.weight_bits(wl)
+    cs = configs.cos_sin(wl)
+    pos = wl.positions()
+    slots = synth.permutation(wl.num_slots, 5, 5)[: wl.T]
+    cache = np.zeros(wl.num_slots * 584, np.uint8)
+    assert oracle.qnorm_rope_kv_insert("fp8", None, kv, w, pos, cs, slots, cache, wl.num_blocks,
+                                       wl.block_size, wl.eps) == 0
+    out, err = oracle.dequant_gather(cache, wl.num_blocks, wl.block_size, slots)
+    assert err == 0
+    got = oracle.bf16_value(out)
+    for t in range(wl.T):
+        v = oracle.kv_values(kv[t], w, cs[pos[t]], wl.eps)
+        scale = cache.reshape(wl.num_blocks, -1)[slots[t] // 64, 64 * 576 + 8 * (slots[t] % 64):][:7]
+        for b in range(7):
+            s = 2.0 ** (int(scale[b]) - 127)
+            a = np.abs(v[64 * b:64 * b + 64]) / s
+            e = np.floor(np.log2(np.maximum(a, 2.0**-6)))
+            half_step = 2.0 ** (e - 3) / 2 * s
+            assert np.all(np.abs(got[t, 64 * b:64 * b + 64] - v[64 * b:64 * b + 64])
+                          <= half_step * (1 + 1e-12))
+        assert np.array_equal(out[t, 448:], oracle.bf16_rne(v[448:]))
+
+
+def test_gather_skips_and_flags():
+    cache = synth.poison_bytes(2 * 4 * 584, seed=8)
+    out, err = oracle.dequant_gather(cache, 2, 4, np.array([-1, 8, 100, -7], np.int64))
+    assert err == oracle.ERR_SLOT_RANGE and np.all(out == 0)
+    out, err = oracle.dequant_gather(cache, 2, 4, np.array([-1, 3], np.int64))
+    assert err == 0 and np.all(out[0] == 0)
