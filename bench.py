@@ -210,7 +210,7 @@ def copy_ceiling_gbs(dev, nbytes: int) -> float:
 
 # ------------------------------------------------------------------ inputs on the device
 
-OPS = ("fused", "prenorm", "kv_only")
+OPS = ("fused", "prenorm", "kv_only", "gather")
 
 
 class DeviceBatch:
@@ -221,7 +221,7 @@ class DeviceBatch:
 
     def __init__(self, wl: configs.Workload, dev, op: str = "fused"):
         import torch
-        if op == "kv_only":
+        if op in ("kv_only", "gather"):
             wl = dataclasses.replace(wl, H=0)
         self.wl = wl
         self.op = op
@@ -241,6 +241,16 @@ class DeviceBatch:
         self.bytes = configs.algorithmic_bytes(wl, self.positions_np, self.slots_np)
         if op == "prenorm":
             self.bytes -= 1024  # no weight read
+        if op == "gather":
+            if wl.store != "fp8":
+                raise ValueError("the reader reads FP8 caches")
+            import kv_norm_rope_gb300 as k
+            k.kv_norm_rope_insert(k.STORE_FP8, self.kv, self.w, self.pos, self.cs, self.slots,
+                                  self.cache, wl.num_blocks, wl.block_size, wl.eps)
+            del self.kv
+            self.out = torch.empty((wl.T, 512), dtype=torch.bfloat16, device=dev)
+            valid = int((self.slots_np >= 0).sum())
+            self.bytes = wl.T * (8 + 1024) + valid * 584
 
     def _normal(self, shape, g):
         import torch
@@ -261,6 +271,10 @@ class DeviceBatch:
     def call(self, lib, stream_handle: int):
         """(C-ABI function, argument tuple) of one step of this batch's op."""
         wl = self.wl
+        if self.op == "gather":
+            return lib.dsv4_dequant_gather, (
+                self.cache.data_ptr(), wl.num_blocks, wl.block_size, self.slots.data_ptr(), wl.T,
+                self.out.data_ptr(), self.err.data_ptr(), stream_handle)
         if self.op == "kv_only":
             return lib.dsv4_kv_norm_rope_insert, (
                 0 if wl.store == "fp8" else 1, self.kv.data_ptr(), self.w.data_ptr(),
@@ -570,7 +584,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(configs.WORKLOADS), default="stress")
     ap.add_argument("--op", choices=OPS, default="fused",
-                    help="fused (default); prenorm: KV arrives normalised; kv_only: no q")
+                    help="fused (default); prenorm: KV arrives normalised; kv_only: no q; "
+                         "gather: read the FP8 cache back out")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -189,6 +189,25 @@ int dsv4_insert_ex(int store_mode, int variant, int kv_norm, void *q, const void
                    void *kv_cache, int64_t num_blocks, int32_t block_size, int64_t num_tokens,
                    int32_t num_heads, float eps, int32_t *device_error, void *stream);
 
+/*
+ * Read rows of an FP8 cache back out as bf16 (1Cat-vLLM PR #1280, "Purpose"
+ * item 5: the dequantize-and-gather of the compressed KV cache; item 2: the
+ * gather writes zeros for unused slots).
+ *
+ *  kv_cache  (device) uint8, FP8 layout of dsv4_qnorm_rope_kv_quant_insert; 8-byte aligned.
+ *  slots     (device) int64 [num_rows]: slot = block*block_size + offset.
+ *  out       (device) bf16 [num_rows, 512], 16-byte aligned: row n = bf16(E4M3 value *
+ *            2^(e_b - 127)) for dims 0..447 (b = dim / 64) and the stored bf16 for
+ *            448..511 -- exact for every row the insert kernels write.  A negative
+ *            slot gives a zero row; a slot >= num_blocks*block_size gives a zero row
+ *            and DSV4_DEVERR_SLOT_RANGE.
+ *  num_rows >= 0 (0: no launch); num_blocks, block_size >= 1.
+ * Returns a dsv4_status.
+ */
+int dsv4_dequant_gather(const uint8_t *kv_cache, int64_t num_blocks, int32_t block_size,
+                        const int64_t *slots, int64_t num_rows, void *out,
+                        int32_t *device_error, void *stream);
+
 /* Launch plan of a call (pure host arithmetic, no CUDA call). */
 typedef struct {
     int32_t variant;        /* DSV4_VARIANT_SMALL or DSV4_VARIANT_STREAM */

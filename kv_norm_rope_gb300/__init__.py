@@ -20,7 +20,7 @@ _ROOT = os.path.dirname(_HERE)
 _CSRC = os.path.join(_HERE, "csrc")
 _INCLUDE = os.path.join(_ROOT, "include")
 LIB_PATH = os.path.join(_HERE, "libdsv4kv.so")
-_SOURCES = ["qnorm_rope_kv_insert.cu", "api.cpp"]
+_SOURCES = ["qnorm_rope_kv_insert.cu", "dequant_gather.cu", "api.cpp"]
 _HEADERS = [os.path.join(_INCLUDE, "dsv4kv.h"), os.path.join(_CSRC, "launch.h")]
 NVCC_ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -33,7 +33,7 @@ FP8_SLOT_BYTES, BF16_SLOT_BYTES = 584, 1024
 
 EXPORTS = ("dsv4_qnorm_rope_kv_quant_insert", "dsv4_qnorm_rope_kv_bf16_insert",
            "dsv4_qnorm_rope_kv_insert_variant", "dsv4_qnorm_rope_kv_rope_quant_insert",
-           "dsv4_kv_norm_rope_insert", "dsv4_insert_ex", "dsv4_launch_plan",
+           "dsv4_kv_norm_rope_insert", "dsv4_insert_ex", "dsv4_dequant_gather", "dsv4_launch_plan",
            "dsv4_fp8_cache_bytes", "dsv4_bf16_cache_bytes", "dsv4_status_string")
 
 
@@ -113,6 +113,8 @@ def lib():
         L.dsv4_kv_norm_rope_insert.argtypes = [c_int, vp, vp, vp, vp, i64, vp, vp, i64, i32, i64,
                                                f32, vp, vp]
         L.dsv4_kv_norm_rope_insert.restype = c_int
+        L.dsv4_dequant_gather.argtypes = [vp, i64, i32, vp, i64, vp, vp, vp]
+        L.dsv4_dequant_gather.restype = c_int
         L.dsv4_launch_plan.argtypes = [i64, i32, i32, i32, i32, ctypes.POINTER(Plan)]
         L.dsv4_launch_plan.restype = c_int
         L.dsv4_fp8_cache_bytes.argtypes = [i64, i32]
@@ -252,3 +254,13 @@ def qnorm_rope_kv_bf16_insert(q, kv, kv_norm_weight, positions, cos_sin_cache, s
         _ptr(device_error), _stream_handle(stream))
     if st != OK:
         raise Dsv4Error(st, "dsv4_qnorm_rope_kv_bf16_insert")
+
+
+def dequant_gather(kv_cache, num_blocks: int, block_size: int, slots, out, device_error=None,
+                   stream=None) -> None:
+    """dsv4_dequant_gather: out (bf16 [n, 512]) = FP8 cache rows at ``slots`` read back."""
+    st = lib().dsv4_dequant_gather(_ptr(kv_cache), num_blocks, block_size, _ptr(slots),
+                                   int(slots.shape[0]), _ptr(out), _ptr(device_error),
+                                   _stream_handle(stream))
+    if st != OK:
+        raise Dsv4Error(st, "dsv4_dequant_gather")

@@ -231,6 +231,36 @@ int dsv4_insert_ex(int store_mode, int variant, int kv_norm, void *q, const void
                   block_size, num_tokens, num_heads, eps, device_error, stream);
 }
 
+int dsv4_dequant_gather(const uint8_t *kv_cache, int64_t num_blocks, int32_t block_size,
+                        const int64_t *slots, int64_t num_rows, void *out,
+                        int32_t *device_error, void *stream)
+{
+    if (num_rows < 0 || num_blocks < 1 || block_size < 1)
+        return DSV4_ERR_SHAPE;
+    if (num_blocks > (INT64_MAX / 4096) / block_size || num_rows > INT64_MAX / 4096)
+        return DSV4_ERR_SHAPE;
+    if (num_rows == 0)
+        return DSV4_OK;
+    if (!kv_cache || !slots || !out)
+        return DSV4_ERR_NULL;
+    if (!aligned(kv_cache, 8) || !aligned(slots, 8) || !aligned(out, 16) ||
+        !aligned(device_error, 4))
+        return DSV4_ERR_ALIGN;
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        dsv4::gather_ctas_per_sm(&per_sm) != DSV4_OK || sms < 1 || per_sm < 1)
+        return DSV4_ERR_CUDA;
+    const int64_t groups = (num_rows + dsv4::gather_rows_per_warp() - 1) /
+                           dsv4::gather_rows_per_warp();
+    const int64_t need = (groups + 7) / 8;  // 8 warps per CTA
+    const int64_t resident = int64_t(sms) * per_sm;
+    return dsv4::launch_gather(kv_cache, num_blocks, block_size, slots, num_rows,
+                               static_cast<uint16_t *>(out), device_error,
+                               need < resident ? need : resident,
+                               static_cast<cudaStream_t>(stream));
+}
+
 size_t dsv4_fp8_cache_bytes(int64_t num_blocks, int32_t block_size)
 {
     if (num_blocks < 1 || block_size < 1)

@@ -1,0 +1,179 @@
+// Reading the FP8 paged cache back out (the consumer of the insert kernels):
+// out[n, :] = the 512 dims stored at slot slots[n], as bf16.  Dims 0..447 are
+// E4M3 payload times 2^(e_b - 127) of their 64-dim block; dims 448..511 are
+// the stored bf16 rope dims.  A negative slot gives a zero row, a slot past the
+// cache a zero row and an error bit.  (1Cat-vLLM PR #1280, "Purpose": item 5,
+// the dequantize-and-gather of the compressed KV cache; item 2, zeros for
+// unused slots.)
+//
+// HBM-bound: per row 584 bytes read and 1024 written.  One warp per row with
+// the insert kernels' lane layout (lane l: dims [8l, 8l+8) and [256+8l,
+// 256+8l+8)), so each 8-byte load instruction covers 256 contiguous cache
+// bytes and each 16-byte store 512 contiguous output bytes; several rows per
+// warp are loaded back to back before any is used.  Every value is exact:
+// an E4M3 code times a power of two fits fp32 for every scale the writer
+// emits, so the one rounding is the final bf16 conversion.
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "launch.h"
+
+namespace dsv4 {
+namespace {
+
+constexpr int kGatherRows = 4;
+
+struct GParams {
+    const uint8_t *cache;
+    int64_t num_slots;
+    int32_t block_size;
+    const int64_t *slots;
+    int64_t rows;
+    uint16_t *out;
+    int32_t *err;
+};
+
+// two E4M3 codes (low byte first) -> two fp32, exact
+__device__ __forceinline__ float2 e4m3x2_to_f32(uint32_t two_codes)
+{
+    uint32_t h2;
+    const unsigned short c = static_cast<unsigned short>(two_codes);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c));
+    float2 f;
+    asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "cvt.f32.f16 %0, lo;\n\tcvt.f32.f16 %1, hi;\n\t}"
+        : "=f"(f.x), "=f"(f.y)
+        : "r"(h2));
+    return f;
+}
+
+// p * 2^(e - 127), exact in fp32 for every E4M3 value p and e in [0, 254]
+__device__ __forceinline__ float scaled(float p, uint32_t e)
+{
+    if (e >= 1u && e <= 254u)
+        return __fmul_rn(p, __uint_as_float(e << 23));
+    if (e == 0u)  // 2^-127 in two exact steps (|p| >= 2^-9, so no bit falls below 2^-149)
+        return __fmul_rn(__fmul_rn(p, 0x1p-64f), 0x1p-63f);
+    return __fmul_rn(__fmul_rn(p, 0x1p64f), 0x1p64f);  // 2^128: beyond bf16, becomes inf
+}
+
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// 8 payload bytes (one 64-bit word) with scale byte e -> 8 bf16 (one 16-byte vector)
+__device__ __forceinline__ uint4 dequant8(uint2 codes, uint32_t e)
+{
+    float2 f[4];
+    f[0] = e4m3x2_to_f32(codes.x);
+    f[1] = e4m3x2_to_f32(codes.x >> 16);
+    f[2] = e4m3x2_to_f32(codes.y);
+    f[3] = e4m3x2_to_f32(codes.y >> 16);
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        o[i] = bf16x2_rn(scaled(f[i].x, e), scaled(f[i].y, e));
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__device__ __forceinline__ uint2 ld8(const uint8_t *p)
+{
+    return __ldcs(reinterpret_cast<const uint2 *>(p));
+}
+
+__global__ void __launch_bounds__(256) dequant_gather_kernel(const GParams p)
+{
+    const int lane = threadIdx.x & 31;
+    const int warps_per_cta = blockDim.x >> 5;
+    const int64_t groups = (p.rows + kGatherRows - 1) / kGatherRows;
+    const int64_t stride = int64_t(gridDim.x) * warps_per_cta;
+    const bool rope_lane = lane >= 24;
+
+    for (int64_t g = int64_t(blockIdx.x) * warps_per_cta + (threadIdx.x >> 5); g < groups;
+         g += stride) {
+        const int64_t r0 = g * kGatherRows;
+        int64_t slot[kGatherRows];
+#pragma unroll
+        for (int j = 0; j < kGatherRows; ++j)
+            slot[j] = r0 + j < p.rows ? __ldg(p.slots + r0 + j) : -1;
+        // all loads of the group back to back
+        uint2 lo[kGatherRows], hi0[kGatherRows], hi1[kGatherRows], sc[kGatherRows];
+#pragma unroll
+        for (int j = 0; j < kGatherRows; ++j) {
+            lo[j] = hi0[j] = hi1[j] = sc[j] = make_uint2(0u, 0u);
+            if (slot[j] >= 0 && slot[j] < p.num_slots) {
+                const int64_t blk = slot[j] / p.block_size;
+                const int64_t off = slot[j] - blk * p.block_size;
+                const uint8_t *base = p.cache + blk * int64_t(p.block_size) * DSV4_FP8_SLOT_BYTES;
+                const uint8_t *data = base + off * DSV4_FP8_DATA_BYTES;
+                lo[j] = ld8(data + 8 * lane);
+                if (!rope_lane) {
+                    hi0[j] = ld8(data + 256 + 8 * lane);
+                } else {
+                    hi0[j] = ld8(data + DSV4_NOPE_DIM + 16 * (lane - 24));
+                    hi1[j] = ld8(data + DSV4_NOPE_DIM + 16 * (lane - 24) + 8);
+                }
+                sc[j] = __ldg(reinterpret_cast<const uint2 *>(
+                    base + int64_t(p.block_size) * DSV4_FP8_DATA_BYTES + off * DSV4_FP8_SCALE_BYTES));
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kGatherRows; ++j) {
+            if (r0 + j >= p.rows)
+                break;
+            uint16_t *row = p.out + (r0 + j) * DSV4_HEAD_DIM;
+            uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
+            if (slot[j] >= p.num_slots) {
+                if (lane == 0 && p.err != nullptr)
+                    atomicOr(p.err, DSV4_DEVERR_SLOT_RANGE);
+            } else if (slot[j] >= 0) {
+                // scale byte of block lane/8 (half 0) and 4 + lane/8 (half 1)
+                const int b0 = lane >> 3, b1 = 4 + (lane >> 3);
+                const uint32_t e0 = (b0 < 4 ? sc[j].x >> (8 * b0) : 0u) & 0xFFu;
+                const uint32_t e1 = (sc[j].y >> (8 * (b1 - 4))) & 0xFFu;
+                a = dequant8(lo[j], e0);
+                b = rope_lane ? make_uint4(hi0[j].x, hi0[j].y, hi1[j].x, hi1[j].y)
+                              : dequant8(hi0[j], e1);
+            }
+            __stcs(reinterpret_cast<uint4 *>(row + 8 * lane), a);
+            __stcs(reinterpret_cast<uint4 *>(row + 256 + 8 * lane), b);
+        }
+    }
+}
+
+}  // namespace
+
+int gather_ctas_per_sm(int *ctas_per_sm)
+{
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, dequant_gather_kernel, 256,
+                                                         0) == cudaSuccess
+               ? DSV4_OK
+               : DSV4_ERR_CUDA;
+}
+
+int launch_gather(const uint8_t *cache, int64_t num_blocks, int32_t block_size,
+                  const int64_t *slots, int64_t rows, uint16_t *out, int32_t *err, int64_t ctas,
+                  cudaStream_t stream)
+{
+    GParams p;
+    p.cache = cache;
+    p.num_slots = num_blocks * int64_t(block_size);
+    p.block_size = block_size;
+    p.slots = slots;
+    p.rows = rows;
+    p.out = out;
+    p.err = err;
+    dequant_gather_kernel<<<unsigned(ctas), 256, 0, stream>>>(p);
+    return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
+}
+
+int gather_rows_per_warp()
+{
+    return kGatherRows;
+}
+
+}  // namespace dsv4

@@ -38,4 +38,11 @@ int stream_ctas_per_sm(int store_mode, int *ctas_per_sm);
 // Enqueue the kernel described by `plan` on `stream`; returns a dsv4_status.
 int launch(int store_mode, const dsv4_plan &plan, const LaunchArgs &args, cudaStream_t stream);
 
+// The FP8 cache reader (dequant_gather.cu).
+int gather_ctas_per_sm(int *ctas_per_sm);
+int gather_rows_per_warp();
+int launch_gather(const uint8_t *cache, int64_t num_blocks, int32_t block_size,
+                  const int64_t *slots, int64_t rows, uint16_t *out, int32_t *err, int64_t ctas,
+                  cudaStream_t stream);
+
 }  // namespace dsv4

@@ -176,3 +176,15 @@ def test_kv_only_and_prenormalised_entries_validate():
                                                     None, None) == k.ERR_NULL
     assert lib.dsv4_qnorm_rope_kv_rope_quant_insert(A, A, A, A, 4096, A, A, 4, 64, 0, 8, 1e-6,
                                                     None, None) == k.OK
+
+
+@pytest.mark.parametrize("args,status", [
+    ((A, 4, 64, A, -1, A, None), k.ERR_SHAPE), ((A, 0, 64, A, 5, A, None), k.ERR_SHAPE),
+    ((A, 4, 0, A, 5, A, None), k.ERR_SHAPE), ((None, 4, 64, A, 5, A, None), k.ERR_NULL),
+    ((A, 4, 64, None, 5, A, None), k.ERR_NULL), ((A, 4, 64, A, 5, None, None), k.ERR_NULL),
+    ((A + 4, 4, 64, A, 5, A, None), k.ERR_ALIGN), ((A, 4, 64, A + 4, 5, A, None), k.ERR_ALIGN),
+    ((A, 4, 64, A, 5, A + 8, None), k.ERR_ALIGN), ((A, 4, 64, A, 5, A, A + 1), k.ERR_ALIGN),
+    ((A + 8, 3, 7, A, 0, A, None), k.OK),
+])
+def test_gather_validation(args, status):
+    assert k.lib().dsv4_dequant_gather(*args, None) == status
