@@ -86,7 +86,8 @@ def barrier(world: int):
 
 # ------------------------------------------------------------------ measurement helpers
 
-KERNEL_SOURCES = ("kv_norm_rope_gb300/csrc/qnorm_rope_kv_insert.cu", "kv_norm_rope_gb300/csrc/launch.h")
+KERNEL_SOURCES = ("kv_norm_rope_gb300/csrc/qnorm_rope_kv_insert.cu", "kv_norm_rope_gb300/csrc/rowmath.cuh",
+                  "kv_norm_rope_gb300/csrc/launch.h")
 
 
 def kernel_fingerprint() -> str:
@@ -211,6 +212,7 @@ def copy_ceiling_gbs(dev, nbytes: int) -> float:
 # ------------------------------------------------------------------ inputs on the device
 
 OPS = ("fused", "prenorm", "kv_only", "gather")
+VARIANTS = {"auto": 0, "small": 1, "stream": 2, "bulk": 3}
 
 
 class DeviceBatch:
@@ -219,8 +221,9 @@ class DeviceBatch:
     slots, the weight and the cos/sin table come from ``synth``.  ``op`` "kv_only"
     holds no q."""
 
-    def __init__(self, wl: configs.Workload, dev, op: str = "fused"):
+    def __init__(self, wl: configs.Workload, dev, op: str = "fused", variant: int = 0):
         import torch
+        self.variant = variant
         if op in ("kv_only", "gather"):
             wl = dataclasses.replace(wl, H=0)
         self.wl = wl
@@ -286,6 +289,12 @@ class DeviceBatch:
                 raise ValueError("the pre-normalised entry stores FP8 rows")
             return lib.dsv4_qnorm_rope_kv_rope_quant_insert, (
                 self.q.data_ptr(), self.kv.data_ptr(), self.pos.data_ptr(), self.cs.data_ptr(),
+                wl.max_position, self.slots.data_ptr(), self.cache.data_ptr(), wl.num_blocks,
+                wl.block_size, wl.T, wl.H, wl.eps, self.err.data_ptr(), stream_handle)
+        if self.variant:
+            return lib.dsv4_insert_ex, (
+                0 if wl.store == "fp8" else 1, self.variant, 1, self.q.data_ptr(),
+                self.kv.data_ptr(), self.w.data_ptr(), self.pos.data_ptr(), self.cs.data_ptr(),
                 wl.max_position, self.slots.data_ptr(), self.cache.data_ptr(), wl.num_blocks,
                 wl.block_size, wl.T, wl.H, wl.eps, self.err.data_ptr(), stream_handle)
         fn = (lib.dsv4_qnorm_rope_kv_quant_insert if wl.store == "fp8"
@@ -474,7 +483,7 @@ def run_ours(args):
     kac_before = known_answer_check() if rank == 0 else "skipped"
     copy_1g = copy_ceiling_gbs(dev, 1 << 30)
     copy_512m = copy_ceiling_gbs(dev, 1 << 29)
-    batch = DeviceBatch(wl, dev, args.op)
+    batch = DeviceBatch(wl, dev, args.op, VARIANTS[args.variant])
     wl = batch.wl
     stream = torch.cuda.current_stream(dev)
     fn, call_args = batch.call(lib, stream.cuda_stream)
@@ -544,7 +553,9 @@ def run_ours(args):
                    "l2": "flushed before every launch (256 MB write)" if flush is not None
                    else f"inputs larger than L2 ({batch.bytes / 1e9:.2f} GB per step)",
                    "io": "bf16 in; bf16 q, e4m3+ue8m0+bf16 cache out",
-                   "variant": "stream" if plan.variant == k.VARIANT_STREAM else "small",
+                   "variant": args.variant if args.variant != "auto" else
+                   {k.VARIANT_STREAM: "stream", k.VARIANT_SMALL: "small",
+                    k.VARIANT_BULK: "bulk"}[plan.variant],
                    "parallelism": f"dp{world}" if world > 1 else "single"},
         "tokens_per_s": round(total_tokens / t_step, 1),
         "frac_of_copy_ceiling": round(value / world / copy_1g, 4),
@@ -583,6 +594,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(configs.WORKLOADS), default="stress")
+    ap.add_argument("--variant", choices=sorted(VARIANTS), default="auto",
+                    help="launch variant of the fused op (default: the library's choice)")
     ap.add_argument("--op", choices=OPS, default="fused",
                     help="fused (default); prenorm: KV arrives normalised; kv_only: no q; "
                          "gather: read the FP8 cache back out")

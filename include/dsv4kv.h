@@ -70,7 +70,9 @@ enum {
 /* bits OR-ed into *device_error */
 enum {
     DSV4_DEVERR_SLOT_RANGE = 1, /* slot_mapping[t] >= num_blocks*block_size: cache row not written */
-    DSV4_DEVERR_POS_RANGE = 2   /* positions[t] < 0 or >= max_position: token not written at all */
+    DSV4_DEVERR_POS_RANGE = 2,  /* positions[t] < 0 or >= max_position: token not written at all */
+    DSV4_DEVERR_TIMEOUT = 4     /* DSV4_VARIANT_BULK only: a bounded wait inside the kernel ran out
+                                   (never expected); the outputs of that launch are undefined */
 };
 
 /* store modes and launch variants of dsv4_qnorm_rope_kv_insert_variant */
@@ -78,7 +80,9 @@ enum { DSV4_STORE_FP8 = 0, DSV4_STORE_BF16 = 1 };
 enum {
     DSV4_VARIANT_AUTO = 0,    /* pick from the row count and the SM count (below) */
     DSV4_VARIANT_SMALL = 1,   /* one row per warp, 2-warp CTAs, one wave: small batches */
-    DSV4_VARIANT_STREAM = 2   /* persistent CTAs sized to the SMs, several rows in flight per warp */
+    DSV4_VARIANT_STREAM = 2,  /* persistent CTAs sized to the SMs, several rows in flight per warp */
+    DSV4_VARIANT_BULK = 3     /* one CTA per SM; 16-row chunks staged through shared memory by the
+                                 bulk-copy (TMA) engine, 12 in flight; q chunks written back in bulk */
 };
 
 /*
@@ -222,7 +226,8 @@ typedef struct {
  * ctas_per_sm CTAs of the streaming kernel fit per SM.  variant AUTO picks
  * SMALL when the rows would not give every warp slot of the GPU at least a
  * full group of rows, else STREAM (SGLang PR #33358, "Modifications" item 3:
- * a grid-starved multi-token layout loses at small N).  Returns a dsv4_status.
+ * a grid-starved multi-token layout loses at small N).  BULK runs one CTA
+ * per SM (at most one per 16-row chunk).  Returns a dsv4_status.
  */
 int dsv4_launch_plan(int64_t num_tokens, int32_t num_heads, int32_t sm_count,
                      int32_t ctas_per_sm, int32_t variant, dsv4_plan *plan);

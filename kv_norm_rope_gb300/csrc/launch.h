@@ -32,11 +32,35 @@ struct LaunchArgs {
     bool kv_norm;  // false: the KV rows arrive normalised (no norm, no weight)
 };
 
+// Kernel arguments (device pointers and sizes), shared by every kernel variant.
+struct KParams {
+    uint16_t *q;
+    const uint16_t *kv;
+    const uint16_t *w;
+    const int64_t *pos;
+    const float *cs;
+    int64_t max_pos;
+    const int64_t *slot;
+    uint8_t *cache;
+    int64_t num_slots;
+    int64_t num_tokens;
+    int32_t block_size;
+    int32_t num_heads;
+    float eps;
+    int32_t *err;
+};
+
 // CTAs of the streaming kernel for `store_mode` that fit on one SM.
 int stream_ctas_per_sm(int store_mode, int *ctas_per_sm);
 
 // Enqueue the kernel described by `plan` on `stream`; returns a dsv4_status.
 int launch(int store_mode, const dsv4_plan &plan, const LaunchArgs &args, cudaStream_t stream);
+
+// The shared-memory-staged variant (qnorm_rope_kv_insert_bulk.cu): one CTA per SM.
+size_t bulk_smem_bytes();
+int bulk_threads();
+int bulk_chunk_rows();
+int launch_bulk(int store_mode, bool kv_norm, int64_t ctas, const KParams &p, cudaStream_t stream);
 
 // The FP8 cache reader (dequant_gather.cu).
 int gather_ctas_per_sm(int *ctas_per_sm);

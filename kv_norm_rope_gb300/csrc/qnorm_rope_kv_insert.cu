@@ -43,397 +43,10 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "launch.h"
+#include "rowmath.cuh"
 
 namespace dsv4 {
 namespace {
-
-constexpr int kHead = DSV4_HEAD_DIM;
-constexpr unsigned kFull = 0xffffffffu;
-constexpr uint32_t kMant1p75 = 0x600000u;  // mantissa field of 1.75 (448 = 1.75 * 2^8)
-// Half-width of the fp32 "too close to call" band around a boundary, in units
-// of the fp32 mantissa field: 2^9 / 2^23 = 2^-14 relative.  The fp32 value of
-// an element is within ~14 ulp (2^-20) of its exact value: 16 sequential fmas
-// and a 5-level tree for the sum (<= 21 ulp, halved by the root), one ulp each
-// for the add of eps, the root, the reciprocal and two products.
-constexpr uint32_t kNearBand = 512u;
-
-struct KParams {
-    uint16_t *q;
-    const uint16_t *kv;
-    const uint16_t *w;
-    const int64_t *pos;
-    const float *cs;
-    int64_t max_pos;
-    const int64_t *slot;
-    uint8_t *cache;
-    int64_t num_slots;
-    int64_t num_tokens;
-    int32_t block_size;
-    int32_t num_heads;
-    float eps;
-    int32_t *err;
-};
-
-__device__ __forceinline__ uint4 ld_stream16(const void *p)
-{
-    return __ldcs(reinterpret_cast<const uint4 *>(p));
-}
-
-__device__ __forceinline__ void st_stream16(void *p, uint4 v)
-{
-    __stcs(reinterpret_cast<uint4 *>(p), v);
-}
-
-__device__ __forceinline__ void st_stream8(void *p, uint2 v)
-{
-    __stcs(reinterpret_cast<uint2 *>(p), v);
-}
-
-// 8 bf16 (one 16-byte vector) -> 8 fp32, exact
-__device__ __forceinline__ void widen8(uint4 u, float *f)
-{
-    f[0] = __uint_as_float(u.x << 16);
-    f[1] = __uint_as_float(u.x & 0xffff0000u);
-    f[2] = __uint_as_float(u.y << 16);
-    f[3] = __uint_as_float(u.y & 0xffff0000u);
-    f[4] = __uint_as_float(u.z << 16);
-    f[5] = __uint_as_float(u.z & 0xffff0000u);
-    f[6] = __uint_as_float(u.w << 16);
-    f[7] = __uint_as_float(u.w & 0xffff0000u);
-}
-
-// two fp32 -> bf16x2 (round to nearest even), `lo` in the low half
-__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi)
-{
-    uint32_t r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-
-__device__ __forceinline__ uint4 bf16x8_rn(const float *y)
-{
-    return make_uint4(bf16x2_rn(y[0], y[1]), bf16x2_rn(y[2], y[3]), bf16x2_rn(y[4], y[5]),
-                      bf16x2_rn(y[6], y[7]));
-}
-
-// four fp32 -> four E4M3 bytes (round to nearest even, saturating at +-448),
-// element 0 in the lowest byte.  The cvt instruction packs its first source
-// into the upper byte of each 16-bit half.
-__device__ __forceinline__ uint32_t e4m3x4_rn(float e0, float e1, float e2, float e3)
-{
-    uint32_t r;
-    asm("{\n\t"
-        ".reg .b16 p01, p23;\n\t"
-        "cvt.rn.satfinite.e4m3x2.f32 p01, %2, %1;\n\t"
-        "cvt.rn.satfinite.e4m3x2.f32 p23, %4, %3;\n\t"
-        "mov.b32 %0, {p01, p23};\n\t"
-        "}"
-        : "=r"(r)
-        : "f"(e0), "f"(e1), "f"(e2), "f"(e3));
-    return r;
-}
-
-__device__ __forceinline__ float warp_sum(float v)
-{
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1)
-        v = __fadd_rn(v, __shfl_xor_sync(kFull, v, m));
-    return v;
-}
-
-__device__ __forceinline__ double warp_sum(double v)
-{
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1)
-        v = __dadd_rn(v, __shfl_xor_sync(kFull, v, m));
-    return v;
-}
-
-// max over the 8 lanes that hold one 64-dim block
-__device__ __forceinline__ float group8_max(float v)
-{
-#pragma unroll
-    for (int m = 1; m <= 4; m <<= 1)
-        v = fmaxf(v, __shfl_xor_sync(kFull, v, m));
-    return v;
-}
-
-__device__ __forceinline__ bool group8_any(bool b)
-{
-    unsigned v = b ? 1u : 0u;
-#pragma unroll
-    for (int m = 1; m <= 4; m <<= 1)
-        v |= __shfl_xor_sync(kFull, v, m);
-    return v != 0u;
-}
-
-// a*c - b*s with one rounding error relative to the result, however much the
-// two products cancel: Kahan's algorithm for a 2x2 determinant (the fma
-// recovers the rounding error of b*s exactly), relative error at most 2^-23
-// (Jeannerod, Louvet and Muller, "Further analysis of Kahan's algorithm for
-// the accurate computation of 2x2 determinants", Math. Comp. 2013).
-__device__ __forceinline__ float det2(float a, float c, float b, float s)
-{
-    const float p = __fmul_rn(b, s);
-    const float e = __fmaf_rn(b, s, -p);  // b*s == p + e exactly
-    return __fsub_rn(__fmaf_rn(a, c, -p), e);
-}
-
-// The 8 rope dims 448+8j .. 455+8j held by lane 24+j (pairs 4j .. 4j+3):
-// out = r * rot(u), i.e. each pair (a, b) -> r * (a*c - b*s, b*c + a*s).
-// Rotating the unscaled inputs first keeps the result accurate when a pair
-// nearly cancels; the common factor r then costs one more rounding.
-__device__ __forceinline__ void rope8_scaled(const float *u, float4 c, float4 s, float r, float *out)
-{
-    const float cc[4] = {c.x, c.y, c.z, c.w};
-    const float ss[4] = {s.x, s.y, s.z, s.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float a = u[2 * i], b = u[2 * i + 1];
-        out[2 * i] = __fmul_rn(det2(a, cc[i], b, ss[i]), r);
-        out[2 * i + 1] = __fmul_rn(det2(b, cc[i], -a, ss[i]), r);
-    }
-}
-
-// 1 / sqrt(sum/512 + eps), each step correctly rounded
-__device__ __forceinline__ float inv_rms(float sum_sq, float eps)
-{
-    return __frcp_rn(__fsqrt_rn(__fadd_rn(__fmul_rn(sum_sq, 1.0f / 512.0f), eps)));
-}
-
-// 2^-s as fp32 for s in [-127, 127]
-__device__ __forceinline__ float pow2_neg(int s)
-{
-    return s == 127 ? __uint_as_float(0x00400000u) : __uint_as_float(uint32_t(127 - s) << 23);
-}
-
-// First guess of a block's UE8M0 exponent from its fp32 amax (>= 0).  With
-// amax = M * 2^E, M in [1, 2): the smallest s with amax <= 448 * 2^s is
-// E - 8 when M <= 1.75 and E - 7 otherwise.  `near` marks amax within the
-// fp32 error band of 1.75 * 2^E, where the exact value must decide.
-struct ScaleGuess {
-    int s;
-    int e;
-    bool near;
-};
-
-__device__ __forceinline__ ScaleGuess ue8m0_guess(float amax)
-{
-    const uint32_t bits = __float_as_uint(amax);
-    const int ef = int(bits >> 23);
-    const uint32_t m = bits & 0x7fffffu;
-    ScaleGuess g;
-    g.e = ef - 127;
-    if (ef == 0) {  // amax < 2^-126: the exponent is at most -134, clamped to -127
-        g.s = -127;
-        g.near = false;
-        return g;
-    }
-    const int s = g.e - 8 + (m > kMant1p75 ? 1 : 0);
-    g.near = m + kNearBand >= kMant1p75 && m <= kMant1p75 + kNearBand;
-    if (g.e - 7 <= -127 || g.e - 8 >= 127)  // both candidates clamp to the same value
-        g.near = false;
-    g.s = min(max(s, -127), 127);
-    return g;
-}
-
-// Exact decision for near blocks, taken by the whole warp when any block of
-// the KV row of token t is too close to call in fp32.  It reloads the row and
-// the weight (both still cached) rather than keep them live in registers,
-// recomputes the norm in fp64 and evaluates each element in the order of the
-// definition, (x * r) * w, against the boundary 1.75 * 2^e of its block.
-// Returns bit 0: the lane's half-0 block exceeds its boundary; bit 1: the
-// half-1 block does (both already OR-ed over the block's 8 lanes).
-__device__ __noinline__ int exact_scale_bumps(const KParams &p, int lane, int64_t t, int e0,
-                                              bool near0, int e1, bool near1)
-{
-    // rolled loops and scalar loads: this path is rare, its registers are not
-    const uint16_t *row = p.kv + t * kHead;
-    double ss = 0.0;
-#pragma unroll 1
-    for (int k = 0; k < 16; ++k) {
-        const int d = (k < 8 ? 0 : 248) + 8 * lane + k;
-        const double x = double(__uint_as_float(uint32_t(__ldg(row + d)) << 16));
-        ss = __fma_rn(x, x, ss);
-    }
-    ss = warp_sum(ss);
-    const double r = 1.0 / sqrt(ss / 512.0 + double(p.eps));
-    bool up0 = false, up1 = false;
-#pragma unroll 1
-    for (int k = 0; k < 16; ++k) {
-        const bool second = k >= 8;
-        if (!(second ? near1 : near0))
-            continue;
-        const int d = (second ? 248 : 0) + 8 * lane + k;
-        const double x = double(__uint_as_float(uint32_t(__ldg(row + d)) << 16));
-        const double w = double(__uint_as_float(uint32_t(__ldg(p.w + d)) << 16));
-        const double v = __dmul_rn(__dmul_rn(x, r), w);
-        const int e = second ? e1 : e0;
-        const double bound = __hiloint2double(int(uint32_t(1023 + e) << 20) | 0x000C0000, 0);
-        if (fabs(v) > bound) {
-            if (second)
-                up1 = true;
-            else
-                up0 = true;
-        }
-    }
-    return (group8_any(up0) ? 1 : 0) | (group8_any(up1) ? 2 : 0);
-}
-
-__device__ __forceinline__ int clamp_s(int s)
-{
-    return min(max(s, -127), 127);
-}
-
-__device__ __forceinline__ void flag_error(int32_t *err, int bit)
-{
-    if (err != nullptr)
-        atomicOr(err, bit);
-}
-
-// v = x * r * w for the lane's 16 dims of the KV row, then the rotation of
-// the rope dims (lanes 24..31).  Deterministic: calling it twice on the same
-// data gives the same bits.
-template <bool kSmemW, bool kKvNorm>
-__device__ __forceinline__ void kv_values(const KParams &p, int lane, uint4 xa, uint4 xb,
-                                          float4 cv, float4 sv, const uint4 *w_smem, float *v)
-{
-    widen8(xa, v);
-    widen8(xb, v + 8);
-    if (!kKvNorm) {
-        // the row arrives normalised: v = x (exact), only the rope dims turn
-        if (lane >= 24) {
-            float u[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                u[k] = v[8 + k];
-            rope8_scaled(u, cv, sv, 1.0f, v + 8);
-        }
-        return;
-    }
-    float ss = 0.0f;
-#pragma unroll
-    for (int k = 0; k < 16; ++k)
-        ss = __fmaf_rn(v[k], v[k], ss);
-    const float r = inv_rms(warp_sum(ss), p.eps);
-    const uint4 wa = kSmemW ? w_smem[lane] : __ldg(reinterpret_cast<const uint4 *>(p.w) + lane);
-    const uint4 wb =
-        kSmemW ? w_smem[32 + lane] : __ldg(reinterpret_cast<const uint4 *>(p.w) + 32 + lane);
-    float w[16];
-    widen8(wa, w);
-    widen8(wb, w + 8);
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-        v[k] = __fmul_rn(__fmul_rn(v[k], r), w[k]);
-    if (lane < 24) {
-#pragma unroll
-        for (int k = 8; k < 16; ++k)
-            v[k] = __fmul_rn(__fmul_rn(v[k], r), w[k]);
-    } else {
-        // rope dims: x*w is exact in fp32 (two 8-bit significands), rotate, then scale
-        float u[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            u[k] = __fmul_rn(v[8 + k], w[8 + k]);
-        rope8_scaled(u, cv, sv, r, v + 8);
-    }
-}
-
-// The KV row of token t: v = x*r*w (or v = x when the row arrives normalised),
-// rotate, store into the paged cache.
-template <int kStore, bool kSmemW, bool kKvNorm>
-__device__ __forceinline__ void kv_row(const KParams &p, int lane, int64_t t, const uint4 *w_smem)
-{
-    const int64_t pos = __ldg(p.pos + t);
-    const int64_t slot = __ldg(p.slot + t);
-    const uint16_t *src = p.kv + t * kHead;
-    const uint4 xa = ld_stream16(src + 8 * lane);
-    const uint4 xb = ld_stream16(src + 256 + 8 * lane);
-    if (pos < 0 || pos >= p.max_pos) {
-        if (lane == 0)
-            flag_error(p.err, DSV4_DEVERR_POS_RANGE);
-        return;
-    }
-    if (slot < 0)
-        return;
-    if (slot >= p.num_slots) {
-        if (lane == 0)
-            flag_error(p.err, DSV4_DEVERR_SLOT_RANGE);
-        return;
-    }
-    const bool rope_lane = lane >= 24;
-    float4 cv = make_float4(0.f, 0.f, 0.f, 0.f), sv = cv;
-    if (rope_lane) {
-        const float *cs = p.cs + pos * DSV4_ROPE_DIM + 4 * (lane - 24);
-        cv = __ldg(reinterpret_cast<const float4 *>(cs));
-        sv = __ldg(reinterpret_cast<const float4 *>(cs + DSV4_ROPE_DIM / 2));
-    }
-    float v[16];
-    kv_values<kSmemW, kKvNorm>(p, lane, xa, xb, cv, sv, w_smem, v);
-
-    if (kStore == DSV4_STORE_BF16) {
-        uint16_t *row = reinterpret_cast<uint16_t *>(p.cache) + slot * kHead;
-        st_stream16(row + 8 * lane, bf16x8_rn(v));
-        st_stream16(row + 256 + 8 * lane, bf16x8_rn(v + 8));
-        return;
-    }
-
-    // block amax: half 0 -> blocks 0..3 (lane / 8), half 1 -> blocks 4..6 (lanes 0..23)
-    float am0 = 0.0f, am1 = 0.0f;
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-        am0 = fmaxf(am0, fabsf(v[k]));
-    if (!rope_lane) {
-#pragma unroll
-        for (int k = 8; k < 16; ++k)
-            am1 = fmaxf(am1, fabsf(v[k]));
-    }
-    ScaleGuess g0 = ue8m0_guess(group8_max(am0));
-    ScaleGuess g1 = ue8m0_guess(group8_max(am1));  // lanes 24..31: amax 0, never near
-    // with no norm, v = x exactly and the guess is already exact
-    if (kKvNorm && __any_sync(kFull, g0.near || g1.near)) {
-        const int bumps = exact_scale_bumps(p, lane, t, g0.e, g0.near, g1.e, g1.near);
-        if (g0.near)
-            g0.s = clamp_s(g0.e - 8 + (bumps & 1));
-        if (g1.near)
-            g1.s = clamp_s(g1.e - 8 + ((bumps >> 1) & 1));
-        // recompute v (same bits) instead of keeping it live across the call
-        kv_values<kSmemW, kKvNorm>(p, lane, __ldg(reinterpret_cast<const uint4 *>(src) + lane),
-                          __ldg(reinterpret_cast<const uint4 *>(src) + 32 + lane), cv, sv,
-                          w_smem, v);
-    }
-
-    const int64_t blk = slot / p.block_size;
-    const int64_t off = slot - blk * p.block_size;
-    uint8_t *base = p.cache + blk * int64_t(p.block_size) * DSV4_FP8_SLOT_BYTES;
-    uint8_t *data = base + off * DSV4_FP8_DATA_BYTES;
-
-    const float k0 = pow2_neg(g0.s);
-    st_stream8(data + 8 * lane,
-               make_uint2(e4m3x4_rn(v[0] * k0, v[1] * k0, v[2] * k0, v[3] * k0),
-                          e4m3x4_rn(v[4] * k0, v[5] * k0, v[6] * k0, v[7] * k0)));
-    if (!rope_lane) {
-        const float k1 = pow2_neg(g1.s);
-        st_stream8(data + 256 + 8 * lane,
-                   make_uint2(e4m3x4_rn(v[8] * k1, v[9] * k1, v[10] * k1, v[11] * k1),
-                              e4m3x4_rn(v[12] * k1, v[13] * k1, v[14] * k1, v[15] * k1)));
-    } else {
-        // rope dims stay bf16; 8-byte stores keep any block_size legal
-        uint8_t *tail = data + DSV4_NOPE_DIM + 16 * (lane - 24);
-        st_stream8(tail, make_uint2(bf16x2_rn(v[8], v[9]), bf16x2_rn(v[10], v[11])));
-        st_stream8(tail + 8, make_uint2(bf16x2_rn(v[12], v[13]), bf16x2_rn(v[14], v[15])));
-    }
-
-    const uint32_t e0 = uint32_t(g0.s + 127), e1 = uint32_t(g1.s + 127);
-    const uint32_t b0 = __shfl_sync(kFull, e0, 0), b1 = __shfl_sync(kFull, e0, 8);
-    const uint32_t b2 = __shfl_sync(kFull, e0, 16), b3 = __shfl_sync(kFull, e0, 24);
-    const uint32_t b4 = __shfl_sync(kFull, e1, 0), b5 = __shfl_sync(kFull, e1, 8);
-    const uint32_t b6 = __shfl_sync(kFull, e1, 16);
-    if (lane == 0)
-        st_stream8(base + int64_t(p.block_size) * DSV4_FP8_DATA_BYTES + off * DSV4_FP8_SCALE_BYTES,
-                   make_uint2(b0 | (b1 << 8) | (b2 << 16) | (b3 << 24), b4 | (b5 << 8) | (b6 << 16)));
-}
 
 // Work items, handed out round-robin over all warps of the grid:
 //   items [0, T)            : the KV row of token t = item
@@ -458,7 +71,12 @@ __global__ void __launch_bounds__(256, 3) qnorm_rope_kv_insert_kernel(const KPar
     for (int64_t it = int64_t(blockIdx.x) * warps_per_cta + (threadIdx.x >> 5); it < items;
          it += stride) {
         if (it < T) {
-            kv_row<kStore, kSmemW, kKvNorm>(p, lane, it, w_smem);
+            const int64_t pos = __ldg(p.pos + it);
+            const int64_t slot = __ldg(p.slot + it);
+            const uint16_t *src = p.kv + it * kHead;
+            const uint4 xa = ld_stream16(src + 8 * lane);
+            const uint4 xb = ld_stream16(src + 256 + 8 * lane);
+            kv_row<kStore, kSmemW, kKvNorm>(p, lane, it, pos, slot, xa, xb, w_smem);
             continue;
         }
         const int64_t r0 = (it - T) * kRows;
@@ -496,37 +114,13 @@ __global__ void __launch_bounds__(256, 3) qnorm_rope_kv_insert_kernel(const KPar
                 break;
             if (pos[j] < 0 || pos[j] >= p.max_pos)
                 continue;  // flagged once per token by its KV row
-            float4 cv = make_float4(0.f, 0.f, 0.f, 0.f), sv = cv;
-            if (lane >= 24) {
-                const float *cs = p.cs + pos[j] * DSV4_ROPE_DIM + 4 * (lane - 24);
-                cv = __ldg(reinterpret_cast<const float4 *>(cs));
-                sv = __ldg(reinterpret_cast<const float4 *>(cs + DSV4_ROPE_DIM / 2));
-            }
-            float y[16];
-            widen8(a[j], y);
-            widen8(b[j], y + 8);
-            float ss = 0.0f;
-#pragma unroll
-            for (int k = 0; k < 16; ++k)
-                ss = __fmaf_rn(y[k], y[k], ss);
-            const float r = inv_rms(warp_sum(ss), p.eps);
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                y[k] = __fmul_rn(y[k], r);
-            if (lane < 24) {
-#pragma unroll
-                for (int k = 8; k < 16; ++k)
-                    y[k] = __fmul_rn(y[k], r);
-            } else {
-                float u[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    u[k] = y[8 + k];
-                rope8_scaled(u, cv, sv, r, y + 8);
-            }
+            float4 cv, sv;
+            load_cs(p, lane, pos[j], cv, sv);
+            uint4 out_a, out_b;
+            q_row(p, lane, a[j], b[j], cv, sv, out_a, out_b);
             uint16_t *dst = p.q + (r0 + j) * kHead;
-            st_stream16(dst + 8 * lane, bf16x8_rn(y));
-            st_stream16(dst + 256 + 8 * lane, bf16x8_rn(y + 8));
+            st_stream16(dst + 8 * lane, out_a);
+            st_stream16(dst + 256 + 8 * lane, out_b);
         }
     }
 }
@@ -580,6 +174,8 @@ int launch(int store_mode, const dsv4_plan &plan, const LaunchArgs &a, cudaStrea
     p.num_heads = a.num_heads;
     p.eps = a.eps;
     p.err = a.err;
+    if (plan.variant == DSV4_VARIANT_BULK)
+        return launch_bulk(store_mode, a.kv_norm, plan.ctas, p, stream);
     const dim3 grid(unsigned(plan.ctas)), block(unsigned(plan.threads));
     const bool small = plan.variant == DSV4_VARIANT_SMALL;
     if (store_mode == DSV4_STORE_BF16) {

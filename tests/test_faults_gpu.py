@@ -29,7 +29,8 @@ def _faulty_inputs(store):
     return harness.make_inputs(wl, positions=pos, slots=slots)
 
 
-@pytest.mark.parametrize("variant", [k.VARIANT_AUTO, k.VARIANT_SMALL, k.VARIANT_STREAM])
+@pytest.mark.parametrize("variant", [k.VARIANT_AUTO, k.VARIANT_SMALL, k.VARIANT_STREAM,
+                                     k.VARIANT_BULK])
 @pytest.mark.parametrize("store", ["fp8", "bf16"])
 def test_out_of_range_flagged_and_skipped(store, variant):
     inp = _faulty_inputs(store)

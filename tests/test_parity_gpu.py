@@ -23,7 +23,7 @@ if not torch.cuda.is_available():  # pragma: no cover - CPU runs deselect the gp
 
 import kv_norm_rope_gb300 as k  # noqa: E402
 
-VARIANTS = [k.VARIANT_AUTO, k.VARIANT_SMALL, k.VARIANT_STREAM]
+VARIANTS = [k.VARIANT_AUTO, k.VARIANT_SMALL, k.VARIANT_STREAM, k.VARIANT_BULK]
 # q rows beyond this many elements are compared on a token sample (the KV side,
 # i.e. the whole cache image, is always compared in full)
 FULL_Q_ELEMS = 1 << 27
@@ -326,3 +326,10 @@ def test_public_entries_match_ex():
     torch.cuda.synchronize()
     ref2 = harness.run_gpu(inp)
     assert np.array_equal(cache2.cpu().numpy(), ref2.cache)
+
+
+@pytest.mark.parametrize("name", ["prefill", "bf16_store", "stress"])
+def test_full_size_workloads_bulk(name):
+    """The shared-memory-staged variant at full size (every cache byte, 1024 sampled
+    tokens' q)."""
+    _check(configs.WORKLOADS[name], k.VARIANT_BULK, n_sample=1024)
