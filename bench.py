@@ -319,11 +319,13 @@ def known_answer_check() -> str:
 
 # ------------------------------------------------------------------ end to end
 
-def e2e_run(batch: DeviceBatch, lib, steps: int, chunks: int = 8):
+def e2e_run(batch: DeviceBatch, lib, steps: int, chunks: int = 16):
     """Same metric through the C ABI with host buffers: per step, token chunks of q, kv,
     positions and slots go host->device from pinned memory, the kernel runs on each chunk,
-    and q plus the cache come back device->host; copies in each direction overlap the
-    kernel of neighbouring chunks on three streams.  Returns (GB/s, h2d, d2h bytes/step)."""
+    and q plus the cache come back device->host.  Uploads, kernels and downloads run on
+    three streams with per-chunk events, so both directions of the host link stay busy
+    across step boundaries (chunk c of step k+1 is uploaded as soon as chunk c of step k
+    has been downloaded).  Returns (GB/s, h2d bytes, d2h bytes, seconds per step)."""
     import torch
     wl = batch.wl
     dev = batch.dev
@@ -339,36 +341,42 @@ def e2e_run(batch: DeviceBatch, lib, steps: int, chunks: int = 8):
     bounds = np.linspace(0, wl.T, chunks + 1).astype(np.int64)
     h2d = q_h.numel() * 2 + kv_h.numel() * 2 + pos_h.numel() * 8 + sl_h.numel() * 8
     d2h = q_h.numel() * 2 + cache_h.numel()
+    downloaded = [None] * chunks   # per chunk: its q is back on the host
+    cache_read = [None]            # the cache image of the previous step is back
 
     def step():
-        done_in, done_k = [], []
+        kernels_done = None
         for c in range(chunks):
             a, b = int(bounds[c]), int(bounds[c + 1])
+            if downloaded[c] is not None:
+                s_in.wait_event(downloaded[c])
             with torch.cuda.stream(s_in):
                 batch.q[a:b].copy_(q_h[a:b], non_blocking=True)
                 batch.kv[a:b].copy_(kv_h[a:b], non_blocking=True)
                 batch.pos[a:b].copy_(pos_h[a:b], non_blocking=True)
                 batch.slots[a:b].copy_(sl_h[a:b], non_blocking=True)
-                ev = torch.cuda.Event()
-                ev.record(s_in)
-                done_in.append(ev)
-            s_k.wait_event(done_in[c])
+                up = torch.cuda.Event()
+                up.record(s_in)
+            s_k.wait_event(up)
+            if c == 0 and cache_read[0] is not None:
+                s_k.wait_event(cache_read[0])  # the kernels overwrite the cache rows
             st = fn(batch.q[a:b].data_ptr(), batch.kv[a:b].data_ptr(), batch.w.data_ptr(),
                     batch.pos[a:b].data_ptr(), batch.cs.data_ptr(), wl.max_position,
                     batch.slots[a:b].data_ptr(), batch.cache.data_ptr(), wl.num_blocks,
                     wl.block_size, b - a, wl.H, wl.eps, batch.err.data_ptr(), s_k.cuda_stream)
             if st != 0:
                 raise RuntimeError(f"launch failed with status {st}")
-            ev = torch.cuda.Event()
-            ev.record(s_k)
-            done_k.append(ev)
-            s_out.wait_event(ev)
+            kernels_done = torch.cuda.Event()
+            kernels_done.record(s_k)
+            s_out.wait_event(kernels_done)
             with torch.cuda.stream(s_out):
                 q_h[a:b].copy_(batch.q[a:b], non_blocking=True)
+                downloaded[c] = torch.cuda.Event()
+                downloaded[c].record(s_out)
         with torch.cuda.stream(s_out):
             cache_h.copy_(batch.cache, non_blocking=True)
-        # the next step's uploads must not overwrite device q before its download
-        s_in.wait_stream(s_out)
+            cache_read[0] = torch.cuda.Event()
+            cache_read[0].record(s_out)
 
     step()
     torch.cuda.synchronize(dev)
@@ -414,12 +422,14 @@ class OracleSample:
 
 
 def _sample_tokens_for(wl: configs.Workload, seconds: float) -> int:
-    probe = OracleSample(wl, 16)
+    """Tokens the oracle processes in about `seconds` on all host cores."""
+    probe = OracleSample(wl, 128)
+    probe.run()  # warm (thread start-up, page faults)
     per_tok = max(probe.run() / probe.n, 1e-7)
     return int(max(1, min(wl.T, seconds / per_tok)))
 
 
-def cpu_baseline(wl: configs.Workload, seconds: float = 5.0):
+def cpu_baseline(wl: configs.Workload, seconds: float = 2.0):
     cores = os.cpu_count() or 1
     sample = OracleSample(wl, _sample_tokens_for(wl, seconds))
     dt = sample.run()
@@ -531,7 +541,8 @@ def run_ours(args):
         e2e = {"value": round(total_bytes / e2e_dt / 1e9, 2), "unit": "GB/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "tokens_per_s": round(total_tokens / e2e_dt, 1),
-               "chunks": 8, "ms_per_step": round(e2e_dt * 1e3, 3)}
+               "chunks": 16, "ms_per_step": round(e2e_dt * 1e3, 3),
+               "link": "pinned host memory; H2D and D2H overlap across chunks and steps"}
     kac_after = known_answer_check() if rank == 0 else "skipped"
     if rank != 0:
         return 0
@@ -599,10 +610,11 @@ def main(argv=None):
     ap.add_argument("--op", choices=OPS, default="fused",
                     help="fused (default); prenorm: KV arrives normalised; kv_only: no q; "
                          "gather: read the FP8 cache back out")
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=6)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=5.0)
+    ap.add_argument("--cpu-seconds", type=float, default=2.0,
+                    help="wall seconds of oracle work on all host cores for cpu_baseline")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
