@@ -58,6 +58,15 @@ def _load():
         lib.oracle_e4m3_value_array.argtypes = [vp, vp, i64]
         lib.oracle_dequant_gather.argtypes = [vp, i64, i32, vp, i64, vp]
         lib.oracle_dequant_gather.restype = i32
+        lib.oracle_gemma_rmsnorm_mxfp8.argtypes = [vp, vp, vp, i64, i64, f32, vp, vp, vp]
+        lib.oracle_ue8m0_of_f32.argtypes = [f32]
+        lib.oracle_ue8m0_of_f32.restype = ctypes.c_int
+        lib.oracle_ue8m0_inverse.argtypes = [ctypes.c_int]
+        lib.oracle_ue8m0_inverse.restype = ctypes.c_double
+        lib.oracle_swizzled_scale_offset.argtypes = [i64, i64, i64]
+        lib.oracle_swizzled_scale_offset.restype = i64
+        lib.oracle_mxfp8_scale_bytes.argtypes = [i64, i64]
+        lib.oracle_mxfp8_scale_bytes.restype = i64
         lib.oracle_ue8m0_exponent.argtypes = [ctypes.c_double]
         lib.oracle_ue8m0_exponent.restype = ctypes.c_int
         _lib = lib
@@ -188,3 +197,35 @@ def dequant_gather(cache: np.ndarray, num_blocks: int, block_size: int, slots: n
     err = _load().oracle_dequant_gather(cache.ctypes.data, num_blocks, block_size, sl.ctypes.data,
                                         sl.size, out.ctypes.data)
     return out, int(err)
+
+
+def mxfp8_scale_bytes(m: int, n: int) -> int:
+    return int(_load().oracle_mxfp8_scale_bytes(m, n))
+
+
+def swizzled_scale_offset(row: int, col: int, padded_cols: int) -> int:
+    return int(_load().oracle_swizzled_scale_offset(row, col, padded_cols))
+
+
+def ue8m0_of_f32(x: float) -> int:
+    return int(_load().oracle_ue8m0_of_f32(x))
+
+
+def ue8m0_inverse(e: int) -> float:
+    return float(_load().oracle_ue8m0_inverse(e))
+
+
+def gemma_rmsnorm_mxfp8(x: np.ndarray, residual: np.ndarray, gamma: np.ndarray, eps: float):
+    """(residual_out bf16 bits [m, n], E4M3 codes [m, n], swizzled UE8M0 scales)."""
+    x = _c(x, np.uint16)
+    residual = _c(residual, np.uint16)
+    gamma = _c(gamma, np.uint16)
+    m, n = x.shape
+    assert n % 128 == 0 and residual.shape == (m, n) and gamma.shape == (n,)
+    res_out = np.empty((m, n), np.uint16)
+    codes = np.empty((m, n), np.uint8)
+    scales = np.empty(mxfp8_scale_bytes(m, n), np.uint8)
+    _load().oracle_gemma_rmsnorm_mxfp8(x.ctypes.data, residual.ctypes.data, gamma.ctypes.data, m, n,
+                                        eps, res_out.ctypes.data, codes.ctypes.data,
+                                        scales.ctypes.data)
+    return res_out, codes, scales

@@ -50,6 +50,7 @@
 #include <math.h>
 #include <pthread.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 #include <unistd.h>
 
@@ -420,6 +421,102 @@ int32_t oracle_dequant_gather(const uint8_t *cache, int64_t num_blocks, int32_t 
         }
     }
     return err;
+}
+
+/* ------------------- residual add + Gemma RMSNorm + MXFP8 (32-element blocks) */
+
+/*
+ * The single-GPU part of the vLLM minimax_m3 finalize_allreduce_norm page
+ * (_LamportGemmaRMSNormMxfp8Kernel): with one rank there is no all-reduce, so
+ * for each row
+ *   prenorm = bf16(x + residual)                 (also the new residual)
+ *   r       = 1 / sqrt(mean(prenorm^2) + eps)
+ *   normed  = bf16(prenorm * r * (1 + gamma))    (Gemma: the scale is 1 + w;
+ *                                                 the page rounds to bf16 here)
+ * and for each block of 32 normed values
+ *   e       = UE8M0 of amax * (1/448), both factors and the product in fp32
+ *             (the page's _ue8m0_ceil of amax * Float32(1.0 / 448.0))
+ *   code    = E4M3_rn_satfinite(normed * 2^(127 - e))   (0 when e is 0 or 254:
+ *             the page's _ue8m0_inverse)
+ * Scales go to the 128x4 swizzled layout (_swizzled_scale_offset); the scales
+ * of the padding rows up to the next multiple of 128 rows are zero.
+ */
+
+/* smallest e in [0, 254] with x <= 2^(e - 127) (254 if none); 0 for x <= 0.
+ * For x > 0 this is ceil(log2 x) + 127, clamped: the exponent of the next
+ * power of two at or above x. */
+int oracle_ue8m0_of_f32(float x)
+{
+    if (!(x > 0.0f))
+        return 0;
+    for (int e = 0; e < 254; ++e)
+        if ((double)x <= ldexp(1.0, e - 127))
+            return e;
+    return 254;
+}
+
+/* the page's inverse scale: 2^(127 - e), except 0 for e = 0 and for e = 254 */
+double oracle_ue8m0_inverse(int e)
+{
+    if (e == 0 || e >= 254)
+        return 0.0;
+    return ldexp(1.0, 127 - e);
+}
+
+/* byte offset of block col of row in the 128x4 swizzled scale layout */
+int64_t oracle_swizzled_scale_offset(int64_t row, int64_t col, int64_t padded_cols)
+{
+    int64_t tile = (row / 128) * 128 * padded_cols + (col / 4) * 512;
+    return tile + (row % 32) * 16 + ((row % 128) / 32) * 4 + col % 4;
+}
+
+int64_t oracle_mxfp8_scale_bytes(int64_t m, int64_t n)
+{
+    int64_t rows = (m + 127) / 128 * 128;
+    int64_t cols = (n / 32 + 3) / 4 * 4;
+    return rows * cols;
+}
+
+/* x, residual: bf16 [m, n]; gamma bf16 [n]; n a multiple of 128.  Writes
+ * residual_out bf16 [m, n], codes [m, n] (E4M3) and scales (all
+ * oracle_mxfp8_scale_bytes(m, n) bytes, padding rows zeroed). */
+void oracle_gemma_rmsnorm_mxfp8(const uint16_t *x, const uint16_t *residual, const uint16_t *gamma,
+                                int64_t m, int64_t n, float eps, uint16_t *residual_out,
+                                uint8_t *codes, uint8_t *scales)
+{
+    const int64_t cols = n / 32, padded_cols = (cols + 3) / 4 * 4;
+    const float inv448 = (float)(1.0 / 448.0);
+    memset(scales, 0, (size_t)oracle_mxfp8_scale_bytes(m, n));
+    double *pre = (double *)malloc((size_t)n * sizeof(double));
+    double *normed = (double *)malloc((size_t)n * sizeof(double));
+    for (int64_t row = 0; row < m; ++row) {
+        const uint16_t *xr = x + row * n, *rr = residual + row * n;
+        double ss = 0.0;
+        for (int64_t d = 0; d < n; ++d) {
+            uint16_t p = oracle_bf16_rne(oracle_bf16_value(xr[d]) + oracle_bf16_value(rr[d]));
+            residual_out[row * n + d] = p;
+            pre[d] = oracle_bf16_value(p);
+            ss += pre[d] * pre[d];
+        }
+        const double r = 1.0 / sqrt(ss / (double)n + (double)eps);
+        for (int64_t d = 0; d < n; ++d)
+            normed[d] = oracle_bf16_value(
+                oracle_bf16_rne(pre[d] * r * (1.0 + oracle_bf16_value(gamma[d]))));
+        for (int64_t c = 0; c < cols; ++c) {
+            double amax = 0.0;
+            for (int64_t d = 32 * c; d < 32 * c + 32; ++d)
+                if (fabs(normed[d]) > amax)
+                    amax = fabs(normed[d]);
+            const float scaled = (float)amax * inv448; /* fp32 product, as on the page */
+            const int e = oracle_ue8m0_of_f32(scaled);
+            const double inv = oracle_ue8m0_inverse(e);
+            for (int64_t d = 32 * c; d < 32 * c + 32; ++d)
+                codes[row * n + d] = oracle_e4m3_rne(normed[d] * inv);
+            scales[oracle_swizzled_scale_offset(row, c, padded_cols)] = (uint8_t)e;
+        }
+    }
+    free(pre);
+    free(normed);
 }
 
 /* ------------------------------------------------- array forms for the tests */
