@@ -211,7 +211,15 @@ def copy_ceiling_gbs(dev, nbytes: int) -> float:
 
 # ------------------------------------------------------------------ inputs on the device
 
-OPS = ("fused", "prenorm", "kv_only", "gather")
+OPS = ("fused", "prenorm", "kv_only", "gather", "mxfp8")
+IO_OF_OP = {
+    "fused": "bf16 q, kv in; bf16 q, FP8 (e4m3 + ue8m0 + bf16) or bf16 cache rows out",
+    "prenorm": "bf16 q, normalised kv in; bf16 q, FP8 cache rows out",
+    "kv_only": "bf16 kv in; FP8 or bf16 cache rows out",
+    "gather": "FP8 cache rows in; bf16 rows out",
+    "mxfp8": "bf16 x, residual in; bf16 residual, e4m3 codes, swizzled ue8m0 scales out",
+}
+MXFP8_HIDDEN = 7168
 VARIANTS = {"auto": 0, "small": 1, "stream": 2, "bulk": 3}
 
 
@@ -224,7 +232,7 @@ class DeviceBatch:
     def __init__(self, wl: configs.Workload, dev, op: str = "fused", variant: int = 0):
         import torch
         self.variant = variant
-        if op in ("kv_only", "gather"):
+        if op in ("kv_only", "gather", "mxfp8"):
             wl = dataclasses.replace(wl, H=0)
         self.wl = wl
         self.op = op
@@ -244,6 +252,17 @@ class DeviceBatch:
         self.bytes = configs.algorithmic_bytes(wl, self.positions_np, self.slots_np)
         if op == "prenorm":
             self.bytes -= 1024  # no weight read
+        if op == "mxfp8":
+            # activation rows [T, MXFP8_HIDDEN]: x, residual (in place), gamma, codes, scales
+            import kv_norm_rope_gb300 as k
+            n = MXFP8_HIDDEN
+            self.x = self._normal((wl.T, n), g)
+            self.res = self._normal((wl.T, n), g)
+            self.gamma = self._normal((n,), g)
+            self.codes = torch.empty((wl.T, n), dtype=torch.uint8, device=dev)
+            self.mx_scales = torch.empty(k.mxfp8_scale_bytes(wl.T, n), dtype=torch.uint8,
+                                         device=dev)
+            self.bytes = wl.T * n * (2 + 2 + 2 + 1) + self.mx_scales.numel() + 2 * n
         if op == "gather":
             if wl.store != "fp8":
                 raise ValueError("the reader reads FP8 caches")
@@ -274,6 +293,11 @@ class DeviceBatch:
     def call(self, lib, stream_handle: int):
         """(C-ABI function, argument tuple) of one step of this batch's op."""
         wl = self.wl
+        if self.op == "mxfp8":
+            return lib.dsv4_add_gemma_rmsnorm_mxfp8, (
+                self.x.data_ptr(), self.res.data_ptr(), self.gamma.data_ptr(), wl.T, MXFP8_HIDDEN,
+                wl.eps, self.res.data_ptr(), self.codes.data_ptr(), self.mx_scales.data_ptr(),
+                stream_handle)
         if self.op == "gather":
             return lib.dsv4_dequant_gather, (
                 self.cache.data_ptr(), wl.num_blocks, wl.block_size, self.slots.data_ptr(), wl.T,
@@ -551,7 +575,7 @@ def run_ours(args):
     achieved = batch.bytes / mean_launch / 1e9
     value = total_bytes / t_step / 1e9
     plan = k.launch_plan(wl.T, wl.H, torch.cuda.get_device_properties(dev).multi_processor_count,
-                         4)
+                         3)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_step * 1e3, 4),
@@ -563,10 +587,11 @@ def run_ours(args):
                    "bytes_per_step": batch.bytes,
                    "l2": "flushed before every launch (256 MB write)" if flush is not None
                    else f"inputs larger than L2 ({batch.bytes / 1e9:.2f} GB per step)",
-                   "io": "bf16 in; bf16 q, e4m3+ue8m0+bf16 cache out",
-                   "variant": args.variant if args.variant != "auto" else
-                   {k.VARIANT_STREAM: "stream", k.VARIANT_SMALL: "small",
-                    k.VARIANT_BULK: "bulk"}[plan.variant],
+                   "io": IO_OF_OP[args.op],
+                   "variant": (args.variant if args.variant != "auto" else
+                               {k.VARIANT_STREAM: "stream", k.VARIANT_SMALL: "small",
+                                k.VARIANT_BULK: "bulk"}[plan.variant])
+                   if args.op in ("fused", "prenorm", "kv_only") else "n/a",
                    "parallelism": f"dp{world}" if world > 1 else "single"},
         "tokens_per_s": round(total_tokens / t_step, 1),
         "frac_of_copy_ceiling": round(value / world / copy_1g, 4),
@@ -609,7 +634,8 @@ def main(argv=None):
                     help="launch variant of the fused op (default: the library's choice)")
     ap.add_argument("--op", choices=OPS, default="fused",
                     help="fused (default); prenorm: KV arrives normalised; kv_only: no q; "
-                         "gather: read the FP8 cache back out")
+                         "gather: read the FP8 cache back out; mxfp8: residual add + Gemma "
+                         "RMSNorm + MXFP8 of [T, 7168] activation rows")
     ap.add_argument("--e2e-steps", type=int, default=6)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -212,6 +212,37 @@ int dsv4_dequant_gather(const uint8_t *kv_cache, int64_t num_blocks, int32_t blo
                         const int64_t *slots, int64_t num_rows, void *out,
                         int32_t *device_error, void *stream);
 
+/*
+ * Residual add + Gemma RMSNorm + MXFP8 quantisation of activation rows: the
+ * single-GPU part of the vLLM minimax_m3 finalize_allreduce_norm page
+ * (_LamportGemmaRMSNormMxfp8Kernel with one rank; no all-reduce).  Per row:
+ *   residual_out = bf16(x + residual)                   (the new residual stream)
+ *   r            = 1 / sqrt(mean(residual_out^2) + eps)
+ *   normed       = bf16(residual_out * r * (1 + gamma))  (Gemma: the scale is 1 + w)
+ * and per 32-element block of normed: e = the UE8M0 byte of fp32(amax * fp32(1/448))
+ * rounded up to a power of two (clamped to [0, 254], 0 for amax 0); codes =
+ * E4M3_rn_satfinite(normed * 2^(127 - e)) (the inverse is 0 for e = 0 and e = 254).
+ *
+ *  x, residual   (device) bf16 [num_rows, hidden], 16-byte aligned; residual_out may
+ *                be residual itself (rewritten in place), x must not overlap an output.
+ *  gamma         (device) bf16 [hidden], 16-byte aligned.
+ *  residual_out  (device) bf16 [num_rows, hidden], 16-byte aligned.
+ *  codes         (device) uint8 [num_rows, hidden] E4M3, 8-byte aligned.
+ *  scales        (device) uint8, dsv4_mxfp8_scale_bytes(num_rows, hidden) bytes: the
+ *                byte of row r, block c sits at (r/128)*128*C + (c/4)*512 + (r%32)*16
+ *                + ((r%128)/32)*4 + c%4, with C = hidden/32 (the 128x4 swizzled layout);
+ *                the rows past num_rows up to the next multiple of 128 get 0.
+ *  hidden        a multiple of 128 in [128, 16384]; num_rows >= 0 (0: no launch).
+ * Returns a dsv4_status.
+ */
+int dsv4_add_gemma_rmsnorm_mxfp8(const void *x, const void *residual, const void *gamma,
+                                 int64_t num_rows, int32_t hidden, float eps, void *residual_out,
+                                 uint8_t *codes, uint8_t *scales, void *stream);
+
+/* Bytes of the swizzled scales of num_rows rows: ceil(num_rows/128)*128 * hidden/32
+ * (0 for an invalid hidden). */
+size_t dsv4_mxfp8_scale_bytes(int64_t num_rows, int32_t hidden);
+
 /* Launch plan of a call (pure host arithmetic, no CUDA call). */
 typedef struct {
     int32_t variant;        /* DSV4_VARIANT_SMALL or DSV4_VARIANT_STREAM */

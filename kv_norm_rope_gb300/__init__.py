@@ -21,7 +21,7 @@ _CSRC = os.path.join(_HERE, "csrc")
 _INCLUDE = os.path.join(_ROOT, "include")
 LIB_PATH = os.path.join(_HERE, "libdsv4kv.so")
 _SOURCES = ["qnorm_rope_kv_insert.cu", "qnorm_rope_kv_insert_bulk.cu", "dequant_gather.cu",
-            "api.cpp"]
+            "gemma_rmsnorm_mxfp8.cu", "api.cpp"]
 _HEADERS = [os.path.join(_INCLUDE, "dsv4kv.h"), os.path.join(_CSRC, "launch.h"),
             os.path.join(_CSRC, "rowmath.cuh")]
 NVCC_ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -35,7 +35,8 @@ FP8_SLOT_BYTES, BF16_SLOT_BYTES = 584, 1024
 
 EXPORTS = ("dsv4_qnorm_rope_kv_quant_insert", "dsv4_qnorm_rope_kv_bf16_insert",
            "dsv4_qnorm_rope_kv_insert_variant", "dsv4_qnorm_rope_kv_rope_quant_insert",
-           "dsv4_kv_norm_rope_insert", "dsv4_insert_ex", "dsv4_dequant_gather", "dsv4_launch_plan",
+           "dsv4_kv_norm_rope_insert", "dsv4_insert_ex", "dsv4_dequant_gather",
+           "dsv4_add_gemma_rmsnorm_mxfp8", "dsv4_mxfp8_scale_bytes", "dsv4_launch_plan",
            "dsv4_fp8_cache_bytes", "dsv4_bf16_cache_bytes", "dsv4_status_string")
 
 
@@ -117,6 +118,10 @@ def lib():
         L.dsv4_kv_norm_rope_insert.restype = c_int
         L.dsv4_dequant_gather.argtypes = [vp, i64, i32, vp, i64, vp, vp, vp]
         L.dsv4_dequant_gather.restype = c_int
+        L.dsv4_add_gemma_rmsnorm_mxfp8.argtypes = [vp, vp, vp, i64, i32, f32, vp, vp, vp, vp]
+        L.dsv4_add_gemma_rmsnorm_mxfp8.restype = c_int
+        L.dsv4_mxfp8_scale_bytes.argtypes = [i64, i32]
+        L.dsv4_mxfp8_scale_bytes.restype = ctypes.c_size_t
         L.dsv4_launch_plan.argtypes = [i64, i32, i32, i32, i32, ctypes.POINTER(Plan)]
         L.dsv4_launch_plan.restype = c_int
         L.dsv4_fp8_cache_bytes.argtypes = [i64, i32]
@@ -266,3 +271,18 @@ def dequant_gather(kv_cache, num_blocks: int, block_size: int, slots, out, devic
                                    _stream_handle(stream))
     if st != OK:
         raise Dsv4Error(st, "dsv4_dequant_gather")
+
+
+def mxfp8_scale_bytes(num_rows: int, hidden: int) -> int:
+    return int(lib().dsv4_mxfp8_scale_bytes(num_rows, hidden))
+
+
+def add_gemma_rmsnorm_mxfp8(x, residual, gamma, eps: float, residual_out, codes, scales,
+                            stream=None) -> None:
+    """dsv4_add_gemma_rmsnorm_mxfp8: residual add + Gemma RMSNorm + MXFP8 rows."""
+    m, n = int(x.shape[0]), int(x.shape[1])
+    st = lib().dsv4_add_gemma_rmsnorm_mxfp8(_ptr(x), _ptr(residual), _ptr(gamma), m, n, eps,
+                                            _ptr(residual_out), _ptr(codes), _ptr(scales),
+                                            _stream_handle(stream))
+    if st != OK:
+        raise Dsv4Error(st, "dsv4_add_gemma_rmsnorm_mxfp8")

@@ -268,6 +268,36 @@ int dsv4_dequant_gather(const uint8_t *kv_cache, int64_t num_blocks, int32_t blo
                                static_cast<cudaStream_t>(stream));
 }
 
+size_t dsv4_mxfp8_scale_bytes(int64_t num_rows, int32_t hidden)
+{
+    if (num_rows < 0 || hidden < 128 || hidden % 128 != 0)
+        return 0;
+    return size_t((num_rows + 127) / 128 * 128) * size_t(hidden / 32);
+}
+
+int dsv4_add_gemma_rmsnorm_mxfp8(const void *x, const void *residual, const void *gamma,
+                                 int64_t num_rows, int32_t hidden, float eps, void *residual_out,
+                                 uint8_t *codes, uint8_t *scales, void *stream)
+{
+    if (num_rows < 0 || hidden < 128 || hidden > 16384 || hidden % 128 != 0)
+        return DSV4_ERR_SHAPE;
+    if (num_rows > (INT64_MAX / 4096) / hidden || num_rows > INT32_MAX - 128)
+        return DSV4_ERR_SHAPE;
+    if (!(eps >= 0.0f) || !std::isfinite(eps))
+        return DSV4_ERR_VALUE;
+    if (num_rows == 0)
+        return DSV4_OK;
+    if (!x || !residual || !gamma || !residual_out || !codes || !scales)
+        return DSV4_ERR_NULL;
+    if (!aligned(x, 16) || !aligned(residual, 16) || !aligned(gamma, 16) ||
+        !aligned(residual_out, 16) || !aligned(codes, 8))
+        return DSV4_ERR_ALIGN;
+    return dsv4::launch_gemma_rmsnorm_mxfp8(
+        static_cast<const uint16_t *>(x), static_cast<const uint16_t *>(residual),
+        static_cast<const uint16_t *>(gamma), num_rows, hidden, eps,
+        static_cast<uint16_t *>(residual_out), codes, scales, static_cast<cudaStream_t>(stream));
+}
+
 size_t dsv4_fp8_cache_bytes(int64_t num_blocks, int32_t block_size)
 {
     if (num_blocks < 1 || block_size < 1)

@@ -188,3 +188,25 @@ def test_kv_only_and_prenormalised_entries_validate():
 ])
 def test_gather_validation(args, status):
     assert k.lib().dsv4_dequant_gather(*args, None) == status
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(m=-1), k.ERR_SHAPE), (dict(n=64), k.ERR_SHAPE), (dict(n=200), k.ERR_SHAPE),
+    (dict(n=16512), k.ERR_SHAPE), (dict(eps=-1.0), k.ERR_VALUE), (dict(eps=math.nan), k.ERR_VALUE),
+    (dict(x=None), k.ERR_NULL), (dict(res=None), k.ERR_NULL), (dict(g=None), k.ERR_NULL),
+    (dict(out=None), k.ERR_NULL), (dict(codes=None), k.ERR_NULL), (dict(scales=None), k.ERR_NULL),
+    (dict(x=A + 8), k.ERR_ALIGN), (dict(res=A + 2), k.ERR_ALIGN), (dict(g=A + 4), k.ERR_ALIGN),
+    (dict(out=A + 8), k.ERR_ALIGN), (dict(codes=A + 4), k.ERR_ALIGN),
+    (dict(m=0, x=None, res=None, g=None, out=None, codes=None, scales=None), k.OK),
+])
+def test_mxfp8_validation(kw, status):
+    a = dict(x=A, res=A, g=A, m=4, n=1024, eps=1e-6, out=A, codes=A, scales=A + 1)
+    a.update(kw)
+    assert k.lib().dsv4_add_gemma_rmsnorm_mxfp8(a["x"], a["res"], a["g"], a["m"], a["n"], a["eps"],
+                                                a["out"], a["codes"], a["scales"], None) == status
+
+
+def test_mxfp8_scale_bytes():
+    assert k.mxfp8_scale_bytes(1, 128) == 128 * 4
+    assert k.mxfp8_scale_bytes(129, 7168) == 256 * 224
+    assert k.mxfp8_scale_bytes(5, 100) == 0
