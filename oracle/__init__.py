@@ -22,6 +22,8 @@ ERR_SLOT_RANGE = 1
 ERR_POS_RANGE = 2
 FP8_SLOT_BYTES = 584
 FP8_DATA_BYTES = 576
+INDEXER_DIM = 128
+INDEXER_SLOT_BYTES = 132
 
 _lib = None
 
@@ -58,6 +60,10 @@ def _load():
         lib.oracle_e4m3_value_array.argtypes = [vp, vp, i64]
         lib.oracle_dequant_gather.argtypes = [vp, i64, i32, vp, i64, vp]
         lib.oracle_dequant_gather.restype = i32
+        lib.oracle_indexer_k_quant_insert.argtypes = [vp, vp, vp, i64, i32, i64]
+        lib.oracle_indexer_k_quant_insert.restype = i32
+        lib.oracle_indexer_k_gather.argtypes = [vp, i64, i32, vp, i64, vp, vp]
+        lib.oracle_indexer_k_gather.restype = i32
         lib.oracle_gemma_rmsnorm_mxfp8.argtypes = [vp, vp, vp, i64, i64, f32, vp, vp, vp]
         lib.oracle_ue8m0_of_f32.argtypes = [f32]
         lib.oracle_ue8m0_of_f32.restype = ctypes.c_int
@@ -197,6 +203,31 @@ def dequant_gather(cache: np.ndarray, num_blocks: int, block_size: int, slots: n
     err = _load().oracle_dequant_gather(cache.ctypes.data, num_blocks, block_size, sl.ctypes.data,
                                         sl.size, out.ctypes.data)
     return out, int(err)
+
+
+def indexer_k_quant_insert(k: np.ndarray, slots: np.ndarray, cache: np.ndarray, num_blocks: int,
+                           block_size: int) -> int:
+    """Quantise indexer K rows (bf16 bits [T, 128]) into the indexer cache
+    (uint8, num_blocks * block_size * 132 bytes) in place; returns the error bits."""
+    k = _c(k, np.uint16)
+    sl = _c(slots, np.int64)
+    assert k.size == sl.size * INDEXER_DIM
+    assert cache.dtype == np.uint8 and cache.flags.c_contiguous
+    assert cache.size == num_blocks * block_size * INDEXER_SLOT_BYTES
+    return int(_load().oracle_indexer_k_quant_insert(k.ctypes.data, sl.ctypes.data, cache.ctypes.data,
+                                                     num_blocks, block_size, sl.size))
+
+
+def indexer_k_gather(cache: np.ndarray, num_blocks: int, block_size: int, slots: np.ndarray):
+    """(codes uint8 [n, 128], scales float32 [n], error bits) read from the indexer cache."""
+    cache = _c(cache, np.uint8)
+    assert cache.size == num_blocks * block_size * INDEXER_SLOT_BYTES
+    sl = _c(slots, np.int64)
+    k_out = np.empty((sl.size, INDEXER_DIM), dtype=np.uint8)
+    scale = np.empty(sl.size, dtype=np.float32)
+    err = _load().oracle_indexer_k_gather(cache.ctypes.data, num_blocks, block_size, sl.ctypes.data,
+                                          sl.size, k_out.ctypes.data, scale.ctypes.data)
+    return k_out, scale, int(err)
 
 
 def mxfp8_scale_bytes(m: int, n: int) -> int:

@@ -550,3 +550,101 @@ void oracle_ue8m0_exponent_array(const double *amax, int32_t *out, int64_t n)
     for (int64_t i = 0; i < n; ++i)
         out[i] = oracle_ue8m0_exponent(amax[i]);
 }
+
+/* ------------------------------------------------ indexer-K quant + insert */
+
+/*
+ * The lightning indexer scores queries against K rows that arrive as a
+ * contiguous [N, 128] E4M3 buffer with one non-negative fp32 scale per row
+ * (rocm-aiter PR #1, "Motivation": kv_scale[n], the K rows gathered out of the
+ * paged cache beforehand), and the norm-rope-store kernel keeps a separate
+ * indexer path ([SG] "Modifications").  Per token t with a valid slot:
+ *   amax  = max |k[t, d]| over the 128 dims (exact: the inputs are bf16)
+ *   s     = the smallest integer with amax <= 448 * 2^s, clamped to [-127, 127]
+ *           (the same power-of-two rule as the 64-element blocks above)
+ *   scale = 2^s as fp32 (exact, 2^-127 being an fp32 subnormal)
+ *   code  = E4M3(k[t, d] * 2^-s)
+ * Cache layout, chosen like the FP8 KV cache's: block b occupies
+ * [b*bs*132, (b+1)*bs*132); slot o's 128 codes sit at b*bs*132 + o*128 and its
+ * scale (little-endian fp32) at b*bs*132 + bs*128 + o*4.
+ * slot < 0: nothing written; slot >= num_blocks * bs: nothing written and
+ * error bit ERR_SLOT_RANGE.
+ */
+enum { IDX_DIM = 128, IDX_SLOT_BYTES = 132 };
+
+static void put_f32_le(uint8_t *p, float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    for (int i = 0; i < 4; ++i)
+        p[i] = (uint8_t)(u >> (8 * i));
+}
+
+static float get_f32_le(const uint8_t *p)
+{
+    uint32_t u = (uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16) |
+                 ((uint32_t)p[3] << 24);
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+int32_t oracle_indexer_k_quant_insert(const uint16_t *k, const int64_t *slots, uint8_t *cache,
+                                      int64_t num_blocks, int32_t block_size, int64_t num_tokens)
+{
+    int32_t err = 0;
+    const int64_t num_slots = num_blocks * (int64_t)block_size;
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        const int64_t slot = slots[t];
+        if (slot < 0)
+            continue;
+        if (slot >= num_slots) {
+            err |= ERR_SLOT_RANGE;
+            continue;
+        }
+        const uint16_t *row = k + t * IDX_DIM;
+        double amax = 0.0;
+        for (int d = 0; d < IDX_DIM; ++d) {
+            double a = fabs(oracle_bf16_value(row[d]));
+            if (a > amax)
+                amax = a;
+        }
+        const int s = oracle_ue8m0_exponent(amax);
+        const int64_t blk = slot / block_size, off = slot % block_size;
+        uint8_t *base = cache + blk * (int64_t)block_size * IDX_SLOT_BYTES;
+        uint8_t *codes = base + off * IDX_DIM;
+        for (int d = 0; d < IDX_DIM; ++d)
+            codes[d] = oracle_e4m3_rne(ldexp(oracle_bf16_value(row[d]), -s));
+        put_f32_le(base + (int64_t)block_size * IDX_DIM + off * 4, (float)ldexp(1.0, s));
+    }
+    return err;
+}
+
+/*
+ * The reader the indexer's prefill path calls before scoring: for each n, the
+ * 128 codes and the fp32 scale stored at slots[n], copied unchanged into
+ * contiguous k_out [n, 128] and scale_out [n].  A negative slot gives zero
+ * codes and scale 0; a slot past the cache the same plus ERR_SLOT_RANGE.
+ */
+int32_t oracle_indexer_k_gather(const uint8_t *cache, int64_t num_blocks, int32_t block_size,
+                                const int64_t *slots, int64_t n_rows, uint8_t *k_out,
+                                float *scale_out)
+{
+    int32_t err = 0;
+    const int64_t num_slots = num_blocks * (int64_t)block_size;
+    for (int64_t n = 0; n < n_rows; ++n) {
+        const int64_t slot = slots[n];
+        if (slot < 0 || slot >= num_slots) {
+            if (slot >= num_slots)
+                err |= ERR_SLOT_RANGE;
+            memset(k_out + n * IDX_DIM, 0, IDX_DIM);
+            scale_out[n] = 0.0f;
+            continue;
+        }
+        const int64_t blk = slot / block_size, off = slot % block_size;
+        const uint8_t *base = cache + blk * (int64_t)block_size * IDX_SLOT_BYTES;
+        memcpy(k_out + n * IDX_DIM, base + off * IDX_DIM, IDX_DIM);
+        scale_out[n] = get_f32_le(base + (int64_t)block_size * IDX_DIM + off * 4);
+    }
+    return err;
+}

@@ -23,6 +23,7 @@ _LIB_PATH = os.path.join(_HERE, "libsynth.so")
 # tensor ids of the counter-based streams
 TID_Q, TID_KV, TID_W, TID_POS, TID_SLOT, TID_POISON, TID_SKIP = 1, 2, 3, 4, 5, 7, 8
 TID_Q_TAIL, TID_KV_TAIL = 9, 10
+TID_IDX_K, TID_IDX_K_TAIL = 11, 12
 
 _lib = None
 

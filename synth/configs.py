@@ -118,6 +118,22 @@ def kv_bits(w: Workload, t0: int = 0, t1: int | None = None, out_ptr: int | None
                              tail_id=synth.TID_KV_TAIL, out_ptr=out_ptr)
 
 
+INDEXER_DIM = 128
+
+
+def indexer_k_bits(w: Workload, t0: int = 0, t1: int | None = None) -> np.ndarray:
+    """bf16 bits of the indexer K rows k[t0:t1] (flattened [t1-t0, 128]), with the
+    workload's tail share and multiplier."""
+    t1 = w.T if t1 is None else t1
+    return synth.normal_bf16((t1 - t0) * INDEXER_DIM, w.seed, synth.TID_IDX_K, start=t0 * INDEXER_DIM,
+                             tail_frac=w.tail_frac, tail_mult=w.tail_mult,
+                             tail_id=synth.TID_IDX_K_TAIL)
+
+
+def indexer_cache_bytes(w: Workload) -> int:
+    return w.num_slots * (INDEXER_DIM + 4)
+
+
 def weight_bits(w: Workload) -> np.ndarray:
     return synth.normal_bf16(HEAD_DIM, w.seed, synth.TID_W, mean=1.0, std=0.1)
 
