@@ -211,13 +211,15 @@ def copy_ceiling_gbs(dev, nbytes: int) -> float:
 
 # ------------------------------------------------------------------ inputs on the device
 
-OPS = ("fused", "prenorm", "kv_only", "gather", "mxfp8")
+OPS = ("fused", "prenorm", "kv_only", "gather", "mxfp8", "indexer", "indexer_gather")
 IO_OF_OP = {
     "fused": "bf16 q, kv in; bf16 q, FP8 (e4m3 + ue8m0 + bf16) or bf16 cache rows out",
     "prenorm": "bf16 q, normalised kv in; bf16 q, FP8 cache rows out",
     "kv_only": "bf16 kv in; FP8 or bf16 cache rows out",
     "gather": "FP8 cache rows in; bf16 rows out",
     "mxfp8": "bf16 x, residual in; bf16 residual, e4m3 codes, swizzled ue8m0 scales out",
+    "indexer": "bf16 indexer K [T, 128] in; e4m3 codes + fp32 power-of-two scale rows out",
+    "indexer_gather": "indexer cache rows in; contiguous e4m3 [T, 128] + fp32 [T] out",
 }
 MXFP8_HIDDEN = 7168
 VARIANTS = {"auto": 0, "small": 1, "stream": 2, "bulk": 3}
@@ -232,7 +234,7 @@ class DeviceBatch:
     def __init__(self, wl: configs.Workload, dev, op: str = "fused", variant: int = 0):
         import torch
         self.variant = variant
-        if op in ("kv_only", "gather", "mxfp8"):
+        if op in ("kv_only", "gather", "mxfp8", "indexer", "indexer_gather"):
             wl = dataclasses.replace(wl, H=0)
         self.wl = wl
         self.op = op
@@ -240,7 +242,7 @@ class DeviceBatch:
         g = torch.Generator(device=dev)
         g.manual_seed(wl.seed * 7919 + 17)
         self.q = self._normal((wl.T, wl.H, 512), g)
-        self.kv = self._normal((wl.T, 512), g)
+        self.kv = self._normal((wl.T, 512), g) if not op.startswith("indexer") else None
         self.positions_np = wl.positions()
         self.slots_np = wl.slot_mapping()
         self.w = torch.from_numpy(configs.weight_bits(wl).view(np.int16)).view(torch.bfloat16).to(dev)
@@ -263,6 +265,21 @@ class DeviceBatch:
             self.mx_scales = torch.empty(k.mxfp8_scale_bytes(wl.T, n), dtype=torch.uint8,
                                          device=dev)
             self.bytes = wl.T * n * (2 + 2 + 2 + 1) + self.mx_scales.numel() + 2 * n
+        if op.startswith("indexer"):
+            # indexer K rows [T, 128] and their paged cache (132 bytes per slot)
+            import kv_norm_rope_gb300 as k
+            self.k = self._normal((wl.T, 128), g)
+            self.idx_cache = torch.zeros(k.indexer_cache_bytes(wl.num_blocks, wl.block_size),
+                                         dtype=torch.uint8, device=dev)
+            valid = int((self.slots_np >= 0).sum())
+            self.bytes = wl.T * 8 + valid * (256 + 132)
+            if op == "indexer_gather":
+                k.indexer_k_quant_insert(self.k, self.slots, self.idx_cache, wl.num_blocks,
+                                         wl.block_size)
+                del self.k
+                self.k_out = torch.empty((wl.T, 128), dtype=torch.uint8, device=dev)
+                self.scale_out = torch.empty(wl.T, dtype=torch.float32, device=dev)
+                self.bytes = wl.T * (8 + 132) + valid * 132
         if op == "gather":
             if wl.store != "fp8":
                 raise ValueError("the reader reads FP8 caches")
@@ -297,6 +314,15 @@ class DeviceBatch:
             return lib.dsv4_add_gemma_rmsnorm_mxfp8, (
                 self.x.data_ptr(), self.res.data_ptr(), self.gamma.data_ptr(), wl.T, MXFP8_HIDDEN,
                 wl.eps, self.res.data_ptr(), self.codes.data_ptr(), self.mx_scales.data_ptr(),
+                stream_handle)
+        if self.op == "indexer":
+            return lib.dsv4_indexer_k_quant_insert, (
+                self.k.data_ptr(), self.slots.data_ptr(), self.idx_cache.data_ptr(), wl.num_blocks,
+                wl.block_size, wl.T, self.err.data_ptr(), stream_handle)
+        if self.op == "indexer_gather":
+            return lib.dsv4_indexer_k_gather, (
+                self.idx_cache.data_ptr(), wl.num_blocks, wl.block_size, self.slots.data_ptr(),
+                wl.T, self.k_out.data_ptr(), self.scale_out.data_ptr(), self.err.data_ptr(),
                 stream_handle)
         if self.op == "gather":
             return lib.dsv4_dequant_gather, (
@@ -635,7 +661,8 @@ def main(argv=None):
     ap.add_argument("--op", choices=OPS, default="fused",
                     help="fused (default); prenorm: KV arrives normalised; kv_only: no q; "
                          "gather: read the FP8 cache back out; mxfp8: residual add + Gemma "
-                         "RMSNorm + MXFP8 of [T, 7168] activation rows")
+                         "RMSNorm + MXFP8 of [T, 7168] activation rows; indexer: indexer-K "
+                         "quant-insert of [T, 128] rows; indexer_gather: read them back out")
     ap.add_argument("--e2e-steps", type=int, default=6)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

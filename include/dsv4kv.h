@@ -64,7 +64,9 @@ enum {
     DSV4_FP8_DATA_BYTES = 576,  /* 448 E4M3 + 64 bf16 */
     DSV4_FP8_SCALE_BYTES = 8,   /* 7 UE8M0 bytes + 1 zero pad byte */
     DSV4_FP8_SLOT_BYTES = 584,
-    DSV4_BF16_SLOT_BYTES = 1024
+    DSV4_BF16_SLOT_BYTES = 1024,
+    DSV4_INDEXER_DIM = 128,        /* indexer K width: one E4M3 row with one fp32 scale */
+    DSV4_INDEXER_SLOT_BYTES = 132  /* 128 E4M3 codes + 4 scale bytes per slot */
 };
 
 /* bits OR-ed into *device_error */
@@ -267,6 +269,53 @@ int dsv4_launch_plan(int64_t num_tokens, int32_t num_heads, int32_t sm_count,
 size_t dsv4_fp8_cache_bytes(int64_t num_blocks, int32_t block_size);
 /* Bytes of a bf16 cache: num_blocks*block_size*1024. */
 size_t dsv4_bf16_cache_bytes(int64_t num_blocks, int32_t block_size);
+
+/*
+ * Indexer-K quant-insert.  The lightning indexer scores queries against K rows
+ * held as E4M3 [N, 128] with one non-negative fp32 scale per row (rocm-aiter
+ * PR #1, "Motivation": k_fp8 and kv_scale, gathered out of the paged cache
+ * before scoring); the norm-rope-store kernel keeps this indexer path beside
+ * the KV path (SGLang PR #33358, "Modifications").  Per token t with
+ * 0 <= slot_mapping[t] < num_blocks*block_size:
+ *   s      = the smallest integer with max|k[t,:]| <= 448 * 2^s, clamped to [-127, 127]
+ *   codes  = E4M3_rn_satfinite(k[t,:] * 2^-s);   scale = 2^s (fp32, exact)
+ * Cache layout: block b occupies bytes [b*bs*132, (b+1)*bs*132); slot o's 128 codes
+ * sit at b*bs*132 + o*128 and its scale (fp32, little-endian) at b*bs*132 + bs*128 + o*4.
+ *
+ *  k              (device) bf16 [num_tokens, 128], 16-byte aligned, finite values.
+ *  slot_mapping   (device) int64 [num_tokens], 8-byte aligned; < 0: the token writes
+ *                 nothing; >= num_blocks*block_size: nothing written and
+ *                 DSV4_DEVERR_SLOT_RANGE.  Non-negative slots are distinct.
+ *  indexer_cache  (device) uint8, dsv4_indexer_cache_bytes(num_blocks, block_size)
+ *                 bytes, 4-byte aligned (8-byte aligned with an even block_size
+ *                 takes 8-byte stores).  Bytes of slots no token names are untouched.
+ *  num_tokens >= 0 (0: no launch); num_blocks, block_size >= 1.
+ * Returns a dsv4_status.
+ */
+int dsv4_indexer_k_quant_insert(const void *k, const int64_t *slot_mapping,
+                                uint8_t *indexer_cache, int64_t num_blocks, int32_t block_size,
+                                int64_t num_tokens, int32_t *device_error, void *stream);
+
+/*
+ * Indexer-K gather: for each n, the 128 codes and the fp32 scale stored at
+ * slots[n] copied unchanged to k_out[n,:] and scale_out[n] -- the contiguous
+ * [N, 128] E4M3 + [N] fp32 form the indexer scores against (rocm-aiter PR #1,
+ * "Motivation").  A negative slot gives zero codes and scale 0; a slot
+ * >= num_blocks*block_size the same and DSV4_DEVERR_SLOT_RANGE.
+ *
+ *  indexer_cache  (device) the layout of dsv4_indexer_k_quant_insert, 4-byte aligned.
+ *  slots          (device) int64 [num_rows], 8-byte aligned.
+ *  k_out          (device) uint8 [num_rows, 128], 8-byte aligned.
+ *  scale_out      (device) fp32 [num_rows], 4-byte aligned.
+ *  num_rows >= 0 (0: no launch); num_blocks, block_size >= 1.
+ * Returns a dsv4_status.
+ */
+int dsv4_indexer_k_gather(const uint8_t *indexer_cache, int64_t num_blocks, int32_t block_size,
+                          const int64_t *slots, int64_t num_rows, uint8_t *k_out,
+                          float *scale_out, int32_t *device_error, void *stream);
+
+/* Bytes of an indexer cache of num_blocks x block_size slots: num_blocks*block_size*132. */
+size_t dsv4_indexer_cache_bytes(int64_t num_blocks, int32_t block_size);
 
 /* Static string naming a dsv4_status value ("unknown status" otherwise). */
 const char *dsv4_status_string(int status);

@@ -21,8 +21,8 @@ _CSRC = os.path.join(_HERE, "csrc")
 _INCLUDE = os.path.join(_ROOT, "include")
 LIB_PATH = os.path.join(_HERE, "libdsv4kv.so")
 _SOURCES = ["qnorm_rope_kv_insert.cu", "qnorm_rope_kv_insert_bulk.cu", "dequant_gather.cu",
-            "gemma_rmsnorm_mxfp8.cu", "api.cpp"]
-_HEADERS = [os.path.join(_INCLUDE, "dsv4kv.h"), os.path.join(_CSRC, "launch.h"),
+            "gemma_rmsnorm_mxfp8.cu", "indexer_k.cu", "api.cpp"]
+_HEADERS = [os.path.join(_INCLUDE, "dsv4kv.h"), os.path.join(_CSRC, "launch.h"), os.path.join(_CSRC, "ops.h"),
             os.path.join(_CSRC, "rowmath.cuh")]
 NVCC_ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -37,7 +37,8 @@ EXPORTS = ("dsv4_qnorm_rope_kv_quant_insert", "dsv4_qnorm_rope_kv_bf16_insert",
            "dsv4_qnorm_rope_kv_insert_variant", "dsv4_qnorm_rope_kv_rope_quant_insert",
            "dsv4_kv_norm_rope_insert", "dsv4_insert_ex", "dsv4_dequant_gather",
            "dsv4_add_gemma_rmsnorm_mxfp8", "dsv4_mxfp8_scale_bytes", "dsv4_launch_plan",
-           "dsv4_fp8_cache_bytes", "dsv4_bf16_cache_bytes", "dsv4_status_string")
+           "dsv4_fp8_cache_bytes", "dsv4_bf16_cache_bytes", "dsv4_indexer_k_quant_insert",
+           "dsv4_indexer_k_gather", "dsv4_indexer_cache_bytes", "dsv4_status_string")
 
 
 class Dsv4Error(RuntimeError):
@@ -128,6 +129,12 @@ def lib():
         L.dsv4_fp8_cache_bytes.restype = ctypes.c_size_t
         L.dsv4_bf16_cache_bytes.argtypes = [i64, i32]
         L.dsv4_bf16_cache_bytes.restype = ctypes.c_size_t
+        L.dsv4_indexer_k_quant_insert.argtypes = [vp, vp, vp, i64, i32, i64, vp, vp]
+        L.dsv4_indexer_k_quant_insert.restype = c_int
+        L.dsv4_indexer_k_gather.argtypes = [vp, i64, i32, vp, i64, vp, vp, vp, vp]
+        L.dsv4_indexer_k_gather.restype = c_int
+        L.dsv4_indexer_cache_bytes.argtypes = [i64, i32]
+        L.dsv4_indexer_cache_bytes.restype = ctypes.c_size_t
         L.dsv4_status_string.argtypes = [c_int]
         L.dsv4_status_string.restype = ctypes.c_char_p
         _lib = L
@@ -271,6 +278,32 @@ def dequant_gather(kv_cache, num_blocks: int, block_size: int, slots, out, devic
                                    _stream_handle(stream))
     if st != OK:
         raise Dsv4Error(st, "dsv4_dequant_gather")
+
+
+def indexer_cache_bytes(num_blocks: int, block_size: int) -> int:
+    return int(lib().dsv4_indexer_cache_bytes(num_blocks, block_size))
+
+
+def indexer_k_quant_insert(k, slot_mapping, indexer_cache, num_blocks: int, block_size: int,
+                           device_error=None, stream=None) -> None:
+    """dsv4_indexer_k_quant_insert: k (bf16 [T, 128]) quantised into the indexer cache
+    (uint8, indexer_cache_bytes(num_blocks, block_size)) at slot_mapping (int64 [T])."""
+    st = lib().dsv4_indexer_k_quant_insert(_ptr(k), _ptr(slot_mapping), _ptr(indexer_cache),
+                                           num_blocks, block_size, int(slot_mapping.shape[0]),
+                                           _ptr(device_error), _stream_handle(stream))
+    if st != OK:
+        raise Dsv4Error(st, "dsv4_indexer_k_quant_insert")
+
+
+def indexer_k_gather(indexer_cache, num_blocks: int, block_size: int, slots, k_out, scale_out,
+                     device_error=None, stream=None) -> None:
+    """dsv4_indexer_k_gather: k_out (uint8 [n, 128]) and scale_out (fp32 [n]) read from
+    the indexer cache at ``slots`` (int64 [n])."""
+    st = lib().dsv4_indexer_k_gather(_ptr(indexer_cache), num_blocks, block_size, _ptr(slots),
+                                     int(slots.shape[0]), _ptr(k_out), _ptr(scale_out),
+                                     _ptr(device_error), _stream_handle(stream))
+    if st != OK:
+        raise Dsv4Error(st, "dsv4_indexer_k_gather")
 
 
 def mxfp8_scale_bytes(num_rows: int, hidden: int) -> int:

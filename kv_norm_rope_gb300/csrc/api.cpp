@@ -10,6 +10,7 @@
 
 #include "dsv4kv.h"
 #include "launch.h"
+#include "ops.h"
 
 namespace {
 
@@ -48,6 +49,38 @@ int device_shape(int store_mode, int32_t *sms, int32_t *ctas)
         g_sms[dev].store(n, std::memory_order_relaxed);
         g_ctas[dev][store_mode].store(c, std::memory_order_relaxed);
     }
+    return DSV4_OK;
+}
+
+// CTAs per SM of the reader and indexer kernels, cached per device beside the
+// SM count; resident = SMs x CTAs per SM, the cap of their persistent grids.
+enum { kOccGather = 0, kOccIndexer = 1, kOccKinds = 2 };
+std::atomic<int32_t> g_occ[kMaxDevices][kOccKinds];
+
+int resident_ctas(int kind, int64_t *resident)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return DSV4_ERR_CUDA;
+    const bool cached = dev >= 0 && dev < kMaxDevices;
+    int sms = cached ? g_sms[dev].load(std::memory_order_relaxed) : 0;
+    int per = cached ? g_occ[dev][kind].load(std::memory_order_relaxed) : 0;
+    if (sms < 1) {
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            sms < 1)
+            return DSV4_ERR_CUDA;
+        if (cached)
+            g_sms[dev].store(sms, std::memory_order_relaxed);
+    }
+    if (per < 1) {
+        const int rc = kind == kOccGather ? dsv4::gather_ctas_per_sm(&per)
+                                          : dsv4::indexer_ctas_per_sm(&per);
+        if (rc != DSV4_OK || per < 1)
+            return DSV4_ERR_CUDA;
+        if (cached)
+            g_occ[dev][kind].store(per, std::memory_order_relaxed);
+    }
+    *resident = int64_t(sms) * per;
     return DSV4_OK;
 }
 
@@ -253,15 +286,12 @@ int dsv4_dequant_gather(const uint8_t *kv_cache, int64_t num_blocks, int32_t blo
     if (!aligned(kv_cache, 8) || !aligned(slots, 8) || !aligned(out, 16) ||
         !aligned(device_error, 4))
         return DSV4_ERR_ALIGN;
-    int dev = 0, sms = 0, per_sm = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        dsv4::gather_ctas_per_sm(&per_sm) != DSV4_OK || sms < 1 || per_sm < 1)
+    int64_t resident = 0;
+    if (resident_ctas(kOccGather, &resident) != DSV4_OK)
         return DSV4_ERR_CUDA;
     const int64_t groups = (num_rows + dsv4::gather_rows_per_warp() - 1) /
                            dsv4::gather_rows_per_warp();
     const int64_t need = (groups + 7) / 8;  // 8 warps per CTA
-    const int64_t resident = int64_t(sms) * per_sm;
     return dsv4::launch_gather(kv_cache, num_blocks, block_size, slots, num_rows,
                                static_cast<uint16_t *>(out), device_error,
                                need < resident ? need : resident,
@@ -296,6 +326,59 @@ int dsv4_add_gemma_rmsnorm_mxfp8(const void *x, const void *residual, const void
         static_cast<const uint16_t *>(x), static_cast<const uint16_t *>(residual),
         static_cast<const uint16_t *>(gamma), num_rows, hidden, eps,
         static_cast<uint16_t *>(residual_out), codes, scales, static_cast<cudaStream_t>(stream));
+}
+
+int dsv4_indexer_k_quant_insert(const void *k, const int64_t *slot_mapping,
+                                uint8_t *indexer_cache, int64_t num_blocks, int32_t block_size,
+                                int64_t num_tokens, int32_t *device_error, void *stream)
+{
+    if (num_tokens < 0 || num_blocks < 1 || block_size < 1)
+        return DSV4_ERR_SHAPE;
+    if (num_blocks > (INT64_MAX / 4096) / block_size || num_tokens > INT64_MAX / 4096)
+        return DSV4_ERR_SHAPE;
+    if (num_tokens == 0)
+        return DSV4_OK;
+    if (!k || !slot_mapping || !indexer_cache)
+        return DSV4_ERR_NULL;
+    if (!aligned(k, 16) || !aligned(slot_mapping, 8) || !aligned(indexer_cache, 4) ||
+        !aligned(device_error, 4))
+        return DSV4_ERR_ALIGN;
+    int64_t resident = 0;
+    if (resident_ctas(kOccIndexer, &resident) != DSV4_OK)
+        return DSV4_ERR_CUDA;
+    return dsv4::launch_indexer_insert(static_cast<const uint16_t *>(k), slot_mapping,
+                                       indexer_cache, num_blocks, block_size, num_tokens,
+                                       device_error, resident, static_cast<cudaStream_t>(stream));
+}
+
+int dsv4_indexer_k_gather(const uint8_t *indexer_cache, int64_t num_blocks, int32_t block_size,
+                          const int64_t *slots, int64_t num_rows, uint8_t *k_out,
+                          float *scale_out, int32_t *device_error, void *stream)
+{
+    if (num_rows < 0 || num_blocks < 1 || block_size < 1)
+        return DSV4_ERR_SHAPE;
+    if (num_blocks > (INT64_MAX / 4096) / block_size || num_rows > INT64_MAX / 4096)
+        return DSV4_ERR_SHAPE;
+    if (num_rows == 0)
+        return DSV4_OK;
+    if (!indexer_cache || !slots || !k_out || !scale_out)
+        return DSV4_ERR_NULL;
+    if (!aligned(indexer_cache, 4) || !aligned(slots, 8) || !aligned(k_out, 8) ||
+        !aligned(scale_out, 4) || !aligned(device_error, 4))
+        return DSV4_ERR_ALIGN;
+    int64_t resident = 0;
+    if (resident_ctas(kOccIndexer, &resident) != DSV4_OK)
+        return DSV4_ERR_CUDA;
+    return dsv4::launch_indexer_gather(indexer_cache, num_blocks, block_size, slots, num_rows,
+                                       k_out, scale_out, device_error, resident,
+                                       static_cast<cudaStream_t>(stream));
+}
+
+size_t dsv4_indexer_cache_bytes(int64_t num_blocks, int32_t block_size)
+{
+    if (num_blocks < 1 || block_size < 1)
+        return 0;
+    return size_t(num_blocks) * size_t(block_size) * DSV4_INDEXER_SLOT_BYTES;
 }
 
 size_t dsv4_fp8_cache_bytes(int64_t num_blocks, int32_t block_size)

@@ -19,7 +19,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "launch.h"
+#include "ops.h"
 
 namespace dsv4 {
 namespace {

@@ -1,0 +1,263 @@
+// Indexer-K quant-insert and gather.  The lightning indexer scores queries
+// against K rows held as E4M3 with one non-negative fp32 scale per 128-dim row
+// (rocm-aiter PR #1, "Motivation": q_fp8 against k_fp8 [N, 128] with kv_scale
+// [N], gathered out of the paged cache first); the norm-rope-store kernel keeps
+// this indexer path beside the KV one (SGLang PR #33358, "Modifications").
+//
+// Insert, per token t with 0 <= slot < num_slots:
+//   amax  = max |k[t, :]|                          (exact: k is bf16)
+//   s     = smallest integer with amax <= 448 * 2^s, clamped to [-127, 127]
+//   codes = E4M3_rn_satfinite(k[t, :] * 2^-s)      (an exact power-of-two scaling)
+//   scale = 2^s as fp32 (2^-127 is the fp32 subnormal 0x00400000)
+// written at block b = slot / bs, offset o: codes at b*bs*132 + o*128, scale at
+// b*bs*132 + bs*128 + o*4.  A negative slot writes nothing; a slot past the
+// cache writes nothing and raises DSV4_DEVERR_SLOT_RANGE.
+// Gather: codes and scale of slots[n] copied to k_out[n, :] and scale_out[n];
+// zeros for a negative slot, zeros and DSV4_DEVERR_SLOT_RANGE past the cache.
+//
+// Both are HBM-bound copies with a little integer work.  Half a warp holds one
+// row (lane h: dims [8h, 8h + 8), one 16-byte load of k), so one warp-wide load
+// reads two adjacent rows, 512 contiguous bytes.  The scale needs no floating
+// point: for non-negative bf16 bit patterns integer order is magnitude order,
+// so amax is an integer max of (bits & 0x7fff), and with amax = (1 + m/128) *
+// 2^(E - 127), s = E - 135 + (m > 0x60) (the mantissa above 1.75 = 448 / 256).
+// Each warp loads kPairs row pairs before it uses any of them.
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ops.h"
+
+namespace dsv4 {
+namespace {
+
+constexpr int kDim = DSV4_INDEXER_DIM;                // 128 dims, 256 bf16 bytes
+constexpr int kSlotBytes = DSV4_INDEXER_SLOT_BYTES;   // 128 codes + 4 scale bytes
+constexpr int kPairs = 4;                             // row pairs a warp loads together
+constexpr int kThreads = 256;
+constexpr unsigned kFull = 0xffffffffu;
+
+struct IParams {
+    const uint16_t *k;        // insert input, bf16 [rows, 128]
+    const uint8_t *src;       // gather input: the indexer cache
+    uint8_t *cache;           // insert output
+    uint8_t *k_out;           // gather outputs
+    float *scale_out;
+    const int64_t *slots;
+    int64_t rows;
+    int64_t num_slots;
+    int32_t block_size;
+    int32_t *err;
+};
+
+__device__ __forceinline__ uint32_t e4m3x4_rn(float e0, float e1, float e2, float e3)
+{
+    uint32_t r;
+    asm("{\n\t.reg .b16 p01, p23;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 p01, %2, %1;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 p23, %4, %3;\n\t"
+        "mov.b32 %0, {p01, p23};\n\t}"
+        : "=r"(r)
+        : "f"(e0), "f"(e1), "f"(e2), "f"(e3));
+    return r;
+}
+
+// the low and the high bf16 of a 32-bit word, widened to fp32 (exact)
+__device__ __forceinline__ float lo_f32(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float hi_f32(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// the 8 codes of one lane: E4M3(x * inv) for the 8 bf16 of v
+__device__ __forceinline__ uint2 encode8(uint4 v, float inv)
+{
+    return make_uint2(e4m3x4_rn(__fmul_rn(lo_f32(v.x), inv), __fmul_rn(hi_f32(v.x), inv),
+                                __fmul_rn(lo_f32(v.y), inv), __fmul_rn(hi_f32(v.y), inv)),
+                      e4m3x4_rn(__fmul_rn(lo_f32(v.z), inv), __fmul_rn(hi_f32(v.z), inv),
+                                __fmul_rn(lo_f32(v.w), inv), __fmul_rn(hi_f32(v.w), inv)));
+}
+
+// the scale exponent s of a row from the bits of its amax (bf16, sign cleared)
+__device__ __forceinline__ int row_exponent(uint32_t amax_bits)
+{
+    const int e = int(amax_bits >> 7), m = int(amax_bits & 0x7fu);
+    const int s = e == 0 ? -127 : e - 135 + (m > 0x60 ? 1 : 0);
+    return s < -127 ? -127 : (s > 127 ? 127 : s);
+}
+
+template <bool kWide>
+__device__ __forceinline__ void store_codes(uint8_t *p, uint2 c)
+{
+    if (kWide) {
+        __stcs(reinterpret_cast<uint2 *>(p), c);
+    } else {
+        __stcs(reinterpret_cast<unsigned *>(p), c.x);
+        __stcs(reinterpret_cast<unsigned *>(p + 4), c.y);
+    }
+}
+
+template <bool kWide>
+__device__ __forceinline__ uint2 load_codes(const uint8_t *p)
+{
+    if (kWide)
+        return __ldcs(reinterpret_cast<const uint2 *>(p));
+    return make_uint2(__ldcs(reinterpret_cast<const unsigned *>(p)),
+                      __ldcs(reinterpret_cast<const unsigned *>(p + 4)));
+}
+
+// kWide: every code row starts on an 8-byte boundary (the cache is 8-byte
+// aligned and the block size even), so each lane stores its 8 codes at once
+template <bool kWide>
+__global__ void __launch_bounds__(kThreads) indexer_k_insert_kernel(const IParams p)
+{
+    const int lane = threadIdx.x & 31, half = lane >> 4, h = lane & 15;
+    const int64_t warps = int64_t(gridDim.x) * (kThreads / 32);
+    const int64_t groups = (p.rows + 2 * kPairs - 1) / (2 * kPairs);
+    for (int64_t g = int64_t(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5); g < groups;
+         g += warps) {
+        const int64_t t0 = g * 2 * kPairs + half;
+        int64_t slot[kPairs];
+        uint4 x[kPairs];
+#pragma unroll
+        for (int j = 0; j < kPairs; ++j)
+            slot[j] = t0 + 2 * j < p.rows ? __ldg(p.slots + t0 + 2 * j) : -1;
+#pragma unroll
+        for (int j = 0; j < kPairs; ++j)
+            x[j] = t0 + 2 * j < p.rows
+                       ? __ldcs(reinterpret_cast<const uint4 *>(p.k + (t0 + 2 * j) * kDim) + h)
+                       : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int j = 0; j < kPairs; ++j) {
+            const uint32_t m2 = __vmaxu2(__vmaxu2(x[j].x & 0x7fff7fffu, x[j].y & 0x7fff7fffu),
+                                         __vmaxu2(x[j].z & 0x7fff7fffu, x[j].w & 0x7fff7fffu));
+            uint32_t amax = max(m2 & 0xffffu, m2 >> 16);
+#pragma unroll
+            for (int o = 1; o < 16; o <<= 1)  // xor below 16 stays inside the half-warp
+                amax = max(amax, __shfl_xor_sync(kFull, amax, o));
+            if (slot[j] < 0)
+                continue;
+            if (slot[j] >= p.num_slots) {
+                if (h == 0 && p.err != nullptr)
+                    atomicOr(p.err, DSV4_DEVERR_SLOT_RANGE);
+                continue;
+            }
+            const int s = row_exponent(amax);
+            const float inv = __uint_as_float(uint32_t(127 - s) << 23);  // 2^-s, normal
+            const int64_t blk = slot[j] / p.block_size;
+            const int64_t off = slot[j] - blk * p.block_size;
+            uint8_t *base = p.cache + blk * int64_t(p.block_size) * kSlotBytes;
+            store_codes<kWide>(base + off * kDim + 8 * h, encode8(x[j], inv));
+            if (h == 0)
+                __stcs(reinterpret_cast<unsigned *>(base + int64_t(p.block_size) * kDim + off * 4),
+                       s > -127 ? uint32_t(s + 127) << 23 : 0x00400000u);
+        }
+    }
+}
+
+template <bool kWide>
+__global__ void __launch_bounds__(kThreads) indexer_k_gather_kernel(const IParams p)
+{
+    const int lane = threadIdx.x & 31, half = lane >> 4, h = lane & 15;
+    const int64_t warps = int64_t(gridDim.x) * (kThreads / 32);
+    const int64_t groups = (p.rows + 2 * kPairs - 1) / (2 * kPairs);
+    for (int64_t g = int64_t(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5); g < groups;
+         g += warps) {
+        const int64_t n0 = g * 2 * kPairs + half;
+        int64_t slot[kPairs];
+#pragma unroll
+        for (int j = 0; j < kPairs; ++j)
+            slot[j] = n0 + 2 * j < p.rows ? __ldg(p.slots + n0 + 2 * j) : -1;
+        uint2 c[kPairs];
+        unsigned sc[kPairs];
+#pragma unroll
+        for (int j = 0; j < kPairs; ++j) {
+            c[j] = make_uint2(0u, 0u);
+            sc[j] = 0u;
+            if (slot[j] >= 0 && slot[j] < p.num_slots) {
+                const int64_t blk = slot[j] / p.block_size;
+                const int64_t off = slot[j] - blk * p.block_size;
+                const uint8_t *base = p.src + blk * int64_t(p.block_size) * kSlotBytes;
+                c[j] = load_codes<kWide>(base + off * kDim + 8 * h);
+                if (h == 0)
+                    sc[j] = __ldcs(reinterpret_cast<const unsigned *>(
+                        base + int64_t(p.block_size) * kDim + off * 4));
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kPairs; ++j) {
+            const int64_t n = n0 + 2 * j;
+            if (n >= p.rows)
+                continue;
+            if (slot[j] >= p.num_slots && h == 0 && p.err != nullptr)
+                atomicOr(p.err, DSV4_DEVERR_SLOT_RANGE);
+            __stcs(reinterpret_cast<uint2 *>(p.k_out + n * kDim) + h, c[j]);
+            if (h == 0)
+                __stcs(reinterpret_cast<unsigned *>(p.scale_out) + n, sc[j]);
+        }
+    }
+}
+
+int64_t grid_for(int64_t rows, int64_t max_ctas)
+{
+    const int64_t groups = (rows + 2 * kPairs - 1) / (2 * kPairs);
+    const int64_t need = (groups + kThreads / 32 - 1) / (kThreads / 32);
+    return need < max_ctas ? need : max_ctas;
+}
+
+}  // namespace
+
+int indexer_ctas_per_sm(int *ctas_per_sm)
+{
+    // the four kernels use the same block size; take the smallest occupancy
+    int a = 0, b = 0, c = 0, d = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, indexer_k_insert_kernel<true>, kThreads, 0) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, indexer_k_insert_kernel<false>, kThreads, 0) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c, indexer_k_gather_kernel<true>, kThreads, 0) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d, indexer_k_gather_kernel<false>, kThreads, 0) != cudaSuccess)
+        return DSV4_ERR_CUDA;
+    *ctas_per_sm = min(min(a, b), min(c, d));
+    return DSV4_OK;
+}
+
+int launch_indexer_insert(const uint16_t *k, const int64_t *slots, uint8_t *cache,
+                          int64_t num_blocks, int32_t block_size, int64_t rows, int32_t *err,
+                          int64_t max_ctas, cudaStream_t stream)
+{
+    IParams p = {};
+    p.k = k;
+    p.cache = cache;
+    p.slots = slots;
+    p.rows = rows;
+    p.num_slots = num_blocks * int64_t(block_size);
+    p.block_size = block_size;
+    p.err = err;
+    const unsigned grid = static_cast<unsigned>(grid_for(rows, max_ctas));
+    const bool wide = (reinterpret_cast<uintptr_t>(cache) & 7u) == 0 && block_size % 2 == 0;
+    if (wide)
+        indexer_k_insert_kernel<true><<<grid, kThreads, 0, stream>>>(p);
+    else
+        indexer_k_insert_kernel<false><<<grid, kThreads, 0, stream>>>(p);
+    return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
+}
+
+int launch_indexer_gather(const uint8_t *cache, int64_t num_blocks, int32_t block_size,
+                          const int64_t *slots, int64_t rows, uint8_t *k_out, float *scale_out,
+                          int32_t *err, int64_t max_ctas, cudaStream_t stream)
+{
+    IParams p = {};
+    p.src = cache;
+    p.k_out = k_out;
+    p.scale_out = scale_out;
+    p.slots = slots;
+    p.rows = rows;
+    p.num_slots = num_blocks * int64_t(block_size);
+    p.block_size = block_size;
+    p.err = err;
+    const unsigned grid = static_cast<unsigned>(grid_for(rows, max_ctas));
+    const bool wide = (reinterpret_cast<uintptr_t>(cache) & 7u) == 0 && block_size % 2 == 0;
+    if (wide)
+        indexer_k_gather_kernel<true><<<grid, kThreads, 0, stream>>>(p);
+    else
+        indexer_k_gather_kernel<false><<<grid, kThreads, 0, stream>>>(p);
+    return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
+}
+
+}  // namespace dsv4

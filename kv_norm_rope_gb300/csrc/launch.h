@@ -62,11 +62,6 @@ int bulk_threads();
 int bulk_chunk_rows();
 int launch_bulk(int store_mode, bool kv_norm, int64_t ctas, const KParams &p, cudaStream_t stream);
 
-// Residual add + Gemma RMSNorm + MXFP8 rows (gemma_rmsnorm_mxfp8.cu).
-int launch_gemma_rmsnorm_mxfp8(const uint16_t *x, const uint16_t *residual, const uint16_t *gamma,
-                               int64_t m, int32_t n, float eps, uint16_t *residual_out,
-                               uint8_t *codes, uint8_t *scales, cudaStream_t stream);
-
 // The FP8 cache reader (dequant_gather.cu).
 int gather_ctas_per_sm(int *ctas_per_sm);
 int gather_rows_per_warp();

@@ -1,0 +1,28 @@
+// Internal interface between the C-ABI layer (api.cpp) and the kernels of the
+// operations beside the fused step: the MXFP8 activation quantiser
+// (gemma_rmsnorm_mxfp8.cu) and the indexer-K insert and gather (indexer_k.cu).
+// Not installed; not part of the ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dsv4kv.h"
+
+namespace dsv4 {
+
+// Residual add + Gemma RMSNorm + MXFP8 rows.
+int launch_gemma_rmsnorm_mxfp8(const uint16_t *x, const uint16_t *residual, const uint16_t *gamma,
+                               int64_t m, int32_t n, float eps, uint16_t *residual_out,
+                               uint8_t *codes, uint8_t *scales, cudaStream_t stream);
+
+// Indexer-K quant-insert and gather; grids are capped at max_ctas.
+int indexer_ctas_per_sm(int *ctas_per_sm);
+int launch_indexer_insert(const uint16_t *k, const int64_t *slots, uint8_t *cache,
+                          int64_t num_blocks, int32_t block_size, int64_t rows, int32_t *err,
+                          int64_t max_ctas, cudaStream_t stream);
+int launch_indexer_gather(const uint8_t *cache, int64_t num_blocks, int32_t block_size,
+                          const int64_t *slots, int64_t rows, uint8_t *k_out, float *scale_out,
+                          int32_t *err, int64_t max_ctas, cudaStream_t stream);
+
+}  // namespace dsv4

@@ -210,3 +210,47 @@ def test_mxfp8_scale_bytes():
     assert k.mxfp8_scale_bytes(1, 128) == 128 * 4
     assert k.mxfp8_scale_bytes(129, 7168) == 256 * 224
     assert k.mxfp8_scale_bytes(5, 100) == 0
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(T=-1), k.ERR_SHAPE), (dict(nb=0), k.ERR_SHAPE), (dict(bs=0), k.ERR_SHAPE),
+    (dict(nb=2 ** 62), k.ERR_SHAPE),
+    (dict(kp=None), k.ERR_NULL), (dict(sl=None), k.ERR_NULL), (dict(cache=None), k.ERR_NULL),
+    (dict(kp=A + 8), k.ERR_ALIGN), (dict(sl=A + 4), k.ERR_ALIGN), (dict(cache=A + 2), k.ERR_ALIGN),
+    (dict(err=A + 2), k.ERR_ALIGN),
+    (dict(T=0, kp=None, sl=None, cache=None), k.OK),
+])
+def test_indexer_insert_validation(kw, status):
+    a = dict(kp=A, sl=A, cache=A + 4, nb=4, bs=64, T=5, err=None)
+    a.update(kw)
+    assert k.lib().dsv4_indexer_k_quant_insert(a["kp"], a["sl"], a["cache"], a["nb"], a["bs"],
+                                               a["T"], a["err"], None) == status
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(n=-1), k.ERR_SHAPE), (dict(nb=0), k.ERR_SHAPE), (dict(bs=0), k.ERR_SHAPE),
+    (dict(cache=None), k.ERR_NULL), (dict(sl=None), k.ERR_NULL), (dict(out=None), k.ERR_NULL),
+    (dict(scale=None), k.ERR_NULL),
+    (dict(cache=A + 2), k.ERR_ALIGN), (dict(sl=A + 4), k.ERR_ALIGN), (dict(out=A + 4), k.ERR_ALIGN),
+    (dict(scale=A + 2), k.ERR_ALIGN), (dict(err=A + 1), k.ERR_ALIGN),
+    (dict(n=0, cache=None, sl=None, out=None, scale=None), k.OK),
+])
+def test_indexer_gather_validation(kw, status):
+    a = dict(cache=A + 4, nb=4, bs=3, sl=A, n=5, out=A + 8, scale=A + 4, err=None)
+    a.update(kw)
+    assert k.lib().dsv4_indexer_k_gather(a["cache"], a["nb"], a["bs"], a["sl"], a["n"], a["out"],
+                                         a["scale"], a["err"], None) == status
+
+
+def test_indexer_cache_bytes():
+    assert k.indexer_cache_bytes(2048, 64) == 2048 * 64 * 132
+    assert k.indexer_cache_bytes(3, 5) == 3 * 5 * 132
+    assert k.indexer_cache_bytes(0, 64) == 0
+
+
+def test_indexer_entries_have_no_cpu_fallback():
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; covered by the GPU tests")
+    assert k.lib().dsv4_indexer_k_quant_insert(A, A, A, 4, 64, 5, None, None) == k.ERR_CUDA
+    assert k.lib().dsv4_indexer_k_gather(A, 4, 64, A, 5, A, A, None, None) == k.ERR_CUDA
