@@ -35,6 +35,10 @@
  *    two tokens share a slot, which one's row lands is unspecified); q does
  *    not overlap kv, the cache or the metadata arrays; inputs are finite and
  *    sum(x^2) of a row stays below 3.4e38.
+ *  - Every paged cache holds at most 2^32 slots (num_blocks * block_size <=
+ *    2^32; larger returns DSV4_ERR_SHAPE).  At 132 bytes or more per slot such
+ *    a cache exceeds one GPU's memory, and the bound lets the kernels split a
+ *    slot into block and offset with a 32-bit division.
  */
 #ifndef DSV4KV_H
 #define DSV4KV_H
@@ -114,7 +118,7 @@ enum {
  *                 all-zero block gives e_b = 0); payload = E4M3_rn(v * 2^-s_b).
  *                 8-byte aligned.  Bytes of slots that are not written keep
  *                 their previous contents.
- *  num_blocks, block_size   cache geometry (>= 1 each).
+ *  num_blocks, block_size   cache geometry (>= 1 each; num_blocks*block_size <= 2^32).
  *  num_tokens     T >= 0 (T == 0 returns DSV4_OK and launches nothing).
  *  num_heads      H >= 1.
  *  eps            >= 0 and finite; added to mean(x^2) inside the root.
@@ -207,7 +211,7 @@ int dsv4_insert_ex(int store_mode, int variant, int kv_norm, void *q, const void
  *            448..511 -- exact for every row the insert kernels write.  A negative
  *            slot gives a zero row; a slot >= num_blocks*block_size gives a zero row
  *            and DSV4_DEVERR_SLOT_RANGE.
- *  num_rows >= 0 (0: no launch); num_blocks, block_size >= 1.
+ *  num_rows >= 0 (0: no launch); num_blocks, block_size >= 1, num_blocks*block_size <= 2^32.
  * Returns a dsv4_status.
  */
 int dsv4_dequant_gather(const uint8_t *kv_cache, int64_t num_blocks, int32_t block_size,
@@ -289,7 +293,7 @@ size_t dsv4_bf16_cache_bytes(int64_t num_blocks, int32_t block_size);
  *  indexer_cache  (device) uint8, dsv4_indexer_cache_bytes(num_blocks, block_size)
  *                 bytes, 4-byte aligned (8-byte aligned with an even block_size
  *                 takes 8-byte stores).  Bytes of slots no token names are untouched.
- *  num_tokens >= 0 (0: no launch); num_blocks, block_size >= 1.
+ *  num_tokens >= 0 (0: no launch); num_blocks, block_size >= 1, num_blocks*block_size <= 2^32.
  * Returns a dsv4_status.
  */
 int dsv4_indexer_k_quant_insert(const void *k, const int64_t *slot_mapping,
@@ -307,7 +311,7 @@ int dsv4_indexer_k_quant_insert(const void *k, const int64_t *slot_mapping,
  *  slots          (device) int64 [num_rows], 8-byte aligned.
  *  k_out          (device) uint8 [num_rows, 128], 8-byte aligned.
  *  scale_out      (device) fp32 [num_rows], 4-byte aligned.
- *  num_rows >= 0 (0: no launch); num_blocks, block_size >= 1.
+ *  num_rows >= 0 (0: no launch); num_blocks, block_size >= 1, num_blocks*block_size <= 2^32.
  * Returns a dsv4_status.
  */
 int dsv4_indexer_k_gather(const uint8_t *indexer_cache, int64_t num_blocks, int32_t block_size,

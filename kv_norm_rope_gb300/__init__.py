@@ -22,8 +22,8 @@ _INCLUDE = os.path.join(_ROOT, "include")
 LIB_PATH = os.path.join(_HERE, "libdsv4kv.so")
 _SOURCES = ["qnorm_rope_kv_insert.cu", "qnorm_rope_kv_insert_bulk.cu", "dequant_gather.cu",
             "gemma_rmsnorm_mxfp8.cu", "indexer_k.cu", "api.cpp"]
-_HEADERS = [os.path.join(_INCLUDE, "dsv4kv.h"), os.path.join(_CSRC, "launch.h"), os.path.join(_CSRC, "ops.h"),
-            os.path.join(_CSRC, "rowmath.cuh")]
+_HEADERS = [os.path.join(_INCLUDE, "dsv4kv.h")] + [
+    os.path.join(_CSRC, h) for h in ("launch.h", "ops.h", "fastdiv.h", "rowmath.cuh")]
 NVCC_ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 # status codes and constants (mirrors include/dsv4kv.h)

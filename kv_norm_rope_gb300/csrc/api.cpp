@@ -19,6 +19,15 @@ bool aligned(const void *p, uintptr_t a)
     return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
 }
 
+// Caches hold at most 2^32 slots (more than any one GPU can hold at 132 bytes
+// per slot), so the kernels divide 32-bit slot numbers by the block size.
+constexpr int64_t kMaxSlots = int64_t(1) << 32;
+
+bool too_many_slots(int64_t num_blocks, int32_t block_size)
+{
+    return num_blocks > kMaxSlots / block_size;
+}
+
 // Per-device cache of (SM count, CTAs of the streaming kernel per SM) for the
 // two store modes: immutable properties, filled on first use.
 constexpr int kMaxDevices = 64;
@@ -105,7 +114,7 @@ int insert(int store_mode, int variant, int flags, void *q, const void *kv, cons
         return DSV4_ERR_SHAPE;
     // every byte offset the kernels form must fit in int64
     const int64_t lim = INT64_MAX / 4096;
-    if (num_tokens > lim / (int64_t(num_heads) + 1) || num_blocks > lim / block_size ||
+    if (num_tokens > lim / (int64_t(num_heads) + 1) || too_many_slots(num_blocks, block_size) ||
         max_position > lim)
         return DSV4_ERR_SHAPE;
     if (!(eps >= 0.0f) || !std::isfinite(eps))
@@ -277,7 +286,7 @@ int dsv4_dequant_gather(const uint8_t *kv_cache, int64_t num_blocks, int32_t blo
 {
     if (num_rows < 0 || num_blocks < 1 || block_size < 1)
         return DSV4_ERR_SHAPE;
-    if (num_blocks > (INT64_MAX / 4096) / block_size || num_rows > INT64_MAX / 4096)
+    if (too_many_slots(num_blocks, block_size) || num_rows > INT64_MAX / 4096)
         return DSV4_ERR_SHAPE;
     if (num_rows == 0)
         return DSV4_OK;
@@ -334,7 +343,7 @@ int dsv4_indexer_k_quant_insert(const void *k, const int64_t *slot_mapping,
 {
     if (num_tokens < 0 || num_blocks < 1 || block_size < 1)
         return DSV4_ERR_SHAPE;
-    if (num_blocks > (INT64_MAX / 4096) / block_size || num_tokens > INT64_MAX / 4096)
+    if (too_many_slots(num_blocks, block_size) || num_tokens > INT64_MAX / 4096)
         return DSV4_ERR_SHAPE;
     if (num_tokens == 0)
         return DSV4_OK;
@@ -357,7 +366,7 @@ int dsv4_indexer_k_gather(const uint8_t *indexer_cache, int64_t num_blocks, int3
 {
     if (num_rows < 0 || num_blocks < 1 || block_size < 1)
         return DSV4_ERR_SHAPE;
-    if (num_blocks > (INT64_MAX / 4096) / block_size || num_rows > INT64_MAX / 4096)
+    if (too_many_slots(num_blocks, block_size) || num_rows > INT64_MAX / 4096)
         return DSV4_ERR_SHAPE;
     if (num_rows == 0)
         return DSV4_OK;

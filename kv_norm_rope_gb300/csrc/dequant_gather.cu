@@ -17,6 +17,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "fastdiv.h"
 #include "launch.h"
 
 namespace dsv4 {
@@ -28,6 +29,7 @@ struct GParams {
     const uint8_t *cache;
     int64_t num_slots;
     int32_t block_size;
+    uint64_t slot_div;  // fastdiv_magic(block_size)
     const int64_t *slots;
     int64_t rows;
     uint16_t *out;
@@ -106,7 +108,7 @@ __global__ void __launch_bounds__(256) dequant_gather_kernel(const GParams p)
         for (int j = 0; j < kGatherRows; ++j) {
             lo[j] = hi0[j] = hi1[j] = sc[j] = make_uint2(0u, 0u);
             if (slot[j] >= 0 && slot[j] < p.num_slots) {
-                const int64_t blk = slot[j] / p.block_size;
+                const int64_t blk = fastdiv(static_cast<uint32_t>(slot[j]), p.slot_div);
                 const int64_t off = slot[j] - blk * p.block_size;
                 const uint8_t *base = p.cache + blk * int64_t(p.block_size) * DSV4_FP8_SLOT_BYTES;
                 const uint8_t *data = base + off * DSV4_FP8_DATA_BYTES;
@@ -163,6 +165,7 @@ int launch_gather(const uint8_t *cache, int64_t num_blocks, int32_t block_size,
     p.cache = cache;
     p.num_slots = num_blocks * int64_t(block_size);
     p.block_size = block_size;
+    p.slot_div = fastdiv_magic(static_cast<uint32_t>(block_size));
     p.slots = slots;
     p.rows = rows;
     p.out = out;

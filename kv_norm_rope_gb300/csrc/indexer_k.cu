@@ -26,6 +26,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "fastdiv.h"
 #include "ops.h"
 
 namespace dsv4 {
@@ -48,6 +49,7 @@ struct IParams {
     int64_t num_slots;
     int32_t block_size;
     int32_t *err;
+    uint64_t slot_div;  // fastdiv_magic(block_size)
 };
 
 __device__ __forceinline__ uint32_t e4m3x4_rn(float e0, float e1, float e2, float e3)
@@ -141,7 +143,7 @@ __global__ void __launch_bounds__(kThreads) indexer_k_insert_kernel(const IParam
             }
             const int s = row_exponent(amax);
             const float inv = __uint_as_float(uint32_t(127 - s) << 23);  // 2^-s, normal
-            const int64_t blk = slot[j] / p.block_size;
+            const int64_t blk = fastdiv(static_cast<uint32_t>(slot[j]), p.slot_div);
             const int64_t off = slot[j] - blk * p.block_size;
             uint8_t *base = p.cache + blk * int64_t(p.block_size) * kSlotBytes;
             store_codes<kWide>(base + off * kDim + 8 * h, encode8(x[j], inv));
@@ -172,7 +174,7 @@ __global__ void __launch_bounds__(kThreads) indexer_k_gather_kernel(const IParam
             c[j] = make_uint2(0u, 0u);
             sc[j] = 0u;
             if (slot[j] >= 0 && slot[j] < p.num_slots) {
-                const int64_t blk = slot[j] / p.block_size;
+                const int64_t blk = fastdiv(static_cast<uint32_t>(slot[j]), p.slot_div);
                 const int64_t off = slot[j] - blk * p.block_size;
                 const uint8_t *base = p.src + blk * int64_t(p.block_size) * kSlotBytes;
                 c[j] = load_codes<kWide>(base + off * kDim + 8 * h);
@@ -228,6 +230,7 @@ int launch_indexer_insert(const uint16_t *k, const int64_t *slots, uint8_t *cach
     p.rows = rows;
     p.num_slots = num_blocks * int64_t(block_size);
     p.block_size = block_size;
+    p.slot_div = fastdiv_magic(static_cast<uint32_t>(block_size));
     p.err = err;
     const unsigned grid = static_cast<unsigned>(grid_for(rows, max_ctas));
     const bool wide = (reinterpret_cast<uintptr_t>(cache) & 7u) == 0 && block_size % 2 == 0;
@@ -250,6 +253,7 @@ int launch_indexer_gather(const uint8_t *cache, int64_t num_blocks, int32_t bloc
     p.rows = rows;
     p.num_slots = num_blocks * int64_t(block_size);
     p.block_size = block_size;
+    p.slot_div = fastdiv_magic(static_cast<uint32_t>(block_size));
     p.err = err;
     const unsigned grid = static_cast<unsigned>(grid_for(rows, max_ctas));
     const bool wide = (reinterpret_cast<uintptr_t>(cache) & 7u) == 0 && block_size % 2 == 0;

@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include "dsv4kv.h"
+#include "fastdiv.h"
 
 namespace dsv4 {
 
@@ -48,6 +49,7 @@ struct KParams {
     int32_t num_heads;
     float eps;
     int32_t *err;
+    uint64_t slot_div;  // fastdiv_magic(block_size): slot / block_size by one multiply
 };
 
 // CTAs of the streaming kernel for `store_mode` that fit on one SM.

@@ -174,6 +174,7 @@ int launch(int store_mode, const dsv4_plan &plan, const LaunchArgs &a, cudaStrea
     p.num_heads = a.num_heads;
     p.eps = a.eps;
     p.err = a.err;
+    p.slot_div = fastdiv_magic(static_cast<uint32_t>(a.block_size));
     if (plan.variant == DSV4_VARIANT_BULK)
         return launch_bulk(store_mode, a.kv_norm, plan.ctas, p, stream);
     const dim3 grid(unsigned(plan.ctas)), block(unsigned(plan.threads));

@@ -23,7 +23,7 @@ constexpr uint32_t kMant1p75 = 0x600000u;  // mantissa field of 1.75 (448 = 1.75
 // of the fp32 mantissa field: 2^9 / 2^23 = 2^-14 relative.  The fp32 value of
 // an element is within ~14 ulp (2^-20) of its exact value: 16 sequential fmas
 // and a 5-level tree for the sum (<= 21 ulp, halved by the root), one ulp each
-// for the add of eps, the root, the reciprocal and two products.
+// for the add of eps, the reciprocal root and two products.
 constexpr uint32_t kNearBand = 512u;
 
 
@@ -148,10 +148,11 @@ __device__ __forceinline__ void rope8_scaled(const float *u, float4 c, float4 s,
     }
 }
 
-// 1 / sqrt(sum/512 + eps), each step correctly rounded
+// 1 / sqrt(sum/512 + eps): the mean and the sum correctly rounded, then one
+// correctly rounded reciprocal square root
 __device__ __forceinline__ float inv_rms(float sum_sq, float eps)
 {
-    return __frcp_rn(__fsqrt_rn(__fadd_rn(__fmul_rn(sum_sq, 1.0f / 512.0f), eps)));
+    return __frsqrt_rn(__fadd_rn(__fmul_rn(sum_sq, 1.0f / 512.0f), eps));
 }
 
 // 2^-s as fp32 for s in [-127, 127]
@@ -355,7 +356,8 @@ __device__ __forceinline__ void kv_row(const KParams &p, int lane, int64_t t, in
                           w_smem, v);
     }
 
-    const int64_t blk = slot / p.block_size;
+    // 0 <= slot < num_slots <= 2^32 here, so the quotient is a 32-bit one
+    const int64_t blk = fastdiv(static_cast<uint32_t>(slot), p.slot_div);
     const int64_t off = slot - blk * p.block_size;
     uint8_t *base = p.cache + blk * int64_t(p.block_size) * DSV4_FP8_SLOT_BYTES;
     uint8_t *data = base + off * DSV4_FP8_DATA_BYTES;
@@ -376,14 +378,16 @@ __device__ __forceinline__ void kv_row(const KParams &p, int lane, int64_t t, in
         st_stream8(tail + 8, make_uint2(bf16x2_rn(v[12], v[13]), bf16x2_rn(v[14], v[15])));
     }
 
-    const uint32_t e0 = uint32_t(g0.s + 127), e1 = uint32_t(g1.s + 127);
-    const uint32_t b0 = __shfl_sync(kFull, e0, 0), b1 = __shfl_sync(kFull, e0, 8);
-    const uint32_t b2 = __shfl_sync(kFull, e0, 16), b3 = __shfl_sync(kFull, e0, 24);
-    const uint32_t b4 = __shfl_sync(kFull, e1, 0), b5 = __shfl_sync(kFull, e1, 8);
-    const uint32_t b6 = __shfl_sync(kFull, e1, 16);
+    // scale word: byte b is the exponent of block b, held by lane 8*(b%4) of
+    // half b/4; each of those lanes ORs its byte into place (byte 7 stays 0)
+    const bool leader = (lane & 7) == 0;
+    const uint32_t shift = 8u * uint32_t(lane >> 3);
+    const uint32_t lo = __reduce_or_sync(kFull, leader ? uint32_t(g0.s + 127) << shift : 0u);
+    const uint32_t hi =
+        __reduce_or_sync(kFull, leader && !rope_lane ? uint32_t(g1.s + 127) << shift : 0u);
     if (lane == 0)
         st_stream8(base + int64_t(p.block_size) * DSV4_FP8_DATA_BYTES + off * DSV4_FP8_SCALE_BYTES,
-                   make_uint2(b0 | (b1 << 8) | (b2 << 16) | (b3 << 24), b4 | (b5 << 8) | (b6 << 16)));
+                   make_uint2(lo, hi));
 }
 
 

@@ -254,3 +254,33 @@ def test_indexer_entries_have_no_cpu_fallback():
         pytest.skip("a GPU is present; covered by the GPU tests")
     assert k.lib().dsv4_indexer_k_quant_insert(A, A, A, 4, 64, 5, None, None) == k.ERR_CUDA
     assert k.lib().dsv4_indexer_k_gather(A, 4, 64, A, 5, A, A, None, None) == k.ERR_CUDA
+
+
+def test_caches_beyond_two_to_the_32_slots_are_rejected():
+    """num_blocks * block_size <= 2^32 for every entry that takes a cache."""
+    lib = k.lib()
+    nb_ok, nb_bad = (1 << 32) // 64, (1 << 32) // 64 + 1
+    assert lib.dsv4_dequant_gather(A, nb_bad, 64, A, 5, A, None, None) == k.ERR_SHAPE
+    assert lib.dsv4_indexer_k_quant_insert(A, A, A, nb_bad, 64, 5, None, None) == k.ERR_SHAPE
+    assert lib.dsv4_indexer_k_gather(A, nb_bad, 64, A, 5, A, A, None, None) == k.ERR_SHAPE
+    assert lib.dsv4_insert_ex(0, 0, 1, A, A, A, A, A, 4096, A, A, nb_bad, 64, 16, 8, 1e-6,
+                              None, None) == k.ERR_SHAPE
+    # exactly 2^32 slots passes the shape check (zero tokens: no launch)
+    assert lib.dsv4_insert_ex(0, 0, 1, A, A, A, A, A, 4096, A, A, nb_ok, 64, 0, 8, 1e-6,
+                              None, None) == k.OK
+    assert lib.dsv4_indexer_k_quant_insert(A, A, A, nb_ok, 64, 0, None, None) == k.OK
+
+
+@pytest.mark.parametrize("d", [2, 3, 7, 64, 100, 1000, (1 << 31) - 1, 1 << 31, (1 << 32) - 1])
+def test_fast_division_identity(d):
+    """The multiply-high division the kernels use (fastdiv.h): with
+    M = floor((2^64 - 1) / d) + 1, n // d == (M * n) >> 64 for 32-bit n
+    (Lemire, Kaser, Kurz 2019, Theorem 1), checked at the edges of n and at
+    multiples of d and their neighbours."""
+    m = (2**64 - 1) // d + 1
+    ns = {0, 1, d - 1, d, d + 1, 2**32 - 1, 2**32 - 2, 2**31, 12345678}
+    for q in (1, 2, 3, 1000, (2**32 - 1) // d):
+        ns |= {q * d - 1, q * d, q * d + 1}
+    for n in ns:
+        if 0 <= n < 2**32:
+            assert (m * n) >> 64 == n // d, (n, d)
