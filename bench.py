@@ -539,6 +539,11 @@ def run_ours(args):
     dev = torch.device("cuda", local_rank)
     lib = k.lib()
     wl = rank_workload(configs.WORKLOADS[args.workload], rank)
+    if args.tokens:
+        if not 0 < args.tokens <= wl.T:
+            raise SystemExit(f"--tokens must be in [1, {wl.T}]")
+        # the first N tokens of the workload (its position and slot rules unchanged)
+        wl = dataclasses.replace(wl, T=args.tokens)
 
     kac_before = known_answer_check() if rank == 0 else "skipped"
     copy_1g = copy_ceiling_gbs(dev, 1 << 30)
@@ -626,7 +631,7 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": profiled_traffic(wl.name.split("@")[0])
-                     if args.op == "fused" else None,
+                     if args.op == "fused" and not args.tokens else None,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "launch_ms_mean": round(mean_launch * 1e3, 4),
@@ -663,6 +668,8 @@ def main(argv=None):
                          "gather: read the FP8 cache back out; mxfp8: residual add + Gemma "
                          "RMSNorm + MXFP8 of [T, 7168] activation rows; indexer: indexer-K "
                          "quant-insert of [T, 128] rows; indexer_gather: read them back out")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="run only the first N tokens of the workload (smaller profiling cases)")
     ap.add_argument("--e2e-steps", type=int, default=6)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
