@@ -21,7 +21,7 @@ _CSRC = os.path.join(_HERE, "csrc")
 _INCLUDE = os.path.join(_ROOT, "include")
 LIB_PATH = os.path.join(_HERE, "libdsv4kv.so")
 _SOURCES = ["qnorm_rope_kv_insert.cu", "qnorm_rope_kv_insert_bulk.cu", "dequant_gather.cu",
-            "gemma_rmsnorm_mxfp8.cu", "indexer_k.cu", "api.cpp"]
+            "gemma_rmsnorm_mxfp8.cu", "indexer_k.cu", "kv_rows.cu", "api.cpp"]
 _HEADERS = [os.path.join(_INCLUDE, "dsv4kv.h")] + [
     os.path.join(_CSRC, h) for h in ("launch.h", "ops.h", "fastdiv.h", "rowmath.cuh")]
 NVCC_ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

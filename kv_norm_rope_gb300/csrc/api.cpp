@@ -63,7 +63,7 @@ int device_shape(int store_mode, int32_t *sms, int32_t *ctas)
 
 // CTAs per SM of the reader and indexer kernels, cached per device beside the
 // SM count; resident = SMs x CTAs per SM, the cap of their persistent grids.
-enum { kOccGather = 0, kOccIndexer = 1, kOccKinds = 2 };
+enum { kOccGather = 0, kOccIndexer = 1, kOccKvRows = 2, kOccKinds = 3 };
 std::atomic<int32_t> g_occ[kMaxDevices][kOccKinds];
 
 int resident_ctas(int kind, int64_t *resident)
@@ -82,8 +82,9 @@ int resident_ctas(int kind, int64_t *resident)
             g_sms[dev].store(sms, std::memory_order_relaxed);
     }
     if (per < 1) {
-        const int rc = kind == kOccGather ? dsv4::gather_ctas_per_sm(&per)
-                                          : dsv4::indexer_ctas_per_sm(&per);
+        const int rc = kind == kOccGather    ? dsv4::gather_ctas_per_sm(&per)
+                       : kind == kOccIndexer ? dsv4::indexer_ctas_per_sm(&per)
+                                             : dsv4::kv_rows_ctas_per_sm(&per);
         if (rc != DSV4_OK || per < 1)
             return DSV4_ERR_CUDA;
         if (cached)
@@ -155,6 +156,13 @@ int insert(int store_mode, int variant, int flags, void *q, const void *kv, cons
     a.eps = eps;
     a.err = device_error;
     a.kv_norm = kv_norm;
+    if (num_heads == 0 && plan.variant == DSV4_VARIANT_STREAM) {
+        // KV rows only: the half-warp-per-row kernel
+        int64_t resident = 0;
+        if (resident_ctas(kOccKvRows, &resident) != DSV4_OK)
+            return DSV4_ERR_CUDA;
+        return dsv4::launch_kv_rows(store_mode, a, resident, static_cast<cudaStream_t>(stream));
+    }
     return dsv4::launch(store_mode, plan, a, static_cast<cudaStream_t>(stream));
 }
 
@@ -194,12 +202,14 @@ int dsv4_launch_plan(int64_t num_tokens, int32_t num_heads, int32_t sm_count, in
         plan->rows_per_warp = 1;
         plan->ctas = chunks < sm_count ? (chunks > 0 ? chunks : 1) : sm_count;
     } else if (variant == DSV4_VARIANT_STREAM) {
-        const int64_t groups = (rows + dsv4::kStreamRowsPerWarp - 1) / dsv4::kStreamRowsPerWarp;
+        // with no q heads the KV-row kernel runs: same CTA size, its own rows per warp
+        const int per_warp = num_heads == 0 ? dsv4::kv_rows_per_warp() : dsv4::kStreamRowsPerWarp;
+        const int64_t groups = (rows + per_warp - 1) / per_warp;
         const int64_t need = (groups + stream_warps - 1) / stream_warps;
         const int64_t resident = int64_t(sm_count) * ctas_per_sm;
         plan->variant = DSV4_VARIANT_STREAM;
         plan->threads = dsv4::kStreamThreads;
-        plan->rows_per_warp = dsv4::kStreamRowsPerWarp;
+        plan->rows_per_warp = per_warp;
         plan->ctas = need < resident ? (need > 0 ? need : 1) : resident;
     } else {
         return DSV4_ERR_VALUE;

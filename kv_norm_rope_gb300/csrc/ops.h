@@ -1,6 +1,7 @@
 // Internal interface between the C-ABI layer (api.cpp) and the kernels of the
-// operations beside the fused step: the MXFP8 activation quantiser
-// (gemma_rmsnorm_mxfp8.cu) and the indexer-K insert and gather (indexer_k.cu).
+// operations beside the fused step: the KV-row kernel for calls with no q
+// (kv_rows.cu), the MXFP8 activation quantiser (gemma_rmsnorm_mxfp8.cu) and the
+// indexer-K insert and gather (indexer_k.cu).
 // Not installed; not part of the ABI.
 #pragma once
 
@@ -8,8 +9,14 @@
 #include <stdint.h>
 
 #include "dsv4kv.h"
+#include "launch.h"
 
 namespace dsv4 {
+
+// KV rows with no q, one row per half-warp (kv_rows.cu); the grid is capped at max_ctas.
+int kv_rows_ctas_per_sm(int *ctas_per_sm);
+int kv_rows_per_warp();
+int launch_kv_rows(int store_mode, const LaunchArgs &a, int64_t max_ctas, cudaStream_t stream);
 
 // Residual add + Gemma RMSNorm + MXFP8 rows.
 int launch_gemma_rmsnorm_mxfp8(const uint16_t *x, const uint16_t *residual, const uint16_t *gamma,
