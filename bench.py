@@ -355,6 +355,40 @@ class DeviceBatch:
                     self.err.data_ptr(), stream_handle)
 
 
+def graph_device_us(batch: DeviceBatch, lib, dev, flush, n: int = 50, reps: int = 7) -> float:
+    """Device time of one launch without the host's launch latency: a CUDA graph of
+    n (L2 flush, launch) pairs replayed and timed with events, minus a graph of the
+    n flushes alone, divided by n (median of `reps` replays)."""
+    import torch
+
+    def timed(with_launch: bool) -> float:
+        s = torch.cuda.Stream(dev)
+        g = torch.cuda.CUDAGraph()
+        fn, a = batch.call(lib, s.cuda_stream)
+        torch.cuda.synchronize(dev)
+        with torch.cuda.stream(s):
+            if with_launch:
+                fn(*a)  # warm outside the capture
+            torch.cuda.synchronize(dev)
+            with torch.cuda.graph(g, stream=s):
+                for i in range(n):
+                    flush.fill_(i & 0xFF)
+                    if with_launch:
+                        fn(*a)
+        torch.cuda.synchronize(dev)
+        ts = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            g.replay()
+            e1.record()
+            torch.cuda.synchronize(dev)
+            ts.append(e0.elapsed_time(e1) * 1e3 / n)
+        return statistics.median(ts)
+
+    return timed(True) - timed(False)
+
+
 def entry(lib, store: str):
     return (lib.dsv4_qnorm_rope_kv_quant_insert if store == "fp8"
             else lib.dsv4_qnorm_rope_kv_bf16_insert)
@@ -598,6 +632,7 @@ def run_ours(args):
                "tokens_per_s": round(total_tokens / e2e_dt, 1),
                "chunks": 16, "ms_per_step": round(e2e_dt * 1e3, 3),
                "link": "pinned host memory; H2D and D2H overlap across chunks and steps"}
+    graph_us = graph_device_us(batch, lib, dev, flush) if flush is not None else None
     kac_after = known_answer_check() if rank == 0 else "skipped"
     if rank != 0:
         return 0
@@ -636,6 +671,12 @@ def run_ours(args):
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "launch_ms_mean": round(mean_launch * 1e3, 4),
                      "launch_ms_median": round(statistics.median(per_launch) * 1e3, 4)},
+        "graph": None if graph_us is None else {
+            "us_per_launch": round(graph_us, 3),
+            "GB/s": round(batch.bytes / graph_us / 1e3, 1),
+            "how": "CUDA graph of 50 (L2 flush, launch) pairs minus a graph of the 50 flushes: "
+                   "the kernel's device time without the host launch latency that a single "
+                   "event-timed launch after a flush includes"},
         "gpu_launches": args.steps,
         "ms_per_step_note": "mean launch time (L2 flushed between launches)" if flush is not None
         else "timed region / steps",
