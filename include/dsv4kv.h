@@ -179,7 +179,9 @@ int dsv4_qnorm_rope_kv_rope_quant_insert(void *q, const void *kv, const int64_t 
  * RMSNorm over 512 with a weight, RoPE on the trailing 64 dims, paged store):
  * store_mode DSV4_STORE_FP8 (kv_cache uint8, FP8 layout above, 8-byte aligned) or
  * DSV4_STORE_BF16 (kv_cache bf16 [num_blocks, block_size, 512], 16-byte aligned).
- * Other arguments as in dsv4_qnorm_rope_kv_quant_insert.
+ * Other arguments as in dsv4_qnorm_rope_kv_quant_insert.  Batches that plan as
+ * STREAM run a kernel laid out for KV rows alone (one row per half-warp); its cache
+ * bytes are identical to those the fused entry points write for the same rows.
  */
 int dsv4_kv_norm_rope_insert(int store_mode, const void *kv, const void *kv_norm_weight,
                              const int64_t *positions, const float *cos_sin_cache,
@@ -264,7 +266,9 @@ typedef struct {
  * SMALL when the rows would not give every warp slot of the GPU at least a
  * full group of rows, else STREAM (SGLang PR #33358, "Modifications" item 3:
  * a grid-starved multi-token layout loses at small N).  BULK runs one CTA
- * per SM (at most one per 16-row chunk).  Returns a dsv4_status.
+ * per SM (at most one per 16-row chunk).  With num_heads 0, STREAM describes the
+ * KV-row kernel: one row per half-warp, rows_per_warp 2, and ctas_per_sm should
+ * then be that kernel's occupancy.  Returns a dsv4_status.
  */
 int dsv4_launch_plan(int64_t num_tokens, int32_t num_heads, int32_t sm_count,
                      int32_t ctas_per_sm, int32_t variant, dsv4_plan *plan);
