@@ -222,7 +222,7 @@ IO_OF_OP = {
     "indexer_gather": "indexer cache rows in; contiguous e4m3 [T, 128] + fp32 [T] out",
 }
 MXFP8_HIDDEN = 7168
-VARIANTS = {"auto": 0, "small": 1, "stream": 2, "bulk": 3}
+VARIANTS = {"auto": 0, "small": 1, "stream": 2, "bulk": 3, "half": 4}
 
 
 class DeviceBatch:
@@ -655,7 +655,7 @@ def run_ours(args):
                    else f"inputs larger than L2 ({batch.bytes / 1e9:.2f} GB per step)",
                    "io": IO_OF_OP[args.op],
                    "variant": (args.variant if args.variant != "auto" else
-                               {k.VARIANT_STREAM: "stream", k.VARIANT_SMALL: "small",
+                               {k.VARIANT_STREAM: "stream", k.VARIANT_SMALL: "small", k.VARIANT_HALF: "half",
                                 k.VARIANT_BULK: "bulk"}[plan.variant])
                    if args.op in ("fused", "prenorm", "kv_only") else "n/a",
                    "parallelism": f"dp{world}" if world > 1 else "single"},

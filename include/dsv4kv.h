@@ -87,8 +87,9 @@ enum {
     DSV4_VARIANT_AUTO = 0,    /* pick from the row count and the SM count (below) */
     DSV4_VARIANT_SMALL = 1,   /* one row per warp, 2-warp CTAs, one wave: small batches */
     DSV4_VARIANT_STREAM = 2,  /* persistent CTAs sized to the SMs, several rows in flight per warp */
-    DSV4_VARIANT_BULK = 3     /* one CTA per SM; 16-row chunks staged through shared memory by the
-                                 bulk-copy (TMA) engine, 12 in flight; q chunks written back in bulk */
+    DSV4_VARIANT_BULK = 3,    /* one CTA per SM; 32-row chunks staged through shared memory by the
+                                 bulk-copy (TMA) engine, 6 in flight; q chunks written back in bulk */
+    DSV4_VARIANT_HALF = 4     /* persistent CTAs sized to the SMs, one row per half-warp (q and KV) */
 };
 
 /*
@@ -264,9 +265,13 @@ typedef struct {
  * Fill *plan for T tokens, H heads on a GPU with sm_count SMs where
  * ctas_per_sm CTAs of the streaming kernel fit per SM.  variant AUTO picks
  * SMALL when the rows would not give every warp slot of the GPU at least a
- * full group of rows, else STREAM (SGLang PR #33358, "Modifications" item 3:
- * a grid-starved multi-token layout loses at small N).  BULK runs one CTA
- * per SM (at most one per 16-row chunk).  With num_heads 0, STREAM describes the
+ * full group of rows (SGLang PR #33358, "Modifications" item 3: a
+ * grid-starved multi-token layout loses at small N); with q heads, HALF when
+ * they would give it fewer than two (decode-sized batches, where HALF measured
+ * faster); else STREAM.  BULK runs one CTA
+ * per SM (at most one per 32-row chunk).  HALF: ceil(T/2) KV row pairs and
+ * groups of rows_per_warp q rows over persistent CTAs (ctas_per_sm then being
+ * the HALF kernel's occupancy).  With num_heads 0, STREAM describes the
  * KV-row kernel: one row per half-warp, rows_per_warp 2, and ctas_per_sm should
  * then be that kernel's occupancy.  Returns a dsv4_status.
  */

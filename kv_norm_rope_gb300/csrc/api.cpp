@@ -63,7 +63,7 @@ int device_shape(int store_mode, int32_t *sms, int32_t *ctas)
 
 // CTAs per SM of the reader and indexer kernels, cached per device beside the
 // SM count; resident = SMs x CTAs per SM, the cap of their persistent grids.
-enum { kOccGather = 0, kOccIndexer = 1, kOccKvRows = 2, kOccKinds = 3 };
+enum { kOccGather = 0, kOccIndexer = 1, kOccKvRows = 2, kOccHalf = 3, kOccKinds = 4 };
 std::atomic<int32_t> g_occ[kMaxDevices][kOccKinds];
 
 int resident_ctas(int kind, int64_t *resident)
@@ -84,7 +84,8 @@ int resident_ctas(int kind, int64_t *resident)
     if (per < 1) {
         const int rc = kind == kOccGather    ? dsv4::gather_ctas_per_sm(&per)
                        : kind == kOccIndexer ? dsv4::indexer_ctas_per_sm(&per)
-                                             : dsv4::kv_rows_ctas_per_sm(&per);
+                       : kind == kOccKvRows  ? dsv4::kv_rows_ctas_per_sm(&per)
+                                             : dsv4::half_ctas_per_sm(&per);
         if (rc != DSV4_OK || per < 1)
             return DSV4_ERR_CUDA;
         if (cached)
@@ -107,7 +108,8 @@ int insert(int store_mode, int variant, int flags, void *q, const void *kv, cons
     if (store_mode != DSV4_STORE_FP8 && store_mode != DSV4_STORE_BF16)
         return DSV4_ERR_VALUE;
     if (variant != DSV4_VARIANT_AUTO && variant != DSV4_VARIANT_SMALL &&
-        variant != DSV4_VARIANT_STREAM && variant != DSV4_VARIANT_BULK)
+        variant != DSV4_VARIANT_STREAM && variant != DSV4_VARIANT_BULK &&
+        variant != DSV4_VARIANT_HALF)
         return DSV4_ERR_VALUE;
     const int32_t min_heads = (flags & kNoQ) ? 0 : 1;
     if (num_tokens < 0 || num_heads < min_heads || num_blocks < 1 || block_size < 1 ||
@@ -135,10 +137,26 @@ int insert(int store_mode, int variant, int flags, void *q, const void *kv, cons
     int st = device_shape(store_mode, &sms, &ctas);
     if (st != DSV4_OK)
         return st;
+    if (variant == DSV4_VARIANT_HALF) {
+        int64_t resident = 0;
+        if (resident_ctas(kOccHalf, &resident) != DSV4_OK)
+            return DSV4_ERR_CUDA;
+        ctas = static_cast<int32_t>(resident / sms);
+    }
     dsv4_plan plan;
     st = dsv4_launch_plan(num_tokens, num_heads, sms, ctas, variant, &plan);
     if (st != DSV4_OK)
         return st;
+    if (variant == DSV4_VARIANT_AUTO && plan.variant == DSV4_VARIANT_HALF) {
+        // size the grid with the half-warp kernel's own occupancy
+        int64_t resident = 0;
+        if (resident_ctas(kOccHalf, &resident) != DSV4_OK)
+            return DSV4_ERR_CUDA;
+        st = dsv4_launch_plan(num_tokens, num_heads, sms, static_cast<int32_t>(resident / sms),
+                              DSV4_VARIANT_HALF, &plan);
+        if (st != DSV4_OK)
+            return st;
+    }
 
     dsv4::LaunchArgs a;
     a.q = static_cast<uint16_t *>(q);
@@ -156,6 +174,8 @@ int insert(int store_mode, int variant, int flags, void *q, const void *kv, cons
     a.eps = eps;
     a.err = device_error;
     a.kv_norm = kv_norm;
+    if (plan.variant == DSV4_VARIANT_HALF)
+        return dsv4::launch_half(store_mode, a, plan.ctas, static_cast<cudaStream_t>(stream));
     if (num_heads == 0 && plan.variant == DSV4_VARIANT_STREAM) {
         // KV rows only: the half-warp-per-row kernel
         int64_t resident = 0;
@@ -182,9 +202,15 @@ int dsv4_launch_plan(int64_t num_tokens, int32_t num_heads, int32_t sm_count, in
     const int64_t rows = num_tokens * (int64_t(num_heads) + 1);
     const int stream_warps = dsv4::kStreamThreads / 32;
     const int64_t warp_slots = int64_t(sm_count) * ctas_per_sm * stream_warps;
-    if (variant == DSV4_VARIANT_AUTO)
-        variant = rows < warp_slots * dsv4::kStreamRowsPerWarp ? DSV4_VARIANT_SMALL
-                                                               : DSV4_VARIANT_STREAM;
+    if (variant == DSV4_VARIANT_AUTO) {
+        // fewer rows than one group per warp slot: one row per warp; with q heads,
+        // fewer than two rounds of groups: the half-warp kernel (measured faster
+        // there, slower on long streams); otherwise the whole-warp stream
+        const int64_t round = warp_slots * dsv4::kStreamRowsPerWarp;
+        variant = rows < round                            ? DSV4_VARIANT_SMALL
+                  : num_heads > 0 && rows < 2 * round     ? DSV4_VARIANT_HALF
+                                                          : DSV4_VARIANT_STREAM;
+    }
     plan->rows = rows;
     if (variant == DSV4_VARIANT_SMALL) {
         const int warps = dsv4::kSmallThreads / 32;
@@ -210,6 +236,15 @@ int dsv4_launch_plan(int64_t num_tokens, int32_t num_heads, int32_t sm_count, in
         plan->variant = DSV4_VARIANT_STREAM;
         plan->threads = dsv4::kStreamThreads;
         plan->rows_per_warp = per_warp;
+        plan->ctas = need < resident ? (need > 0 ? need : 1) : resident;
+    } else if (variant == DSV4_VARIANT_HALF) {
+        const int64_t per_warp = dsv4::half_q_rows_per_warp();
+        const int64_t items = (num_tokens + 1) / 2 + (num_tokens * num_heads + per_warp - 1) / per_warp;
+        const int64_t need = (items + stream_warps - 1) / stream_warps;
+        const int64_t resident = int64_t(sm_count) * ctas_per_sm;
+        plan->variant = DSV4_VARIANT_HALF;
+        plan->threads = dsv4::kStreamThreads;
+        plan->rows_per_warp = static_cast<int32_t>(per_warp);
         plan->ctas = need < resident ? (need > 0 ? need : 1) : resident;
     } else {
         return DSV4_ERR_VALUE;

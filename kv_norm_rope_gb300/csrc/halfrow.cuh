@@ -1,0 +1,329 @@
+// Row arithmetic of the half-warp layout, shared by the kernels that give
+// each 512-wide row half a warp (kv_rows.cu, qnorm_rope_kv_insert_half.cu).
+//
+// Lane h = lane % 16 of half r = lane / 16 holds dims [128v + 8h, 128v + 8h + 8)
+// of its row for v = 0..3: four 16-byte vectors, so one warp-wide load covers
+// 256 contiguous bytes of each of two rows.  Vector v of lane h lies in
+// quantisation block 2v + h/8; dims 448..511 (vector 3, h >= 8) are the rope
+// dims, the same 4 pairs per lane as lane 24 + (h - 8) of a whole-warp row.
+//
+// Every value is bit-identical to the whole-warp helpers in rowmath.cuh:
+// lane h's partial sums over vectors (0, 2) and (1, 3) are exactly the
+// partials of whole-warp lanes h and h + 16, their sum is the first level of
+// the whole-warp butterfly (xor 16) and the remaining levels (xor 8, 4, 2, 1)
+// are the same; the elementwise operations, the rotation, the block maxima
+// and the exact fp64 decision near a scale boundary are the same operations
+// on the same values.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "rowmath.cuh"
+
+namespace dsv4 {
+namespace {
+
+// The weight in shared memory as fp32 (exact), laid out so that the 16 lanes
+// of a half-warp read 16 consecutive float4: lane h's 8 weights of vector j
+// are float4s (2j) * 16 + h and (2j + 1) * 16 + h.
+__device__ __forceinline__ int w_index(int j, int part, int h)
+{
+    return (2 * j + part) * 16 + h;
+}
+
+// The first UE8M0 guess of the fused kernel's ue8m0_guess, with the same s and
+// near flag: amax = M * 2^E (M in [1, 2)), s = E - 8 + (M > 1.75) clamped to
+// [-127, 127] (amax below 2^-126 lands on -127); near when the mantissa is
+// within kNearBand of 1.75's and the two candidates do not clamp to the same
+// value (biased exponent above 7).
+__device__ __forceinline__ ScaleGuess guess_lean(float amax)
+{
+    const uint32_t bits = __float_as_uint(amax);
+    const int ef = int(bits >> 23);
+    const uint32_t m = bits & 0x7fffffu;
+    ScaleGuess g;
+    g.e = ef - 127;
+    g.s = min(max(ef - 135 + (m > kMant1p75 ? 1 : 0), -127), 127);
+    g.near = (m - (kMant1p75 - kNearBand)) <= 2u * kNearBand && ef > 7;
+    return g;
+}
+
+__device__ __forceinline__ float half_sum(float v)
+{
+#pragma unroll
+    for (int m = 8; m >= 1; m >>= 1)
+        v = __fadd_rn(v, __shfl_xor_sync(kFull, v, m));
+    return v;
+}
+
+__device__ __forceinline__ double half_sum(double v)
+{
+#pragma unroll
+    for (int m = 8; m >= 1; m >>= 1)
+        v = __dadd_rn(v, __shfl_xor_sync(kFull, v, m));
+    return v;
+}
+
+// cos and sin of the 4 pairs held by a rope lane (h >= 8) at row pos; zeros
+// elsewhere and for rows that are not written
+__device__ __forceinline__ void half_load_cs(const KParams &p, int h, bool active, int64_t pos,
+                                             float4 &cv, float4 &sv)
+{
+    cv = make_float4(0.f, 0.f, 0.f, 0.f);
+    sv = cv;
+    if (active && h >= 8) {
+        const float *cs = p.cs + pos * DSV4_ROPE_DIM + 4 * (h - 8);
+        cv = __ldg(reinterpret_cast<const float4 *>(cs));
+        sv = __ldg(reinterpret_cast<const float4 *>(cs + DSV4_ROPE_DIM / 2));
+    }
+}
+
+// v = x * r * w (or x) for the lane's 32 dims of its row, rope dims rotated
+template <bool kKvNorm>
+__device__ __forceinline__ void half_row_values(const KParams &p, int h, const uint4 *x, float4 cv,
+                                                float4 sv, const float4 *w_smem, float (*v)[8])
+{
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        widen8(x[j], v[j]);
+    const bool rope_lane = h >= 8;
+    if (!kKvNorm) {
+        if (rope_lane) {
+            float u[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                u[k] = v[3][k];
+            rope8_scaled(u, cv, sv, 1.0f, v[3]);
+        }
+        return;
+    }
+    // the whole-warp order: lane h's vectors (0, 2), lane h + 16's (1, 3)
+    float sa = 0.0f, sb = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        sa = __fmaf_rn(v[0][k], v[0][k], sa);
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        sa = __fmaf_rn(v[2][k], v[2][k], sa);
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        sb = __fmaf_rn(v[1][k], v[1][k], sb);
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        sb = __fmaf_rn(v[3][k], v[3][k], sb);
+    const float r = inv_rms(half_sum(__fadd_rn(sa, sb)), p.eps);
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+        const float4 wa = w_smem[w_index(j, 0, h)], wb = w_smem[w_index(j, 1, h)];
+        const float w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            v[j][k] = __fmul_rn(__fmul_rn(v[j][k], r), w[k]);
+    }
+    const float4 wa = w_smem[w_index(3, 0, h)], wb = w_smem[w_index(3, 1, h)];
+    const float w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+    if (!rope_lane) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            v[3][k] = __fmul_rn(__fmul_rn(v[3][k], r), w[k]);
+    } else {
+        // x*w is exact in fp32; rotate, then scale
+        float u[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            u[k] = __fmul_rn(v[3][k], w[k]);
+        rope8_scaled(u, cv, sv, r, v[3]);
+    }
+}
+
+// The exact decision for blocks too close to a boundary in fp32 (rare): the
+// row's norm in fp64 in the whole-warp order, then each element of a near
+// block as (x * r) * w in fp64 against 1.75 * 2^e.  Returns bit j set when
+// the lane's block of vector j exceeds its boundary (OR-ed over the block).
+__device__ __noinline__ int half_exact_bumps(const KParams &p, int h, int64_t t, const int *e,
+                                             const bool *near)
+{
+    const uint16_t *row = p.kv + t * kHead;
+    double sa = 0.0, sb = 0.0;
+#pragma unroll 1
+    for (int k = 0; k < 16; ++k) {
+        const int da = (k < 8 ? 0 : 248) + 8 * h + k;   // vectors 0 then 2
+        const int db = (k < 8 ? 128 : 376) + 8 * h + k; // vectors 1 then 3
+        const double xa = double(__uint_as_float(uint32_t(__ldg(row + da)) << 16));
+        const double xb = double(__uint_as_float(uint32_t(__ldg(row + db)) << 16));
+        sa = __fma_rn(xa, xa, sa);
+        sb = __fma_rn(xb, xb, sb);
+    }
+    const double ss = half_sum(__dadd_rn(sa, sb));
+    const double r = 1.0 / sqrt(ss / 512.0 + double(p.eps));
+    int bits = 0;
+#pragma unroll 1
+    for (int j = 0; j < 4; ++j) {
+        bool up = false;
+        if (near[j]) {
+            const double bound = __hiloint2double(int(uint32_t(1023 + e[j]) << 20) | 0x000C0000, 0);
+#pragma unroll 1
+            for (int k = 0; k < 8; ++k) {
+                const int d = 128 * j + 8 * h + k;
+                const double x = double(__uint_as_float(uint32_t(__ldg(row + d)) << 16));
+                const double w = double(__uint_as_float(uint32_t(__ldg(p.w + d)) << 16));
+                if (fabs(__dmul_rn(__dmul_rn(x, r), w)) > bound)
+                    up = true;
+            }
+        }
+        if (group8_any(up))
+            bits |= 1 << j;
+    }
+    return bits;
+}
+
+// The FP8 store of a half-warp row: block scales, E4M3 payload, bf16 rope
+// tail and the scale word.
+template <bool kKvNorm>
+__device__ __forceinline__ void half_row_fp8(const KParams &p, int h, bool active, int64_t t,
+                                             int64_t slot, float (*v)[8])
+{
+    const bool rope_lane = h >= 8;
+
+    ScaleGuess g[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        float am = 0.0f;
+        if (j < 3 || !rope_lane) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                am = fmaxf(am, fabsf(v[j][k]));
+        }
+        g[j] = guess_lean(group8_max(am));  // rope lanes: amax 0, never near
+        g[j].near = g[j].near && active;
+    }
+    if (kKvNorm && __any_sync(kFull, g[0].near || g[1].near || g[2].near || g[3].near)) {
+        const int e[4] = {g[0].e, g[1].e, g[2].e, g[3].e};
+        const bool nr[4] = {g[0].near, g[1].near, g[2].near, g[3].near};
+        const int bumps = half_exact_bumps(p, h, active ? t : 0, e, nr);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (g[j].near)
+                g[j].s = clamp_s(g[j].e - 8 + ((bumps >> j) & 1));
+    }
+
+    // scale word of each half: lane h = 0 leads blocks 0, 2, 4, 6 and lane
+    // h = 8 blocks 1, 3, 5; bytes land at 8 * block, byte 7 stays 0
+    const uint32_t b0 = uint32_t(g[0].s + 127), b1 = uint32_t(g[1].s + 127);
+    const uint32_t b2 = uint32_t(g[2].s + 127), b3 = uint32_t(g[3].s + 127);
+    const uint32_t lo_part = h == 0 ? (b0 | (b1 << 16)) : (b0 << 8) | (b1 << 24);
+    const uint32_t hi_part = h == 0 ? (b2 | (b3 << 16)) : (b2 << 8);
+    const uint32_t lo = lo_part | __shfl_xor_sync(kFull, lo_part, 8);
+    const uint32_t hi = hi_part | __shfl_xor_sync(kFull, hi_part, 8);
+
+    if (!active)
+        return;
+    const int64_t blk = fastdiv(static_cast<uint32_t>(slot), p.slot_div);
+    const int64_t off = slot - blk * p.block_size;
+    uint8_t *base = p.cache + blk * int64_t(p.block_size) * DSV4_FP8_SLOT_BYTES;
+    uint8_t *data = base + off * DSV4_FP8_DATA_BYTES;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        if (j == 3 && rope_lane)
+            break;
+        const float kj = pow2_neg(g[j].s);
+        st_stream8(data + 128 * j + 8 * h,
+                   make_uint2(e4m3x4_rn(v[j][0] * kj, v[j][1] * kj, v[j][2] * kj, v[j][3] * kj),
+                              e4m3x4_rn(v[j][4] * kj, v[j][5] * kj, v[j][6] * kj, v[j][7] * kj)));
+    }
+    if (rope_lane) {
+        // rope dims stay bf16; 8-byte stores keep any block_size legal
+        uint8_t *tail = data + DSV4_NOPE_DIM + 16 * (h - 8);
+        st_stream8(tail, make_uint2(bf16x2_rn(v[3][0], v[3][1]), bf16x2_rn(v[3][2], v[3][3])));
+        st_stream8(tail + 8, make_uint2(bf16x2_rn(v[3][4], v[3][5]), bf16x2_rn(v[3][6], v[3][7])));
+    }
+    if (h == 0)
+        st_stream8(base + int64_t(p.block_size) * DSV4_FP8_DATA_BYTES + off * DSV4_FP8_SCALE_BYTES,
+                   make_uint2(lo, hi));
+}
+
+// One row per half-warp.  active: this half's row is written (valid token,
+// position and slot); inactive halves still take part in every shuffle.
+template <int kStore, bool kKvNorm>
+__device__ __forceinline__ void half_row(const KParams &p, int h, bool active, int64_t t,
+                                         int64_t pos, int64_t slot, const uint4 *x,
+                                         const float4 *w_smem)
+{
+    float4 cv, sv;
+    half_load_cs(p, h, active, pos, cv, sv);
+    float v[4][8];
+    half_row_values<kKvNorm>(p, h, x, cv, sv, w_smem, v);
+
+    if constexpr (kStore == DSV4_STORE_BF16) {
+        if (active) {
+            uint16_t *row = reinterpret_cast<uint16_t *>(p.cache) + slot * kHead;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                st_stream16(row + 128 * j + 8 * h, bf16x8_rn(v[j]));
+        }
+    } else {
+        half_row_fp8<kKvNorm>(p, h, active, t, slot, v);
+    }
+}
+
+// thread i < 64 widens the 8 weights of dims [8i, 8i + 8): j = i / 16, h = i % 16
+__device__ __forceinline__ void stage_weight(const uint16_t *w, int i, float4 *w_smem)
+{
+    float f[8];
+    widen8(__ldg(reinterpret_cast<const uint4 *>(w) + i), f);
+    const int j = i >> 4, h = i & 15;
+    w_smem[w_index(j, 0, h)] = make_float4(f[0], f[1], f[2], f[3]);
+    w_smem[w_index(j, 1, h)] = make_float4(f[4], f[5], f[6], f[7]);
+}
+
+
+// One q head row: y = x * r with the rope dims rotated first (compensated)
+// and then scaled, the operations of q_row on the same values; returns the
+// lane's four output vectors (bf16, round to nearest).
+__device__ __forceinline__ void q_half_row(const KParams &p, int h, const uint4 *x, float4 cv,
+                                           float4 sv, uint4 *out)
+{
+    float y[4][8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        widen8(x[j], y[j]);
+    // the whole-warp order: lane h's vectors (0, 2), lane h + 16's (1, 3)
+    float sa = 0.0f, sb = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        sa = __fmaf_rn(y[0][k], y[0][k], sa);
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        sa = __fmaf_rn(y[2][k], y[2][k], sa);
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        sb = __fmaf_rn(y[1][k], y[1][k], sb);
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        sb = __fmaf_rn(y[3][k], y[3][k], sb);
+    const float r = inv_rms(half_sum(__fadd_rn(sa, sb)), p.eps);
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            y[j][k] = __fmul_rn(y[j][k], r);
+    }
+    if (h < 8) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            y[3][k] = __fmul_rn(y[3][k], r);
+    } else {
+        float u[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            u[k] = y[3][k];
+        rope8_scaled(u, cv, sv, r, y[3]);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        out[j] = bf16x8_rn(y[j]);
+}
+
+}  // namespace
+}  // namespace dsv4

@@ -1,5 +1,6 @@
 // Internal interface between the C-ABI layer (api.cpp) and the kernels of the
-// operations beside the fused step: the KV-row kernel for calls with no q
+// operations beside the whole-warp fused kernels: the half-warp fused kernel
+// (qnorm_rope_kv_insert_half.cu), the KV-row kernel for calls with no q
 // (kv_rows.cu), the MXFP8 activation quantiser (gemma_rmsnorm_mxfp8.cu) and the
 // indexer-K insert and gather (indexer_k.cu).
 // Not installed; not part of the ABI.
@@ -17,6 +18,11 @@ namespace dsv4 {
 int kv_rows_ctas_per_sm(int *ctas_per_sm);
 int kv_rows_per_warp();
 int launch_kv_rows(int store_mode, const LaunchArgs &a, int64_t max_ctas, cudaStream_t stream);
+
+// The fused step with one row per half-warp (qnorm_rope_kv_insert_half.cu).
+int half_ctas_per_sm(int *ctas_per_sm);
+int half_q_rows_per_warp();
+int launch_half(int store_mode, const LaunchArgs &a, int64_t ctas, cudaStream_t stream);
 
 // Residual add + Gemma RMSNorm + MXFP8 rows.
 int launch_gemma_rmsnorm_mxfp8(const uint16_t *x, const uint16_t *residual, const uint16_t *gamma,

@@ -1,0 +1,167 @@
+// The fused step with one row per half-warp (DSV4_VARIANT_HALF): q heads and
+// KV rows both in the half-warp layout of halfrow.cuh.
+//
+// The whole-warp streaming kernel is DRAM-bound on large batches but spends
+// ~195 warp instructions per q row, a good part of it per-row overhead: the
+// 32-lane butterfly, the reciprocal root, both sides of the rope branch,
+// metadata and address arithmetic.  On small batches (decode) those
+// instructions, issued by every warp at the same moment after its loads land,
+// are what the launch waits on.  With half a warp per row each of them serves
+// two rows.  The values are bit-identical to the other variants (the sums keep
+// the whole-warp order; the same operations on the same values).
+//
+// Work items, handed out round-robin over all warps of the grid:
+//   items [0, ceil(T/2))          : KV rows 2i and 2i + 1 (one per half)
+//   then groups of 2*kQPairs q rows in memory order; half r of the warp takes
+//   rows r0 + 2j + r, j < kQPairs, and loads all of them before computing any.
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "halfrow.cuh"
+#include "ops.h"
+
+namespace dsv4 {
+namespace {
+
+constexpr int kHalfThreads = 256;
+constexpr int kQPairs = 2;  // q row pairs per warp item (4 rows)
+
+template <int kStore, bool kKvNorm>
+__global__ void __launch_bounds__(kHalfThreads, 3) qnorm_rope_kv_insert_half_kernel(const KParams p)
+{
+    __shared__ float4 w_smem[128];
+    if (kKvNorm) {
+        for (int i = threadIdx.x; i < 64; i += kHalfThreads)
+            stage_weight(p.w, i, w_smem);
+        __syncthreads();
+    }
+    const int lane = threadIdx.x & 31, h = lane & 15, half = lane >> 4;
+    const int64_t H = p.num_heads;
+    const int64_t T = p.num_tokens;
+    const int64_t q_rows = T * H;
+    const int64_t kv_items = (T + 1) / 2;
+    const int64_t items = kv_items + (q_rows + 2 * kQPairs - 1) / (2 * kQPairs);
+    const int64_t stride = int64_t(gridDim.x) * (kHalfThreads / 32);
+
+    for (int64_t it = int64_t(blockIdx.x) * (kHalfThreads / 32) + (threadIdx.x >> 5); it < items;
+         it += stride) {
+        if (it < kv_items) {
+            const int64_t t = 2 * it + half;
+            const int64_t pos = t < T ? __ldg(p.pos + t) : 0;
+            const int64_t slot = t < T ? __ldg(p.slot + t) : -1;
+            uint4 x[4];
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+                x[v] = t < T ? ld_stream16(p.kv + t * kHead + 128 * v + 8 * h)
+                             : make_uint4(0u, 0u, 0u, 0u);
+            const bool pos_ok = pos >= 0 && pos < p.max_pos;
+            if (t < T && h == 0) {
+                if (!pos_ok)
+                    flag_error(p.err, DSV4_DEVERR_POS_RANGE);
+                else if (slot >= p.num_slots)
+                    flag_error(p.err, DSV4_DEVERR_SLOT_RANGE);
+            }
+            const bool active = t < T && pos_ok && slot >= 0 && slot < p.num_slots;
+            if (__any_sync(kFull, active))
+                half_row<kStore, kKvNorm>(p, h, active, t, pos, slot, x, w_smem);
+            continue;
+        }
+        const int64_t r0 = (it - kv_items) * 2 * kQPairs;
+        // token of this half's rows r0 + 2j + half: r0 = t0 * H + head0, and a
+        // row d past r0 is d heads further on
+        const int64_t t0 = r0 / H, head0 = r0 - t0 * H;
+        int64_t pos[kQPairs];
+        bool live[kQPairs];
+#pragma unroll
+        for (int j = 0; j < kQPairs; ++j) {
+            int64_t hd = head0 + 2 * j + half, tok = t0;
+            while (hd >= H) {  // at most 2 * kQPairs steps
+                hd -= H;
+                ++tok;
+            }
+            live[j] = r0 + 2 * j + half < q_rows;
+            pos[j] = live[j] ? __ldg(p.pos + tok) : 0;
+        }
+        // all row loads back to back: no dependency between them
+        uint4 x[kQPairs][4];
+#pragma unroll
+        for (int j = 0; j < kQPairs; ++j) {
+            const uint16_t *src = p.q + (r0 + 2 * j + half) * kHead + 8 * h;
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+                x[j][v] = live[j] ? ld_stream16(src + 128 * v) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int j = 0; j < kQPairs; ++j) {
+            // rows past the end or with a position outside the table are not
+            // written (the KV row of the token flags the position)
+            const bool active = live[j] && pos[j] >= 0 && pos[j] < p.max_pos;
+            if (!__any_sync(kFull, active))
+                continue;
+            float4 cv, sv;
+            half_load_cs(p, h, active, pos[j], cv, sv);
+            uint4 out[4];
+            q_half_row(p, h, x[j], cv, sv, out);
+            if (active) {
+                uint16_t *dst = p.q + (r0 + 2 * j + half) * kHead + 8 * h;
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                    st_stream16(dst + 128 * v, out[v]);
+            }
+        }
+    }
+}
+
+template <int kStore>
+void launch_store(bool kv_norm, unsigned grid, cudaStream_t stream, const KParams &p)
+{
+    if (kv_norm)
+        qnorm_rope_kv_insert_half_kernel<kStore, true><<<grid, kHalfThreads, 0, stream>>>(p);
+    else
+        qnorm_rope_kv_insert_half_kernel<kStore, false><<<grid, kHalfThreads, 0, stream>>>(p);
+}
+
+}  // namespace
+
+int half_ctas_per_sm(int *ctas_per_sm)
+{
+    // the normalising FP8 kernel is the largest of the four
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+               ctas_per_sm, qnorm_rope_kv_insert_half_kernel<DSV4_STORE_FP8, true>, kHalfThreads,
+               0) == cudaSuccess
+               ? DSV4_OK
+               : DSV4_ERR_CUDA;
+}
+
+int half_q_rows_per_warp()
+{
+    return 2 * kQPairs;
+}
+
+int launch_half(int store_mode, const LaunchArgs &a, int64_t ctas, cudaStream_t stream)
+{
+    KParams p;
+    p.q = a.q;
+    p.kv = a.kv;
+    p.w = a.w;
+    p.pos = a.pos;
+    p.cs = a.cs;
+    p.max_pos = a.max_pos;
+    p.slot = a.slot;
+    p.cache = a.cache;
+    p.num_slots = a.num_slots;
+    p.num_tokens = a.num_tokens;
+    p.block_size = a.block_size;
+    p.num_heads = a.num_heads;
+    p.eps = a.eps;
+    p.err = a.err;
+    p.slot_div = fastdiv_magic(static_cast<uint32_t>(a.block_size));
+    if (store_mode == DSV4_STORE_BF16)
+        launch_store<DSV4_STORE_BF16>(a.kv_norm, static_cast<unsigned>(ctas), stream, p);
+    else
+        launch_store<DSV4_STORE_FP8>(a.kv_norm, static_cast<unsigned>(ctas), stream, p);
+    return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
+}
+
+}  // namespace dsv4

@@ -107,10 +107,15 @@ def test_launch_plan_small_and_stream():
     # 131072 x 129 rows: persistent grid, 4 CTAs on each of 152 SMs
     p = k.launch_plan(131072, 128, 152, 4)
     assert (p.variant, p.threads, p.ctas, p.rows) == (k.VARIANT_STREAM, 256, 608, 131072 * 129)
-    # the crossover: rows below warp slots x rows per warp go SMALL
+    # the crossovers: rows below one round of groups (warp slots x rows per warp) go
+    # SMALL; with q heads, below two rounds HALF; beyond, STREAM
     slots = 152 * 4 * 8 * p.rows_per_warp
     assert k.launch_plan(slots // 65 - 1, 64, 152, 4).variant == k.VARIANT_SMALL
-    assert k.launch_plan(slots // 65 + 1, 64, 152, 4).variant == k.VARIANT_STREAM
+    assert k.launch_plan(slots // 65 + 1, 64, 152, 4).variant == k.VARIANT_HALF
+    assert k.launch_plan(2 * slots // 65 - 1, 64, 152, 4).variant == k.VARIANT_HALF
+    assert k.launch_plan(2 * slots // 65 + 1, 64, 152, 4).variant == k.VARIANT_STREAM
+    # KV rows only: never HALF (they have their own kernel behind STREAM)
+    assert k.launch_plan(slots + 1, 0, 152, 4).variant == k.VARIANT_STREAM
     # forced variants
     assert k.launch_plan(131072, 128, 152, 4, k.VARIANT_SMALL).ctas == 131072 * 129 // 2
     p = k.launch_plan(3, 1, 152, 4, k.VARIANT_STREAM)
@@ -294,3 +299,12 @@ def test_launch_plan_for_kv_rows_only_stream():
     assert plan.ctas == 7  # 50 row pairs, 8 warps per CTA
     plan = k.launch_plan(100000, 8, 152, 3, k.VARIANT_STREAM)
     assert plan.rows_per_warp == 3
+
+
+def test_launch_plan_half():
+    """HALF: ceil(T/2) KV row pairs plus groups of 4 q rows, 8 warps per CTA."""
+    plan = k.launch_plan(256, 64, 152, 3, k.VARIANT_HALF)
+    items = 128 + 256 * 64 // 4
+    assert plan.variant == k.VARIANT_HALF and plan.rows_per_warp == 4 and plan.threads == 256
+    assert plan.ctas == min(-(-items // 8), 152 * 3)
+    assert k.launch_plan(3, 1, 152, 3, k.VARIANT_HALF).ctas == 1

@@ -23,7 +23,7 @@ if not torch.cuda.is_available():  # pragma: no cover - CPU runs deselect the gp
 
 import kv_norm_rope_gb300 as k  # noqa: E402
 
-VARIANTS = [k.VARIANT_AUTO, k.VARIANT_SMALL, k.VARIANT_STREAM, k.VARIANT_BULK]
+VARIANTS = [k.VARIANT_AUTO, k.VARIANT_SMALL, k.VARIANT_STREAM, k.VARIANT_BULK, k.VARIANT_HALF]
 # q rows beyond this many elements are compared on a token sample (the KV side,
 # i.e. the whole cache image, is always compared in full)
 FULL_Q_ELEMS = 1 << 27
