@@ -86,8 +86,8 @@ def barrier(world: int):
 
 # ------------------------------------------------------------------ measurement helpers
 
-KERNEL_SOURCES = ("kv_norm_rope_gb300/csrc/qnorm_rope_kv_insert.cu", "kv_norm_rope_gb300/csrc/rowmath.cuh",
-                  "kv_norm_rope_gb300/csrc/launch.h")
+KERNEL_SOURCES = tuple("kv_norm_rope_gb300/csrc/" + f for f in (
+    "qnorm_rope_kv_insert.cu", "rowmath.cuh", "convert.cuh", "fastdiv.h", "launch.h"))
 
 
 def kernel_fingerprint() -> str:

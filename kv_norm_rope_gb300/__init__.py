@@ -24,7 +24,8 @@ _SOURCES = ["qnorm_rope_kv_insert.cu", "qnorm_rope_kv_insert_bulk.cu", "dequant_
             "gemma_rmsnorm_mxfp8.cu", "indexer_k.cu", "kv_rows.cu", "qnorm_rope_kv_insert_half.cu",
             "api.cpp"]
 _HEADERS = [os.path.join(_INCLUDE, "dsv4kv.h")] + [
-    os.path.join(_CSRC, h) for h in ("launch.h", "ops.h", "fastdiv.h", "rowmath.cuh", "halfrow.cuh")]
+    os.path.join(_CSRC, h)
+    for h in ("launch.h", "ops.h", "fastdiv.h", "convert.cuh", "rowmath.cuh", "halfrow.cuh")]
 NVCC_ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 # status codes and constants (mirrors include/dsv4kv.h)

@@ -17,6 +17,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "convert.cuh"
 #include "fastdiv.h"
 #include "launch.h"
 
@@ -36,20 +37,6 @@ struct GParams {
     int32_t *err;
 };
 
-// two E4M3 codes (low byte first) -> two fp32, exact
-__device__ __forceinline__ float2 e4m3x2_to_f32(uint32_t two_codes)
-{
-    uint32_t h2;
-    const unsigned short c = static_cast<unsigned short>(two_codes);
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c));
-    float2 f;
-    asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
-        "cvt.f32.f16 %0, lo;\n\tcvt.f32.f16 %1, hi;\n\t}"
-        : "=f"(f.x), "=f"(f.y)
-        : "r"(h2));
-    return f;
-}
-
 // p * 2^(e - 127), exact in fp32 for every E4M3 value p and e in [0, 254]
 __device__ __forceinline__ float scaled(float p, uint32_t e)
 {
@@ -58,13 +45,6 @@ __device__ __forceinline__ float scaled(float p, uint32_t e)
     if (e == 0u)  // 2^-127 in two exact steps (|p| >= 2^-9, so no bit falls below 2^-149)
         return __fmul_rn(__fmul_rn(p, 0x1p-64f), 0x1p-63f);
     return __fmul_rn(__fmul_rn(p, 0x1p64f), 0x1p64f);  // 2^128: beyond bf16, becomes inf
-}
-
-__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi)
-{
-    uint32_t r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-    return r;
 }
 
 // 8 payload bytes (one 64-bit word) with scale byte e -> 8 bf16 (one 16-byte vector)

@@ -19,6 +19,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "convert.cuh"
 #include "ops.h"
 
 namespace dsv4 {
@@ -39,40 +40,9 @@ struct MParams {
     float eps;
 };
 
-__device__ __forceinline__ void widen8(uint4 u, float *f)
-{
-    f[0] = __uint_as_float(u.x << 16);
-    f[1] = __uint_as_float(u.x & 0xffff0000u);
-    f[2] = __uint_as_float(u.y << 16);
-    f[3] = __uint_as_float(u.y & 0xffff0000u);
-    f[4] = __uint_as_float(u.z << 16);
-    f[5] = __uint_as_float(u.z & 0xffff0000u);
-    f[6] = __uint_as_float(u.w << 16);
-    f[7] = __uint_as_float(u.w & 0xffff0000u);
-}
-
-__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi)
-{
-    uint32_t r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-
 __device__ __forceinline__ float bf16_round(float v)
 {
     return __uint_as_float(bf16x2_rn(v, 0.0f) << 16);
-}
-
-__device__ __forceinline__ uint32_t e4m3x4_rn(float e0, float e1, float e2, float e3)
-{
-    uint32_t r;
-    asm("{\n\t.reg .b16 p01, p23;\n\t"
-        "cvt.rn.satfinite.e4m3x2.f32 p01, %2, %1;\n\t"
-        "cvt.rn.satfinite.e4m3x2.f32 p23, %4, %3;\n\t"
-        "mov.b32 %0, {p01, p23};\n\t}"
-        : "=r"(r)
-        : "f"(e0), "f"(e1), "f"(e2), "f"(e3));
-    return r;
 }
 
 // the exponent of the next power of two at or above x > 0, biased by 127 and

@@ -26,6 +26,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "convert.cuh"
 #include "fastdiv.h"
 #include "ops.h"
 
@@ -52,29 +53,15 @@ struct IParams {
     uint64_t slot_div;  // fastdiv_magic(block_size)
 };
 
-__device__ __forceinline__ uint32_t e4m3x4_rn(float e0, float e1, float e2, float e3)
-{
-    uint32_t r;
-    asm("{\n\t.reg .b16 p01, p23;\n\t"
-        "cvt.rn.satfinite.e4m3x2.f32 p01, %2, %1;\n\t"
-        "cvt.rn.satfinite.e4m3x2.f32 p23, %4, %3;\n\t"
-        "mov.b32 %0, {p01, p23};\n\t}"
-        : "=r"(r)
-        : "f"(e0), "f"(e1), "f"(e2), "f"(e3));
-    return r;
-}
-
-// the low and the high bf16 of a 32-bit word, widened to fp32 (exact)
-__device__ __forceinline__ float lo_f32(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float hi_f32(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
 // the 8 codes of one lane: E4M3(x * inv) for the 8 bf16 of v
 __device__ __forceinline__ uint2 encode8(uint4 v, float inv)
 {
-    return make_uint2(e4m3x4_rn(__fmul_rn(lo_f32(v.x), inv), __fmul_rn(hi_f32(v.x), inv),
-                                __fmul_rn(lo_f32(v.y), inv), __fmul_rn(hi_f32(v.y), inv)),
-                      e4m3x4_rn(__fmul_rn(lo_f32(v.z), inv), __fmul_rn(hi_f32(v.z), inv),
-                                __fmul_rn(lo_f32(v.w), inv), __fmul_rn(hi_f32(v.w), inv)));
+    float f[8];
+    widen8(v, f);
+    return make_uint2(e4m3x4_rn(__fmul_rn(f[0], inv), __fmul_rn(f[1], inv), __fmul_rn(f[2], inv),
+                                __fmul_rn(f[3], inv)),
+                      e4m3x4_rn(__fmul_rn(f[4], inv), __fmul_rn(f[5], inv), __fmul_rn(f[6], inv),
+                                __fmul_rn(f[7], inv)));
 }
 
 // the scale exponent s of a row from the bits of its amax (bf16, sign cleared)

@@ -1,4 +1,5 @@
-// Row arithmetic shared by the fused kernels (included by both kernel files).
+// Row arithmetic of the whole-warp layout, shared by the fused kernels (and
+// the scale helpers the half-warp layout of halfrow.cuh builds on).
 //
 // One warp owns one 512-wide row; lane l holds dims [8l, 8l+8) and
 // [256+8l, 256+8l+8) as two 16-byte vectors.  Every operation is pinned with
@@ -10,6 +11,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "convert.cuh"
 #include "launch.h"
 
 namespace dsv4 {
@@ -27,64 +29,6 @@ constexpr uint32_t kMant1p75 = 0x600000u;  // mantissa field of 1.75 (448 = 1.75
 constexpr uint32_t kNearBand = 512u;
 
 
-__device__ __forceinline__ uint4 ld_stream16(const void *p)
-{
-    return __ldcs(reinterpret_cast<const uint4 *>(p));
-}
-
-__device__ __forceinline__ void st_stream16(void *p, uint4 v)
-{
-    __stcs(reinterpret_cast<uint4 *>(p), v);
-}
-
-__device__ __forceinline__ void st_stream8(void *p, uint2 v)
-{
-    __stcs(reinterpret_cast<uint2 *>(p), v);
-}
-
-// 8 bf16 (one 16-byte vector) -> 8 fp32, exact
-__device__ __forceinline__ void widen8(uint4 u, float *f)
-{
-    f[0] = __uint_as_float(u.x << 16);
-    f[1] = __uint_as_float(u.x & 0xffff0000u);
-    f[2] = __uint_as_float(u.y << 16);
-    f[3] = __uint_as_float(u.y & 0xffff0000u);
-    f[4] = __uint_as_float(u.z << 16);
-    f[5] = __uint_as_float(u.z & 0xffff0000u);
-    f[6] = __uint_as_float(u.w << 16);
-    f[7] = __uint_as_float(u.w & 0xffff0000u);
-}
-
-// two fp32 -> bf16x2 (round to nearest even), `lo` in the low half
-__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi)
-{
-    uint32_t r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-
-__device__ __forceinline__ uint4 bf16x8_rn(const float *y)
-{
-    return make_uint4(bf16x2_rn(y[0], y[1]), bf16x2_rn(y[2], y[3]), bf16x2_rn(y[4], y[5]),
-                      bf16x2_rn(y[6], y[7]));
-}
-
-// four fp32 -> four E4M3 bytes (round to nearest even, saturating at +-448),
-// element 0 in the lowest byte.  The cvt instruction packs its first source
-// into the upper byte of each 16-bit half.
-__device__ __forceinline__ uint32_t e4m3x4_rn(float e0, float e1, float e2, float e3)
-{
-    uint32_t r;
-    asm("{\n\t"
-        ".reg .b16 p01, p23;\n\t"
-        "cvt.rn.satfinite.e4m3x2.f32 p01, %2, %1;\n\t"
-        "cvt.rn.satfinite.e4m3x2.f32 p23, %4, %3;\n\t"
-        "mov.b32 %0, {p01, p23};\n\t"
-        "}"
-        : "=r"(r)
-        : "f"(e0), "f"(e1), "f"(e2), "f"(e3));
-    return r;
-}
 
 __device__ __forceinline__ float warp_sum(float v)
 {
