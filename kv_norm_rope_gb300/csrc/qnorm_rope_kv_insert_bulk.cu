@@ -30,6 +30,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "rowmath.cuh"
 
 namespace dsv4 {
@@ -323,9 +325,19 @@ template <int kStore, bool kKvNorm>
 int launch_bulk_one(dim3 grid, cudaStream_t stream, const KParams &p)
 {
     auto kernel = qnorm_rope_kv_insert_bulk_kernel<kStore, kKvNorm>;
-    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(bulk_smem_bytes())) != cudaSuccess)
+    // the opt-in to more than 48 KB of dynamic shared memory, once per device
+    // (bit d of `configured` for device d < 64; other devices set it every call)
+    static std::atomic<uint64_t> configured{0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
         return DSV4_ERR_CUDA;
+    const uint64_t bit = dev >= 0 && dev < 64 ? uint64_t(1) << dev : 0;
+    if (bit == 0 || (configured.load(std::memory_order_relaxed) & bit) == 0) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(bulk_smem_bytes())) != cudaSuccess)
+            return DSV4_ERR_CUDA;
+        configured.fetch_or(bit, std::memory_order_relaxed);
+    }
     kernel<<<grid, kBulkThreadsPerCta, bulk_smem_bytes(), stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
 }
