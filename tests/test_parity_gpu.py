@@ -65,9 +65,10 @@ def test_heavy_tails_all_variants():
 
 
 @pytest.mark.parametrize("store", ["fp8", "bf16"])
-@pytest.mark.parametrize("bs", [1, 3, 7, 64])
+@pytest.mark.parametrize("bs", [1, 3, 7, 64, 256, 1024])
 def test_block_sizes(bs, store):
-    """Odd block sizes put FP8 data rows on 8-byte (not 16-byte) boundaries."""
+    """Odd block sizes put FP8 data rows on 8-byte (not 16-byte) boundaries; large
+    ones put a whole batch in one or two blocks."""
     wl = configs.generic(200, 4, seed=bs)
     wl = configs.Workload(wl.name + f"_bs{bs}_{store}", wl.T, wl.H, store, wl.max_position,
                           -(-2 * wl.T // bs), bs, wl.seed)
@@ -333,3 +334,18 @@ def test_full_size_workloads_bulk(name):
     """The shared-memory-staged variant at full size (every cache byte, 1024 sampled
     tokens' q)."""
     _check(configs.WORKLOADS[name], k.VARIANT_BULK, n_sample=1024)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_positions_at_both_ends_of_the_table(variant):
+    """Positions 0 and max_position - 1 (the last row of the cos/sin table) are in
+    range; max_position is the first one out of range."""
+    wl = configs.generic(64, 8, seed=140, max_position=1000, skip_frac=0.0)
+    pos = np.where(np.arange(64) % 3 == 0, 0, 999).astype(np.int64)
+    pos[5] = 1000
+    inp = harness.make_inputs(wl, positions=pos)
+    gpu = harness.run_gpu(inp, variant)
+    ref_q, ref_cache, ref_err = harness.run_oracle(inp)
+    assert gpu.err == ref_err == k.DEVERR_POS_RANGE
+    rep = harness.compare_results(inp, gpu, ref_q, ref_cache)
+    assert rep.ok, str(rep)
