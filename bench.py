@@ -91,10 +91,17 @@ KERNEL_SOURCES = tuple("kv_norm_rope_gb300/csrc/" + f for f in (
 
 
 def kernel_fingerprint() -> str:
-    """16 hex digits identifying the kernel sources (sha256 over their sha256s)."""
+    """16 hex digits identifying the code of the kernel sources: comments and
+    whitespace are dropped before hashing, so a comment edit does not orphan the
+    figures profiled on that code (sha256 over the files' sha256s)."""
     import hashlib
-    digests = "".join(hashlib.sha256(open(os.path.join(ROOT, f), "rb").read()).hexdigest()
-                      for f in KERNEL_SOURCES)
+    import re
+    digests = ""
+    for f in KERNEL_SOURCES:
+        text = open(os.path.join(ROOT, f)).read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        digests += hashlib.sha256(" ".join(text.split()).encode()).hexdigest()
     return hashlib.sha256(digests.encode()).hexdigest()[:16]
 
 

@@ -15,17 +15,20 @@
 //    512 contiguous bytes (four full 128-byte lines) and every byte is read and
 //    written exactly once, with evict-first (.cs) hints: q and kv are touched
 //    once, so they should not push the cos/sin rows out of L1/L2.
-//  * Work rows are token-major: rows t*(H+1) .. t*(H+1)+H-1 are the q heads of
-//    token t in memory order, row t*(H+1)+H is its KV row.  Every warp is
-//    uniformly a q row or a KV row at any moment (no divergence inside a row),
-//    and neighbouring warps share a token's 256-byte cos/sin row in L1
-//    (the 910B section: re-gathering cos/sin per head cost 2.8x there).
+//  * Work items: first the T KV rows (one per item), then the T*H q rows in
+//    memory order in groups of kRows (rows t*H .. t*H+H-1 are token t's
+//    heads).  A warp is uniformly on a KV row or a q group at any moment (no
+//    divergence inside a row); the KV rows, heavier than q rows, stay out of
+//    the q loop's register budget; neighbouring warps share a token's 256-byte
+//    cos/sin row in L1 (the 910B section: re-gathering cos/sin per head cost
+//    2.8x there).
 //  * The streaming variant runs persistent CTAs sized to the SM count and each
 //    warp issues the loads of several rows before it uses any of them, so
 //    enough bytes stay in flight per SM to cover DRAM latency (the SGLang
 //    section "Modifications": the one-token layout stalled on
 //    long_scoreboard with DRAM at 5-7% of peak).  The small variant, for tiny
-//    batches, gives every row its own warp in one wave.
+//    batches, gives every row its own warp in one wave.  (Two more layouts live
+//    in their own files: one row per half-warp, and rows staged by bulk copies.)
 //  * Sums of squares are a fixed per-lane sequence followed by a fixed xor
 //    butterfly, and the rotation is pinned to explicit fma/mul intrinsics, so
 //    a row's bits do not depend on which warp, CTA or variant ran it (the
@@ -37,8 +40,8 @@
 //    boundary 448*2^k; only then does the warp recompute the row's norm and
 //    the affected elements in fp64 (GB300's fp64 rate is low, so this is kept
 //    off the common path: about 3e-4 of KV rows take it on Gaussian data).
-//  * Nothing waits, spins or traps.  Out-of-range positions or slots set a
-//    bit in the caller's error word and the affected writes are skipped.
+//  * Nothing here waits, spins or traps.  Out-of-range positions or slots set
+//    a bit in the caller's error word and the affected writes are skipped.
 
 #include <cuda_runtime.h>
 #include <stdint.h>
