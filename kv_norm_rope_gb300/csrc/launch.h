@@ -1,5 +1,7 @@
-// Internal interface between the C-ABI layer (api.cpp) and the kernels
-// (qnorm_rope_kv_insert.cu).  Not installed; not part of the ABI.
+// Internal interface between the C-ABI layer (api.cpp) and the whole-warp
+// fused kernels (qnorm_rope_kv_insert.cu, qnorm_rope_kv_insert_bulk.cu), plus
+// the kernel arguments every fused kernel takes.  Not installed; not part of
+// the ABI.
 #pragma once
 
 #include <cuda_runtime.h>
