@@ -164,26 +164,33 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
         self.out.close()
-        rows = []
         with open(self.path) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
-                    continue
-                if self.bus_id and self.bus_id.lower() not in parts[1].lower():
-                    continue
-                try:
-                    rows.append((float(parts[2]), float(parts[3]), parts[5:9]))
-                except ValueError:
-                    continue
+            lines = f.readlines()
         os.remove(self.path)
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({n for _, _, flags in rows for n, fl in zip(names, flags)
-                          if fl.lower() == "active"})
-        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": reasons, "samples": len(rows)}
+        return summarise_clocks(lines, self.bus_id)
+
+
+def summarise_clocks(lines, bus_id: str | None) -> dict:
+    """Median SM clock, max SM clock and the active throttle reasons of nvidia-smi
+    CSV samples (the fields of ClockSampler), keeping only the GPU with `bus_id`."""
+    rows = []
+    for line in lines:
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 9:
+            continue
+        if bus_id and bus_id.lower() not in parts[1].lower():
+            continue
+        try:
+            rows.append((float(parts[2]), float(parts[3]), parts[5:9]))
+        except ValueError:
+            continue
+    if not rows:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    reasons = sorted({n for _, _, flags in rows for n, fl in zip(names, flags)
+                      if fl.lower() == "active"})
+    return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+            "reasons": reasons, "samples": len(rows)}
 
 
 def bus_id_of(device_index: int) -> str | None:
