@@ -193,6 +193,19 @@ def summarise_clocks(lines, bus_id: str | None) -> dict:
             "reasons": reasons, "samples": len(rows)}
 
 
+def self_check(per_gpu_gbs: float, achieved_gbs: float, copy_1g: float, copy_512m: float) -> dict:
+    """A kernel cannot move its bytes faster than a plain device-to-device copy of the
+    same run; more than 5% above it means the timed work is not what was counted.
+    Reported, and warned about on stderr, rather than fatal."""
+    ceiling = max(copy_1g, copy_512m)
+    worst = max(per_gpu_gbs, achieved_gbs) / ceiling
+    ok = worst <= 1.05
+    if not ok:
+        print(f"bench self-check: {worst:.3f} x the in-run copy ceiling ({ceiling:.0f} GB/s)",
+              file=sys.stderr)
+    return {"ok": ok, "over_copy_ceiling": round(worst, 4)}
+
+
 def bus_id_of(device_index: int) -> str | None:
     import torch
     p = torch.cuda.get_device_properties(device_index)
@@ -675,6 +688,7 @@ def run_ours(args):
                    "parallelism": f"dp{world}" if world > 1 else "single"},
         "tokens_per_s": round(total_tokens / t_step, 1),
         "frac_of_copy_ceiling": round(value / world / copy_1g, 4),
+        "self_check": self_check(value / world, achieved, copy_1g, copy_512m),
         "frac_of_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
         "copy_ceiling_gbs": {"1GiB": round(copy_1g, 1), "512MiB": round(copy_512m, 1)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,

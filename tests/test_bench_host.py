@@ -65,3 +65,9 @@ def test_committed_summaries_name_their_commands():
         assert "ncu " in text and "--clock-control none" in text, name
         assert "python bench.py" in text, name
         assert "_work" not in text, name
+
+
+def test_self_check_flags_rates_above_the_copy_ceiling():
+    assert bench.self_check(6500.0, 6510.0, 6630.0, 6400.0) == {"ok": True, "over_copy_ceiling": 0.9819}
+    bad = bench.self_check(7200.0, 7300.0, 6630.0, 6400.0)
+    assert not bad["ok"] and bad["over_copy_ceiling"] > 1.05
