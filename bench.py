@@ -540,12 +540,35 @@ def _sample_tokens_for(wl: configs.Workload, seconds: float) -> int:
     return int(max(1, min(wl.T, seconds / per_tok)))
 
 
+def cpu_model() -> str:
+    """The host CPU as /proc/cpuinfo names it (x86 "model name"; on Arm the
+    implementer and part numbers), else the machine type."""
+    import platform
+    try:
+        info = open("/proc/cpuinfo").read()
+    except OSError:
+        return platform.machine()
+    for key in ("model name", "Model"):
+        for line in info.splitlines():
+            if line.startswith(key) and ":" in line:
+                return line.split(":", 1)[1].strip()
+    fields = {}
+    for line in info.splitlines():
+        if ":" in line:
+            k, v = (x.strip() for x in line.split(":", 1))
+            fields.setdefault(k, v)
+    if "CPU implementer" in fields:
+        return (f"{platform.machine()} implementer {fields['CPU implementer']} "
+                f"part {fields.get('CPU part', '?')}")
+    return platform.machine()
+
+
 def cpu_baseline(wl: configs.Workload, seconds: float = 2.0):
     cores = os.cpu_count() or 1
     sample = OracleSample(wl, _sample_tokens_for(wl, seconds))
     dt = sample.run()
     return {"value": round(sample.bytes / dt / 1e9, 4), "unit": "GB/s", "cores": cores,
-            "kind": "oracle",
+            "cpu": cpu_model(), "kind": "oracle",
             "sample": f"first {sample.n} tokens of {wl.name} ({wl.T}x{wl.H}), all heads + KV "
                       f"rows, {dt:.1f} s on {cores} threads",
             "tokens_per_s": round(sample.n / dt, 1)}
@@ -578,7 +601,7 @@ def run_reference(args):
                        "step_sample_tokens": sample.n},
             "tokens_per_s": round(sample.n / mean, 1),
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
-                             "kind": "oracle",
+                             "cpu": cpu_model(), "kind": "oracle",
                              "sample": f"first {sample.n} tokens of {wl.name} per step, all "
                                        f"heads + KV rows"},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,

@@ -71,3 +71,7 @@ def test_self_check_flags_rates_above_the_copy_ceiling():
     assert bench.self_check(6500.0, 6510.0, 6630.0, 6400.0) == {"ok": True, "over_copy_ceiling": 0.9819}
     bad = bench.self_check(7200.0, 7300.0, 6630.0, 6400.0)
     assert not bad["ok"] and bad["over_copy_ceiling"] > 1.05
+
+
+def test_cpu_model_is_a_nonempty_name():
+    assert isinstance(bench.cpu_model(), str) and bench.cpu_model()
