@@ -182,6 +182,9 @@ int launch_gemma_rmsnorm_mxfp8(const uint16_t *x, const uint16_t *residual, cons
     p.padded_cols = ((n / 32) + 3) / 4 * 4;
     p.eps = eps;
     const int64_t grid = (m + 127) / 128 * 128;  // padding rows zero their scales
+    // threads x fragments per thread covering the row; at hidden 7168, 8 warps of
+    // 4 fragments measured 3-4% faster than 4 warps of 8 (and than 7, 12, 14, 16
+    // or 28 warps): more warps per row shorten the row's load-reduce-store chain
     const int fragments = n / 8;
     if (fragments <= 128)
         launch_rows<128, 1>(grid, stream, p);
@@ -190,7 +193,7 @@ int launch_gemma_rmsnorm_mxfp8(const uint16_t *x, const uint16_t *residual, cons
     else if (fragments <= 512)
         launch_rows<128, 4>(grid, stream, p);
     else if (fragments <= 1024)
-        launch_rows<128, 8>(grid, stream, p);
+        launch_rows<256, 4>(grid, stream, p);
     else
         launch_rows<256, 8>(grid, stream, p);
     return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
