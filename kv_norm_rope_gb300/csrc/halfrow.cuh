@@ -278,6 +278,33 @@ __device__ __forceinline__ void stage_weight(const uint16_t *w, int i, float4 *w
 }
 
 
+// One KV row per half-warp: this half takes token t (idle when t >= T).  It
+// loads the token's metadata and row, flags an out-of-range position or slot,
+// and writes the cache row when both are in range.  Both halves reach every
+// shuffle; a pair with no row to write skips the arithmetic (warp-uniform).
+template <int kStore, bool kKvNorm>
+__device__ __forceinline__ void kv_pair_item(const KParams &p, int h, int64_t t,
+                                             const float4 *w_smem)
+{
+    const bool live = t < p.num_tokens;
+    const int64_t pos = live ? __ldg(p.pos + t) : 0;
+    const int64_t slot = live ? __ldg(p.slot + t) : -1;
+    uint4 x[4];
+#pragma unroll
+    for (int v = 0; v < 4; ++v)
+        x[v] = live ? ld_stream16(p.kv + t * kHead + 128 * v + 8 * h) : make_uint4(0u, 0u, 0u, 0u);
+    const bool pos_ok = pos >= 0 && pos < p.max_pos;
+    if (live && h == 0) {
+        if (!pos_ok)
+            flag_error(p.err, DSV4_DEVERR_POS_RANGE);
+        else if (slot >= p.num_slots)
+            flag_error(p.err, DSV4_DEVERR_SLOT_RANGE);
+    }
+    const bool active = live && pos_ok && slot >= 0 && slot < p.num_slots;
+    if (__any_sync(kFull, active))
+        half_row<kStore, kKvNorm>(p, h, active, t, pos, slot, x, w_smem);
+}
+
 // One q head row: y = x * r with the rope dims rotated first (compensated)
 // and then scaled, the operations of q_row on the same values; returns the
 // lane's four output vectors (bf16, round to nearest).

@@ -9,7 +9,8 @@
 // the rope branch, the scale word, address arithmetic) rather than per-element
 // work.  Here half a warp owns a row (the layout of halfrow.cuh), so every warp
 // instruction serves two rows, and the cache bytes stay identical to the
-// fused kernel's.  Each warp loads kKvPairs row pairs before it computes any.
+// fused kernel's.  A warp item is one row pair; 2-8 rows per warp, and 2-4 CTAs
+// per SM, measured within 5% of this.
 
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -21,7 +22,6 @@ namespace dsv4 {
 namespace {
 
 constexpr int kKvThreads = 256;
-constexpr int kKvPairs = 1;  // row pairs per warp loaded together
 
 template <int kStore, bool kKvNorm>
 __global__ void __launch_bounds__(kKvThreads, 3) kv_rows_kernel(const KParams p)
@@ -33,45 +33,11 @@ __global__ void __launch_bounds__(kKvThreads, 3) kv_rows_kernel(const KParams p)
         __syncthreads();
     }
     const int lane = threadIdx.x & 31, h = lane & 15, half = lane >> 4;
-    const int64_t T = p.num_tokens;
-    const int64_t groups = (T + 2 * kKvPairs - 1) / (2 * kKvPairs);
+    const int64_t pairs = (p.num_tokens + 1) / 2;
     const int64_t stride = int64_t(gridDim.x) * (kKvThreads / 32);
-    for (int64_t g = int64_t(blockIdx.x) * (kKvThreads / 32) + (threadIdx.x >> 5); g < groups;
-         g += stride) {
-        const int64_t t0 = g * 2 * kKvPairs + half;
-        int64_t pos[kKvPairs], slot[kKvPairs];
-        uint4 x[kKvPairs][4];
-#pragma unroll
-        for (int j = 0; j < kKvPairs; ++j) {
-            const int64_t t = t0 + 2 * j;
-            pos[j] = t < T ? __ldg(p.pos + t) : 0;
-            slot[j] = t < T ? __ldg(p.slot + t) : -1;
-        }
-#pragma unroll
-        for (int j = 0; j < kKvPairs; ++j) {
-            const int64_t t = t0 + 2 * j;
-#pragma unroll
-            for (int v = 0; v < 4; ++v)
-                x[j][v] = t < T ? ld_stream16(p.kv + t * kHead + 128 * v + 8 * h)
-                                : make_uint4(0u, 0u, 0u, 0u);
-        }
-#pragma unroll
-        for (int j = 0; j < kKvPairs; ++j) {
-            const int64_t t = t0 + 2 * j;
-            const bool pos_ok = pos[j] >= 0 && pos[j] < p.max_pos;
-            if (t < T && h == 0) {
-                if (!pos_ok)
-                    flag_error(p.err, DSV4_DEVERR_POS_RANGE);
-                else if (slot[j] >= p.num_slots)
-                    flag_error(p.err, DSV4_DEVERR_SLOT_RANGE);
-            }
-            const bool active = t < T && pos_ok && slot[j] >= 0 && slot[j] < p.num_slots;
-            // both halves idle: skip the pair's arithmetic (a warp-uniform branch)
-            if (!__any_sync(kFull, active))
-                continue;
-            half_row<kStore, kKvNorm>(p, h, active, t, pos[j], slot[j], x[j], w_smem);
-        }
-    }
+    for (int64_t g = int64_t(blockIdx.x) * (kKvThreads / 32) + (threadIdx.x >> 5); g < pairs;
+         g += stride)
+        kv_pair_item<kStore, kKvNorm>(p, h, 2 * g + half, w_smem);
 }
 
 template <int kStore>
@@ -96,7 +62,7 @@ int kv_rows_ctas_per_sm(int *ctas_per_sm)
 
 int kv_rows_per_warp()
 {
-    return 2 * kKvPairs;
+    return 2;
 }
 
 int launch_kv_rows(int store_mode, const LaunchArgs &a, int64_t max_ctas, cudaStream_t stream)
@@ -117,8 +83,8 @@ int launch_kv_rows(int store_mode, const LaunchArgs &a, int64_t max_ctas, cudaSt
     p.eps = a.eps;
     p.err = a.err;
     p.slot_div = fastdiv_magic(static_cast<uint32_t>(a.block_size));
-    const int64_t groups = (a.num_tokens + 2 * kKvPairs - 1) / (2 * kKvPairs);
-    const int64_t need = (groups + kKvThreads / 32 - 1) / (kKvThreads / 32);
+    const int64_t pairs = (a.num_tokens + 1) / 2;
+    const int64_t need = (pairs + kKvThreads / 32 - 1) / (kKvThreads / 32);
     const unsigned grid = static_cast<unsigned>(need < max_ctas ? need : max_ctas);
     if (store_mode == DSV4_STORE_BF16)
         launch_store<DSV4_STORE_BF16>(a.kv_norm, grid, stream, p);

@@ -47,24 +47,7 @@ __global__ void __launch_bounds__(kHalfThreads, 3) qnorm_rope_kv_insert_half_ker
     for (int64_t it = int64_t(blockIdx.x) * (kHalfThreads / 32) + (threadIdx.x >> 5); it < items;
          it += stride) {
         if (it < kv_items) {
-            const int64_t t = 2 * it + half;
-            const int64_t pos = t < T ? __ldg(p.pos + t) : 0;
-            const int64_t slot = t < T ? __ldg(p.slot + t) : -1;
-            uint4 x[4];
-#pragma unroll
-            for (int v = 0; v < 4; ++v)
-                x[v] = t < T ? ld_stream16(p.kv + t * kHead + 128 * v + 8 * h)
-                             : make_uint4(0u, 0u, 0u, 0u);
-            const bool pos_ok = pos >= 0 && pos < p.max_pos;
-            if (t < T && h == 0) {
-                if (!pos_ok)
-                    flag_error(p.err, DSV4_DEVERR_POS_RANGE);
-                else if (slot >= p.num_slots)
-                    flag_error(p.err, DSV4_DEVERR_SLOT_RANGE);
-            }
-            const bool active = t < T && pos_ok && slot >= 0 && slot < p.num_slots;
-            if (__any_sync(kFull, active))
-                half_row<kStore, kKvNorm>(p, h, active, t, pos, slot, x, w_smem);
+            kv_pair_item<kStore, kKvNorm>(p, h, 2 * it + half, w_smem);
             continue;
         }
         const int64_t r0 = (it - kv_items) * 2 * kQPairs;
