@@ -355,6 +355,14 @@ class DeviceBatch:
             return lib.dsv4_dequant_gather, (
                 self.cache.data_ptr(), wl.num_blocks, wl.block_size, self.slots.data_ptr(), wl.T,
                 self.out.data_ptr(), self.err.data_ptr(), stream_handle)
+        if self.op in ("kv_only", "prenorm") and self.variant:
+            # the general entry, for an explicit launch variant
+            return lib.dsv4_insert_ex, (
+                0 if wl.store == "fp8" else 1, self.variant, 1 if self.op == "kv_only" else 0,
+                self.q.data_ptr() if wl.H else None, self.kv.data_ptr(), self.w.data_ptr(),
+                self.pos.data_ptr(), self.cs.data_ptr(), wl.max_position, self.slots.data_ptr(),
+                self.cache.data_ptr(), wl.num_blocks, wl.block_size, wl.T, wl.H, wl.eps,
+                self.err.data_ptr(), stream_handle)
         if self.op == "kv_only":
             return lib.dsv4_kv_norm_rope_insert, (
                 0 if wl.store == "fp8" else 1, self.kv.data_ptr(), self.w.data_ptr(),

@@ -266,11 +266,11 @@ typedef struct {
 /*
  * Fill *plan for T tokens, H heads on a GPU with sm_count SMs where
  * ctas_per_sm CTAs of the streaming kernel fit per SM.  variant AUTO picks
- * SMALL when the rows would not give every warp slot of the GPU at least a
- * full group of rows (SGLang PR #33358, "Modifications" item 3: a
- * grid-starved multi-token layout loses at small N); with q heads, HALF when
- * they would give it fewer than two (decode-sized batches, where HALF measured
- * faster); else STREAM.  BULK runs one CTA
+ * SMALL when there are fewer rows than a quarter of the GPU's warp slots (SGLang
+ * PR #33358, "Modifications" item 3: a grid-starved multi-token layout loses at
+ * small N); with q heads, HALF below 8 rounds of the streaming kernel's groups
+ * (warp slots x rows_per_warp x 8; decode-sized batches, where HALF measured
+ * faster); else STREAM (for num_heads 0, the KV-row kernel).  BULK runs one CTA
  * per SM (at most one per 32-row chunk).  HALF: ceil(T/2) KV row pairs and
  * groups of rows_per_warp q rows over persistent CTAs (ctas_per_sm then being
  * the HALF kernel's occupancy).  With num_heads 0, STREAM describes the

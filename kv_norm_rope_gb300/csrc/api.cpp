@@ -203,12 +203,15 @@ int dsv4_launch_plan(int64_t num_tokens, int32_t num_heads, int32_t sm_count, in
     const int stream_warps = dsv4::kStreamThreads / 32;
     const int64_t warp_slots = int64_t(sm_count) * ctas_per_sm * stream_warps;
     if (variant == DSV4_VARIANT_AUTO) {
-        // fewer rows than one group per warp slot: one row per warp; with q heads,
-        // fewer than two rounds of groups: the half-warp kernel (measured faster
-        // there, slower on long streams); otherwise the whole-warp stream
+        // Measured on GB300 (graph-timed, cold L2): one row per warp is fastest
+        // below about a quarter of the warp slots; from there, with q heads, the
+        // half-warp kernel beats both the others up to 8 rounds of the stream
+        // kernel's 3-row groups (6-35% at 2K-66K rows, a tie near 100K-130K);
+        // beyond, the whole-warp stream (2% ahead on long streams).  With no q
+        // heads, STREAM runs the KV-row kernel, ahead of SMALL from ~2K rows.
         const int64_t round = warp_slots * dsv4::kStreamRowsPerWarp;
-        variant = rows < round                            ? DSV4_VARIANT_SMALL
-                  : num_heads > 0 && rows < 2 * round     ? DSV4_VARIANT_HALF
+        variant = rows < warp_slots / 4                   ? DSV4_VARIANT_SMALL
+                  : num_heads > 0 && rows < 8 * round     ? DSV4_VARIANT_HALF
                                                           : DSV4_VARIANT_STREAM;
     }
     plan->rows = rows;

@@ -107,15 +107,17 @@ def test_launch_plan_small_and_stream():
     # 131072 x 129 rows: persistent grid, 4 CTAs on each of 152 SMs
     p = k.launch_plan(131072, 128, 152, 4)
     assert (p.variant, p.threads, p.ctas, p.rows) == (k.VARIANT_STREAM, 256, 608, 131072 * 129)
-    # the crossovers: rows below one round of groups (warp slots x rows per warp) go
-    # SMALL; with q heads, below two rounds HALF; beyond, STREAM
-    slots = 152 * 4 * 8 * p.rows_per_warp
-    assert k.launch_plan(slots // 65 - 1, 64, 152, 4).variant == k.VARIANT_SMALL
-    assert k.launch_plan(slots // 65 + 1, 64, 152, 4).variant == k.VARIANT_HALF
-    assert k.launch_plan(2 * slots // 65 - 1, 64, 152, 4).variant == k.VARIANT_HALF
-    assert k.launch_plan(2 * slots // 65 + 1, 64, 152, 4).variant == k.VARIANT_STREAM
+    # the crossovers: rows below a quarter of the warp slots go SMALL; with q heads,
+    # below 8 rounds of 3-row groups HALF; beyond, STREAM
+    warp_slots = 152 * 4 * 8
+    rnd = warp_slots * p.rows_per_warp
+    assert k.launch_plan(warp_slots // 4 // 9 - 1, 8, 152, 4).variant == k.VARIANT_SMALL
+    assert k.launch_plan(warp_slots // 4 // 9 + 1, 8, 152, 4).variant == k.VARIANT_HALF
+    assert k.launch_plan(8 * rnd // 65 - 1, 64, 152, 4).variant == k.VARIANT_HALF
+    assert k.launch_plan(8 * rnd // 65 + 1, 64, 152, 4).variant == k.VARIANT_STREAM
     # KV rows only: never HALF (they have their own kernel behind STREAM)
-    assert k.launch_plan(slots + 1, 0, 152, 4).variant == k.VARIANT_STREAM
+    assert k.launch_plan(warp_slots // 4 - 1, 0, 152, 4).variant == k.VARIANT_SMALL
+    assert k.launch_plan(warp_slots // 4 + 1, 0, 152, 4).variant == k.VARIANT_STREAM
     # forced variants
     assert k.launch_plan(131072, 128, 152, 4, k.VARIANT_SMALL).ctas == 131072 * 129 // 2
     p = k.launch_plan(3, 1, 152, 4, k.VARIANT_STREAM)
