@@ -87,7 +87,8 @@ def barrier(world: int):
 # ------------------------------------------------------------------ measurement helpers
 
 KERNEL_SOURCES = tuple("kv_norm_rope_gb300/csrc/" + f for f in (
-    "qnorm_rope_kv_insert.cu", "rowmath.cuh", "convert.cuh", "fastdiv.h", "launch.h"))
+    "qnorm_rope_kv_insert.cu", "rowmath.cuh", "convert.cuh", "fastdiv.h", "launch.h",
+    "launch_status.h"))
 
 
 def kernel_fingerprint() -> str:

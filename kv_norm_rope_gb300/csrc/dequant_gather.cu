@@ -20,6 +20,7 @@
 #include "convert.cuh"
 #include "fastdiv.h"
 #include "launch.h"
+#include "launch_status.h"
 
 namespace dsv4 {
 namespace {
@@ -150,8 +151,7 @@ int launch_gather(const uint8_t *cache, int64_t num_blocks, int32_t block_size,
     p.rows = rows;
     p.out = out;
     p.err = err;
-    dequant_gather_kernel<<<unsigned(ctas), 256, 0, stream>>>(p);
-    return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
+    return launch_kernel(dequant_gather_kernel, dim3(unsigned(ctas)), dim3(256), 0, stream, p);
 }
 
 int gather_rows_per_warp()

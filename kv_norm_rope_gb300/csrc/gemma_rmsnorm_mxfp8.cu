@@ -20,6 +20,7 @@
 #include <stdint.h>
 
 #include "convert.cuh"
+#include "launch_status.h"
 #include "ops.h"
 
 namespace dsv4 {
@@ -159,9 +160,10 @@ __global__ void __launch_bounds__(kThreads) gemma_rmsnorm_mxfp8_kernel(const MPa
 }
 
 template <int kThreads, int kTrips>
-void launch_rows(int64_t grid, cudaStream_t stream, const MParams &p)
+int launch_rows(int64_t grid, cudaStream_t stream, const MParams &p)
 {
-    gemma_rmsnorm_mxfp8_kernel<kThreads, kTrips><<<unsigned(grid), kThreads, 0, stream>>>(p);
+    return launch_kernel(gemma_rmsnorm_mxfp8_kernel<kThreads, kTrips>, dim3(unsigned(grid)),
+                         dim3(kThreads), 0, stream, p);
 }
 
 }  // namespace
@@ -187,16 +189,14 @@ int launch_gemma_rmsnorm_mxfp8(const uint16_t *x, const uint16_t *residual, cons
     // or 28 warps): more warps per row shorten the row's load-reduce-store chain
     const int fragments = n / 8;
     if (fragments <= 128)
-        launch_rows<128, 1>(grid, stream, p);
-    else if (fragments <= 256)
-        launch_rows<128, 2>(grid, stream, p);
-    else if (fragments <= 512)
-        launch_rows<128, 4>(grid, stream, p);
-    else if (fragments <= 1024)
-        launch_rows<256, 4>(grid, stream, p);
-    else
-        launch_rows<256, 8>(grid, stream, p);
-    return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
+        return launch_rows<128, 1>(grid, stream, p);
+    if (fragments <= 256)
+        return launch_rows<128, 2>(grid, stream, p);
+    if (fragments <= 512)
+        return launch_rows<128, 4>(grid, stream, p);
+    if (fragments <= 1024)
+        return launch_rows<256, 4>(grid, stream, p);
+    return launch_rows<256, 8>(grid, stream, p);
 }
 
 }  // namespace dsv4

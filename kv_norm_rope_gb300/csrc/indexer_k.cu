@@ -28,6 +28,7 @@
 
 #include "convert.cuh"
 #include "fastdiv.h"
+#include "launch_status.h"
 #include "ops.h"
 
 namespace dsv4 {
@@ -221,11 +222,8 @@ int launch_indexer_insert(const uint16_t *k, const int64_t *slots, uint8_t *cach
     p.err = err;
     const unsigned grid = static_cast<unsigned>(grid_for(rows, max_ctas));
     const bool wide = (reinterpret_cast<uintptr_t>(cache) & 7u) == 0 && block_size % 2 == 0;
-    if (wide)
-        indexer_k_insert_kernel<true><<<grid, kThreads, 0, stream>>>(p);
-    else
-        indexer_k_insert_kernel<false><<<grid, kThreads, 0, stream>>>(p);
-    return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
+    return launch_kernel(wide ? indexer_k_insert_kernel<true> : indexer_k_insert_kernel<false>,
+                         dim3(grid), dim3(kThreads), 0, stream, p);
 }
 
 int launch_indexer_gather(const uint8_t *cache, int64_t num_blocks, int32_t block_size,
@@ -244,11 +242,8 @@ int launch_indexer_gather(const uint8_t *cache, int64_t num_blocks, int32_t bloc
     p.err = err;
     const unsigned grid = static_cast<unsigned>(grid_for(rows, max_ctas));
     const bool wide = (reinterpret_cast<uintptr_t>(cache) & 7u) == 0 && block_size % 2 == 0;
-    if (wide)
-        indexer_k_gather_kernel<true><<<grid, kThreads, 0, stream>>>(p);
-    else
-        indexer_k_gather_kernel<false><<<grid, kThreads, 0, stream>>>(p);
-    return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
+    return launch_kernel(wide ? indexer_k_gather_kernel<true> : indexer_k_gather_kernel<false>,
+                         dim3(grid), dim3(kThreads), 0, stream, p);
 }
 
 }  // namespace dsv4

@@ -16,6 +16,7 @@
 #include <stdint.h>
 
 #include "halfrow.cuh"
+#include "launch_status.h"
 #include "ops.h"
 
 namespace dsv4 {
@@ -41,12 +42,10 @@ __global__ void __launch_bounds__(kKvThreads, 3) kv_rows_kernel(const KParams p)
 }
 
 template <int kStore>
-void launch_store(bool kv_norm, unsigned grid, cudaStream_t stream, const KParams &p)
+int launch_store(bool kv_norm, unsigned grid, cudaStream_t stream, const KParams &p)
 {
-    if (kv_norm)
-        kv_rows_kernel<kStore, true><<<grid, kKvThreads, 0, stream>>>(p);
-    else
-        kv_rows_kernel<kStore, false><<<grid, kKvThreads, 0, stream>>>(p);
+    return launch_kernel(kv_norm ? kv_rows_kernel<kStore, true> : kv_rows_kernel<kStore, false>,
+                         dim3(grid), dim3(kKvThreads), 0, stream, p);
 }
 
 }  // namespace
@@ -86,11 +85,8 @@ int launch_kv_rows(int store_mode, const LaunchArgs &a, int64_t max_ctas, cudaSt
     const int64_t pairs = (a.num_tokens + 1) / 2;
     const int64_t need = (pairs + kKvThreads / 32 - 1) / (kKvThreads / 32);
     const unsigned grid = static_cast<unsigned>(need < max_ctas ? need : max_ctas);
-    if (store_mode == DSV4_STORE_BF16)
-        launch_store<DSV4_STORE_BF16>(a.kv_norm, grid, stream, p);
-    else
-        launch_store<DSV4_STORE_FP8>(a.kv_norm, grid, stream, p);
-    return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
+    return store_mode == DSV4_STORE_BF16 ? launch_store<DSV4_STORE_BF16>(a.kv_norm, grid, stream, p)
+                                         : launch_store<DSV4_STORE_FP8>(a.kv_norm, grid, stream, p);
 }
 
 }  // namespace dsv4

@@ -46,6 +46,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "launch_status.h"
 #include "rowmath.cuh"
 
 namespace dsv4 {
@@ -136,12 +137,10 @@ struct Kernels {
 };
 
 template <int kStore, bool kKvNorm>
-void launch_one(bool small, dim3 grid, dim3 block, cudaStream_t stream, const KParams &p)
+int launch_one(bool small, dim3 grid, dim3 block, cudaStream_t stream, const KParams &p)
 {
-    if (small)
-        Kernels<kStore, kKvNorm>::small<<<grid, block, 0, stream>>>(p);
-    else
-        Kernels<kStore, kKvNorm>::stream<<<grid, block, 0, stream>>>(p);
+    return launch_kernel(small ? Kernels<kStore, kKvNorm>::small : Kernels<kStore, kKvNorm>::stream,
+                         grid, block, 0, stream, p);
 }
 
 }  // namespace
@@ -182,18 +181,11 @@ int launch(int store_mode, const dsv4_plan &plan, const LaunchArgs &a, cudaStrea
         return launch_bulk(store_mode, a.kv_norm, plan.ctas, p, stream);
     const dim3 grid(unsigned(plan.ctas)), block(unsigned(plan.threads));
     const bool small = plan.variant == DSV4_VARIANT_SMALL;
-    if (store_mode == DSV4_STORE_BF16) {
-        if (a.kv_norm)
-            launch_one<DSV4_STORE_BF16, true>(small, grid, block, stream, p);
-        else
-            launch_one<DSV4_STORE_BF16, false>(small, grid, block, stream, p);
-    } else {
-        if (a.kv_norm)
-            launch_one<DSV4_STORE_FP8, true>(small, grid, block, stream, p);
-        else
-            launch_one<DSV4_STORE_FP8, false>(small, grid, block, stream, p);
-    }
-    return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
+    if (store_mode == DSV4_STORE_BF16)
+        return a.kv_norm ? launch_one<DSV4_STORE_BF16, true>(small, grid, block, stream, p)
+                         : launch_one<DSV4_STORE_BF16, false>(small, grid, block, stream, p);
+    return a.kv_norm ? launch_one<DSV4_STORE_FP8, true>(small, grid, block, stream, p)
+                     : launch_one<DSV4_STORE_FP8, false>(small, grid, block, stream, p);
 }
 
 }  // namespace dsv4

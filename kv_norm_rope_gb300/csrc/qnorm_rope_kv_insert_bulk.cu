@@ -33,6 +33,7 @@
 #include <atomic>
 
 #include "rowmath.cuh"
+#include "launch_status.h"
 
 namespace dsv4 {
 namespace {
@@ -338,8 +339,7 @@ int launch_bulk_one(dim3 grid, cudaStream_t stream, const KParams &p)
             return DSV4_ERR_CUDA;
         configured.fetch_or(bit, std::memory_order_relaxed);
     }
-    kernel<<<grid, kBulkThreadsPerCta, bulk_smem_bytes(), stream>>>(p);
-    return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
+    return launch_kernel(kernel, grid, dim3(kBulkThreadsPerCta), bulk_smem_bytes(), stream, p);
 }
 
 }  // namespace

@@ -19,6 +19,7 @@
 #include <stdint.h>
 
 #include "halfrow.cuh"
+#include "launch_status.h"
 #include "ops.h"
 
 namespace dsv4 {
@@ -97,12 +98,11 @@ __global__ void __launch_bounds__(kHalfThreads, 3) qnorm_rope_kv_insert_half_ker
 }
 
 template <int kStore>
-void launch_store(bool kv_norm, unsigned grid, cudaStream_t stream, const KParams &p)
+int launch_store(bool kv_norm, unsigned grid, cudaStream_t stream, const KParams &p)
 {
-    if (kv_norm)
-        qnorm_rope_kv_insert_half_kernel<kStore, true><<<grid, kHalfThreads, 0, stream>>>(p);
-    else
-        qnorm_rope_kv_insert_half_kernel<kStore, false><<<grid, kHalfThreads, 0, stream>>>(p);
+    return launch_kernel(kv_norm ? qnorm_rope_kv_insert_half_kernel<kStore, true>
+                                 : qnorm_rope_kv_insert_half_kernel<kStore, false>,
+                         dim3(grid), dim3(kHalfThreads), 0, stream, p);
 }
 
 }  // namespace
@@ -140,11 +140,9 @@ int launch_half(int store_mode, const LaunchArgs &a, int64_t ctas, cudaStream_t 
     p.eps = a.eps;
     p.err = a.err;
     p.slot_div = fastdiv_magic(static_cast<uint32_t>(a.block_size));
-    if (store_mode == DSV4_STORE_BF16)
-        launch_store<DSV4_STORE_BF16>(a.kv_norm, static_cast<unsigned>(ctas), stream, p);
-    else
-        launch_store<DSV4_STORE_FP8>(a.kv_norm, static_cast<unsigned>(ctas), stream, p);
-    return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
+    const unsigned grid = static_cast<unsigned>(ctas);
+    return store_mode == DSV4_STORE_BF16 ? launch_store<DSV4_STORE_BF16>(a.kv_norm, grid, stream, p)
+                                         : launch_store<DSV4_STORE_FP8>(a.kv_norm, grid, stream, p);
 }
 
 }  // namespace dsv4
