@@ -188,6 +188,61 @@ def _stream_handle(stream) -> int | None:
     return stream.cuda_stream
 
 
+def _kinds():
+    import torch
+    two_byte = (torch.bfloat16, torch.int16) + ((torch.uint16,) if hasattr(torch, "uint16") else ())
+    return {"bf16": two_byte, "i64": (torch.int64,), "f32": (torch.float32,),
+            "u8": (torch.uint8, torch.int8), "i32": (torch.int32,), "bytes": None}
+
+
+def _check(name: str, t, kind: str, numel: int | None = None, min_bytes: int | None = None):
+    """Reject a tensor argument the C ABI cannot check: wrong element type (bf16 data
+    may come as any 2-byte dtype), not contiguous, or the wrong number of elements /
+    too few bytes.  Raw integer pointers pass unchecked; _on_cuda checks devices."""
+    if t is None or isinstance(t, int):
+        return
+    allowed = _kinds()[kind]
+    if allowed is not None and t.dtype not in allowed:
+        raise TypeError(f"{name}: expected {kind} data, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if numel is not None and t.numel() != numel:
+        raise ValueError(f"{name}: expected {numel} elements, got {t.numel()}")
+    if min_bytes is not None and t.numel() * t.element_size() < min_bytes:
+        raise ValueError(f"{name}: needs at least {min_bytes} bytes, has "
+                         f"{t.numel() * t.element_size()}")
+
+
+def _on_cuda(**tensors):
+    """Every tensor argument lives on one CUDA device: there is no CPU path."""
+    devices = set()
+    for name, t in tensors.items():
+        if t is None or isinstance(t, int):
+            continue
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+        devices.add(t.device)
+    if len(devices) > 1:
+        raise ValueError(f"tensor arguments on several devices: {sorted(map(str, devices))}")
+
+
+def _check_step(store_mode, q, kv, w, positions, cos_sin_cache, slot_mapping, kv_cache,
+                num_blocks, block_size, device_error, T, H):
+    _check("positions", positions, "i64", T)
+    _check("slot_mapping", slot_mapping, "i64", T)
+    _check("q", q, "bf16", T * H * 512)
+    _check("kv", kv, "bf16", T * 512)
+    _check("kv_norm_weight", w, "bf16", 512)
+    _check("cos_sin_cache", cos_sin_cache, "f32")
+    if not isinstance(cos_sin_cache, int) and cos_sin_cache.numel() % 64:
+        raise ValueError("cos_sin_cache must hold rows of 64 fp32 (32 cos, 32 sin)")
+    need = (fp8_cache_bytes if store_mode == STORE_FP8 else bf16_cache_bytes)(num_blocks, block_size)
+    _check("kv_cache", kv_cache, "bytes", min_bytes=need)
+    _check("device_error", device_error, "i32")
+    _on_cuda(q=q, kv=kv, kv_norm_weight=w, positions=positions, cos_sin_cache=cos_sin_cache,
+             slot_mapping=slot_mapping, kv_cache=kv_cache, device_error=device_error)
+
+
 def _shape_args(q, kv, positions, cos_sin_cache):
     T = int(positions.shape[0])
     if q is None:
@@ -213,6 +268,8 @@ def insert(store_mode: int, q, kv, kv_norm_weight, positions, cos_sin_cache, slo
     T, H, max_pos = _shape_args(q, kv, positions, cos_sin_cache)
     if num_heads is not None:
         H = num_heads
+    _check_step(store_mode, q, kv, kv_norm_weight if kv_norm else None, positions, cos_sin_cache,
+                slot_mapping, kv_cache, num_blocks, block_size, device_error, T, H)
     st = lib().dsv4_insert_ex(
         store_mode, variant, 1 if kv_norm else 0, _ptr(q), _ptr(kv), _ptr(kv_norm_weight),
         _ptr(positions), _ptr(cos_sin_cache), max_pos, _ptr(slot_mapping), _ptr(kv_cache),
@@ -226,6 +283,8 @@ def qnorm_rope_kv_rope_quant_insert(q, kv, positions, cos_sin_cache, slot_mappin
                                     stream=None) -> None:
     """dsv4_qnorm_rope_kv_rope_quant_insert: KV rows arrive normalised (rope + FP8 only)."""
     T, H, max_pos = _shape_args(q, kv, positions, cos_sin_cache)
+    _check_step(STORE_FP8, q, kv, None, positions, cos_sin_cache, slot_mapping, kv_cache,
+                num_blocks, block_size, device_error, T, H)
     st = lib().dsv4_qnorm_rope_kv_rope_quant_insert(
         _ptr(q), _ptr(kv), _ptr(positions), _ptr(cos_sin_cache), max_pos, _ptr(slot_mapping),
         _ptr(kv_cache), num_blocks, block_size, T, H, eps, _ptr(device_error),
@@ -239,6 +298,8 @@ def kv_norm_rope_insert(store_mode: int, kv, kv_norm_weight, positions, cos_sin_
                         stream=None) -> None:
     """dsv4_kv_norm_rope_insert: KV rows only (norm with weight, rope, FP8 or bf16 store)."""
     T, _, max_pos = _shape_args(None, kv, positions, cos_sin_cache)
+    _check_step(store_mode, None, kv, kv_norm_weight, positions, cos_sin_cache, slot_mapping,
+                kv_cache, num_blocks, block_size, device_error, T, 0)
     st = lib().dsv4_kv_norm_rope_insert(
         store_mode, _ptr(kv), _ptr(kv_norm_weight), _ptr(positions), _ptr(cos_sin_cache),
         max_pos, _ptr(slot_mapping), _ptr(kv_cache), num_blocks, block_size, T, eps,
@@ -252,6 +313,8 @@ def qnorm_rope_kv_quant_insert(q, kv, kv_norm_weight, positions, cos_sin_cache, 
                                stream=None) -> None:
     """dsv4_qnorm_rope_kv_quant_insert: FP8 (448 E4M3 + 7 UE8M0 + 64 bf16) cache rows."""
     T, H, max_pos = _shape_args(q, kv, positions, cos_sin_cache)
+    _check_step(STORE_FP8, q, kv, kv_norm_weight, positions, cos_sin_cache, slot_mapping, kv_cache,
+                num_blocks, block_size, device_error, T, H)
     st = lib().dsv4_qnorm_rope_kv_quant_insert(
         _ptr(q), _ptr(kv), _ptr(kv_norm_weight), _ptr(positions), _ptr(cos_sin_cache), max_pos,
         _ptr(slot_mapping), _ptr(kv_cache), num_blocks, block_size, T, H, eps,
@@ -265,6 +328,8 @@ def qnorm_rope_kv_bf16_insert(q, kv, kv_norm_weight, positions, cos_sin_cache, s
                               stream=None) -> None:
     """dsv4_qnorm_rope_kv_bf16_insert: 512 bf16 cache rows."""
     T, H, max_pos = _shape_args(q, kv, positions, cos_sin_cache)
+    _check_step(STORE_BF16, q, kv, kv_norm_weight, positions, cos_sin_cache, slot_mapping,
+                kv_cache, num_blocks, block_size, device_error, T, H)
     st = lib().dsv4_qnorm_rope_kv_bf16_insert(
         _ptr(q), _ptr(kv), _ptr(kv_norm_weight), _ptr(positions), _ptr(cos_sin_cache), max_pos,
         _ptr(slot_mapping), _ptr(kv_cache), num_blocks, block_size, T, H, eps,
@@ -276,6 +341,12 @@ def qnorm_rope_kv_bf16_insert(q, kv, kv_norm_weight, positions, cos_sin_cache, s
 def dequant_gather(kv_cache, num_blocks: int, block_size: int, slots, out, device_error=None,
                    stream=None) -> None:
     """dsv4_dequant_gather: out (bf16 [n, 512]) = FP8 cache rows at ``slots`` read back."""
+    n = int(slots.shape[0])
+    _check("slots", slots, "i64", n)
+    _check("kv_cache", kv_cache, "bytes", min_bytes=fp8_cache_bytes(num_blocks, block_size))
+    _check("out", out, "bf16", n * 512)
+    _check("device_error", device_error, "i32")
+    _on_cuda(kv_cache=kv_cache, slots=slots, out=out, device_error=device_error)
     st = lib().dsv4_dequant_gather(_ptr(kv_cache), num_blocks, block_size, _ptr(slots),
                                    int(slots.shape[0]), _ptr(out), _ptr(device_error),
                                    _stream_handle(stream))
@@ -291,6 +362,13 @@ def indexer_k_quant_insert(k, slot_mapping, indexer_cache, num_blocks: int, bloc
                            device_error=None, stream=None) -> None:
     """dsv4_indexer_k_quant_insert: k (bf16 [T, 128]) quantised into the indexer cache
     (uint8, indexer_cache_bytes(num_blocks, block_size)) at slot_mapping (int64 [T])."""
+    T = int(slot_mapping.shape[0])
+    _check("slot_mapping", slot_mapping, "i64", T)
+    _check("k", k, "bf16", T * 128)
+    _check("indexer_cache", indexer_cache, "bytes",
+           min_bytes=indexer_cache_bytes(num_blocks, block_size))
+    _check("device_error", device_error, "i32")
+    _on_cuda(k=k, slot_mapping=slot_mapping, indexer_cache=indexer_cache, device_error=device_error)
     st = lib().dsv4_indexer_k_quant_insert(_ptr(k), _ptr(slot_mapping), _ptr(indexer_cache),
                                            num_blocks, block_size, int(slot_mapping.shape[0]),
                                            _ptr(device_error), _stream_handle(stream))
@@ -302,6 +380,15 @@ def indexer_k_gather(indexer_cache, num_blocks: int, block_size: int, slots, k_o
                      device_error=None, stream=None) -> None:
     """dsv4_indexer_k_gather: k_out (uint8 [n, 128]) and scale_out (fp32 [n]) read from
     the indexer cache at ``slots`` (int64 [n])."""
+    n = int(slots.shape[0])
+    _check("slots", slots, "i64", n)
+    _check("indexer_cache", indexer_cache, "bytes",
+           min_bytes=indexer_cache_bytes(num_blocks, block_size))
+    _check("k_out", k_out, "u8", n * 128)
+    _check("scale_out", scale_out, "f32", n)
+    _check("device_error", device_error, "i32")
+    _on_cuda(indexer_cache=indexer_cache, slots=slots, k_out=k_out, scale_out=scale_out,
+             device_error=device_error)
     st = lib().dsv4_indexer_k_gather(_ptr(indexer_cache), num_blocks, block_size, _ptr(slots),
                                      int(slots.shape[0]), _ptr(k_out), _ptr(scale_out),
                                      _ptr(device_error), _stream_handle(stream))
@@ -315,8 +402,18 @@ def mxfp8_scale_bytes(num_rows: int, hidden: int) -> int:
 
 def add_gemma_rmsnorm_mxfp8(x, residual, gamma, eps: float, residual_out, codes, scales,
                             stream=None) -> None:
-    """dsv4_add_gemma_rmsnorm_mxfp8: residual add + Gemma RMSNorm + MXFP8 rows."""
+    """dsv4_add_gemma_rmsnorm_mxfp8: residual add + Gemma RMSNorm + MXFP8 rows.
+
+    x, residual, residual_out: bf16 [m, n]; gamma: bf16 [n]; codes: uint8 [m, n];
+    scales: uint8, mxfp8_scale_bytes(m, n) bytes."""
     m, n = int(x.shape[0]), int(x.shape[1])
+    for name, t in (("x", x), ("residual", residual), ("residual_out", residual_out)):
+        _check(name, t, "bf16", m * n)
+    _check("gamma", gamma, "bf16", n)
+    _check("codes", codes, "u8", m * n)
+    _check("scales", scales, "u8", min_bytes=mxfp8_scale_bytes(m, n))
+    _on_cuda(x=x, residual=residual, gamma=gamma, residual_out=residual_out, codes=codes,
+             scales=scales)
     st = lib().dsv4_add_gemma_rmsnorm_mxfp8(_ptr(x), _ptr(residual), _ptr(gamma), m, n, eps,
                                             _ptr(residual_out), _ptr(codes), _ptr(scales),
                                             _stream_handle(stream))

@@ -92,7 +92,8 @@ def test_no_cpu_fallback_without_a_gpu():
     if torch.cuda.is_available():
         pytest.skip("a GPU is present; covered by the GPU tests")
     assert _call() == k.ERR_CUDA
-    with pytest.raises(k.Dsv4Error):
+    # the binding refuses host tensors before any call: there is no CPU path
+    with pytest.raises(ValueError, match="CUDA tensor"):
         k.insert(k.STORE_FP8, torch.zeros(16, 8, 512, dtype=torch.bfloat16),
                  torch.zeros(16, 512, dtype=torch.bfloat16), torch.zeros(512, dtype=torch.bfloat16),
                  torch.zeros(16, dtype=torch.int64), torch.zeros(4096, 64),
@@ -310,3 +311,36 @@ def test_launch_plan_half():
     assert plan.variant == k.VARIANT_HALF and plan.rows_per_warp == 4 and plan.threads == 256
     assert plan.ctas == min(-(-items // 8), 152 * 3)
     assert k.launch_plan(3, 1, 152, 3, k.VARIANT_HALF).ctas == 1
+
+
+def test_binding_rejects_mistyped_and_misshaped_tensors():
+    """Element types, contiguity, device and sizes are checked before the C call."""
+    torch = pytest.importorskip("torch")
+    T, H = 4, 2
+    ok = dict(q=torch.zeros(T, H, 512, dtype=torch.bfloat16), kv=torch.zeros(T, 512, dtype=torch.bfloat16),
+              w=torch.zeros(512, dtype=torch.bfloat16), pos=torch.zeros(T, dtype=torch.int64),
+              cs=torch.zeros(8, 64), sl=torch.zeros(T, dtype=torch.int64),
+              cache=torch.zeros(2 * 4 * 584, dtype=torch.uint8))
+
+    def call(**kw):
+        a = dict(ok); a.update(kw)
+        k.insert(k.STORE_FP8, a["q"], a["kv"], a["w"], a["pos"], a["cs"], a["sl"], a["cache"], 2, 4, 1e-6,
+                 stream=0)
+
+    with pytest.raises(TypeError, match="positions"):
+        call(pos=torch.zeros(T, dtype=torch.int32))
+    with pytest.raises(TypeError, match="cos_sin_cache"):
+        call(cs=torch.zeros(8, 64, dtype=torch.float64))
+    with pytest.raises(TypeError, match="q"):
+        call(q=torch.zeros(T, H, 512))
+    with pytest.raises(ValueError, match="contiguous"):
+        call(kv=torch.zeros(512, T, dtype=torch.bfloat16).t())
+    with pytest.raises(ValueError, match="kv:"):
+        call(kv=torch.zeros(T + 1, 512, dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="kv_cache"):
+        call(cache=torch.zeros(100, dtype=torch.uint8))
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        call()
+    with pytest.raises(TypeError, match="k_out"):
+        k.indexer_k_gather(torch.zeros(132 * 64, dtype=torch.uint8), 1, 64, torch.zeros(3, dtype=torch.int64),
+                           torch.zeros(3, 128, dtype=torch.int16), torch.zeros(3))
