@@ -32,23 +32,6 @@ __device__ __forceinline__ int w_index(int j, int part, int h)
     return (2 * j + part) * 16 + h;
 }
 
-// The first UE8M0 guess of the fused kernel's ue8m0_guess, with the same s and
-// near flag: amax = M * 2^E (M in [1, 2)), s = E - 8 + (M > 1.75) clamped to
-// [-127, 127] (amax below 2^-126 lands on -127); near when the mantissa is
-// within kNearBand of 1.75's and the two candidates do not clamp to the same
-// value (biased exponent above 7).
-__device__ __forceinline__ ScaleGuess guess_lean(float amax)
-{
-    const uint32_t bits = __float_as_uint(amax);
-    const int ef = int(bits >> 23);
-    const uint32_t m = bits & 0x7fffffu;
-    ScaleGuess g;
-    g.e = ef - 127;
-    g.s = min(max(ef - 135 + (m > kMant1p75 ? 1 : 0), -127), 127);
-    g.near = (m - (kMant1p75 - kNearBand)) <= 2u * kNearBand && ef > 7;
-    return g;
-}
-
 __device__ __forceinline__ float half_sum(float v)
 {
 #pragma unroll
@@ -195,7 +178,7 @@ __device__ __forceinline__ void half_row_fp8(const KParams &p, int h, bool activ
             for (int k = 0; k < 8; ++k)
                 am = fmaxf(am, fabsf(v[j][k]));
         }
-        g[j] = guess_lean(group8_max(am));  // rope lanes: amax 0, never near
+        g[j] = ue8m0_guess(group8_max(am));  // rope lanes: amax 0, never near
         g[j].near = g[j].near && active;
     }
     if (kKvNorm && __any_sync(kFull, g[0].near || g[1].near || g[2].near || g[3].near)) {

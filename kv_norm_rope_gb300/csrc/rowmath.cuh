@@ -117,21 +117,16 @@ struct ScaleGuess {
 
 __device__ __forceinline__ ScaleGuess ue8m0_guess(float amax)
 {
+    // amax below 2^-126 (biased exponent 0) lands on -127 through the clamp; the
+    // band test is one unsigned compare; with biased exponent <= 7 both
+    // candidates clamp to -127, so the exact path has nothing to decide
     const uint32_t bits = __float_as_uint(amax);
     const int ef = int(bits >> 23);
     const uint32_t m = bits & 0x7fffffu;
     ScaleGuess g;
     g.e = ef - 127;
-    if (ef == 0) {  // amax < 2^-126: the exponent is at most -134, clamped to -127
-        g.s = -127;
-        g.near = false;
-        return g;
-    }
-    const int s = g.e - 8 + (m > kMant1p75 ? 1 : 0);
-    g.near = m + kNearBand >= kMant1p75 && m <= kMant1p75 + kNearBand;
-    if (g.e - 7 <= -127 || g.e - 8 >= 127)  // both candidates clamp to the same value
-        g.near = false;
-    g.s = min(max(s, -127), 127);
+    g.s = min(max(ef - 135 + (m > kMant1p75 ? 1 : 0), -127), 127);
+    g.near = (m - (kMant1p75 - kNearBand)) <= 2u * kNearBand && ef > 7;
     return g;
 }
 
