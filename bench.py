@@ -259,7 +259,8 @@ class DeviceBatch:
     slots, the weight and the cos/sin table come from ``synth``.  ``op`` "kv_only"
     holds no q."""
 
-    def __init__(self, wl: configs.Workload, dev, op: str = "fused", variant: int = 0):
+    def __init__(self, wl: configs.Workload, dev, op: str = "fused", variant: int = 0,
+                 hidden: int = MXFP8_HIDDEN):
         import torch
         self.variant = variant
         if op in ("kv_only", "gather", "mxfp8", "indexer", "indexer_gather"):
@@ -283,9 +284,9 @@ class DeviceBatch:
         if op == "prenorm":
             self.bytes -= 1024  # no weight read
         if op == "mxfp8":
-            # activation rows [T, MXFP8_HIDDEN]: x, residual (in place), gamma, codes, scales
+            # activation rows [T, hidden]: x, residual (in place), gamma, codes, scales
             import kv_norm_rope_gb300 as k
-            n = MXFP8_HIDDEN
+            n = self.hidden = hidden
             self.x = self._normal((wl.T, n), g)
             self.res = self._normal((wl.T, n), g)
             self.gamma = self._normal((n,), g)
@@ -340,7 +341,7 @@ class DeviceBatch:
         wl = self.wl
         if self.op == "mxfp8":
             return lib.dsv4_add_gemma_rmsnorm_mxfp8, (
-                self.x.data_ptr(), self.res.data_ptr(), self.gamma.data_ptr(), wl.T, MXFP8_HIDDEN,
+                self.x.data_ptr(), self.res.data_ptr(), self.gamma.data_ptr(), wl.T, self.hidden,
                 wl.eps, self.res.data_ptr(), self.codes.data_ptr(), self.mx_scales.data_ptr(),
                 stream_handle)
         if self.op == "indexer":
@@ -641,7 +642,7 @@ def run_ours(args):
     kac_before = known_answer_check() if rank == 0 else "skipped"
     copy_1g = copy_ceiling_gbs(dev, 1 << 30)
     copy_512m = copy_ceiling_gbs(dev, 1 << 29)
-    batch = DeviceBatch(wl, dev, args.op, VARIANTS[args.variant])
+    batch = DeviceBatch(wl, dev, args.op, VARIANTS[args.variant], args.hidden)
     wl = batch.wl
     stream = torch.cuda.current_stream(dev)
     fn, call_args = batch.call(lib, stream.cuda_stream)
@@ -713,6 +714,7 @@ def run_ours(args):
                    "l2": "flushed before every launch (256 MB write)" if flush is not None
                    else f"inputs larger than L2 ({batch.bytes / 1e9:.2f} GB per step)",
                    "io": IO_OF_OP[args.op],
+                   **({"hidden": args.hidden} if args.op == "mxfp8" else {}),
                    "variant": (args.variant if args.variant != "auto" else
                                {k.VARIANT_STREAM: "stream", k.VARIANT_SMALL: "small", k.VARIANT_HALF: "half",
                                 k.VARIANT_BULK: "bulk"}[plan.variant])
@@ -769,6 +771,8 @@ def main(argv=None):
                          "gather: read the FP8 cache back out; mxfp8: residual add + Gemma "
                          "RMSNorm + MXFP8 of [T, 7168] activation rows; indexer: indexer-K "
                          "quant-insert of [T, 128] rows; indexer_gather: read them back out")
+    ap.add_argument("--hidden", type=int, default=MXFP8_HIDDEN,
+                    help="row width of --op mxfp8 (a multiple of 128 up to 16384)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="run only the first N tokens of the workload (smaller profiling cases)")
     ap.add_argument("--e2e-steps", type=int, default=6)

@@ -184,19 +184,21 @@ int launch_gemma_rmsnorm_mxfp8(const uint16_t *x, const uint16_t *residual, cons
     p.padded_cols = ((n / 32) + 3) / 4 * 4;
     p.eps = eps;
     const int64_t grid = (m + 127) / 128 * 128;  // padding rows zero their scales
-    // threads x fragments per thread covering the row; at hidden 7168, 8 warps of
-    // 4 fragments measured 3-4% faster than 4 warps of 8 (and than 7, 12, 14, 16
-    // or 28 warps): more warps per row shorten the row's load-reduce-store chain
+    // threads x fragments per thread covering the row, from sweeps on GB300: 8
+    // warps per row (16 for the widest) with 2-4 fragments per thread; more warps
+    // shorten the row's load-reduce-store chain.  Hidden 7168: 8 x 4 beat 4 x 8 by
+    // 3-4% (and 7, 12, 14, 16, 28 warps); 16384: 16 x 4 beat 8 x 8 by 8%; 4096:
+    // 8 x 2 beat 4 x 4 by 1%; 2048: 4 x 2 beat 8 x 1 by 11%.
     const int fragments = n / 8;
     if (fragments <= 128)
         return launch_rows<128, 1>(grid, stream, p);
     if (fragments <= 256)
         return launch_rows<128, 2>(grid, stream, p);
     if (fragments <= 512)
-        return launch_rows<128, 4>(grid, stream, p);
+        return launch_rows<256, 2>(grid, stream, p);
     if (fragments <= 1024)
         return launch_rows<256, 4>(grid, stream, p);
-    return launch_rows<256, 8>(grid, stream, p);
+    return launch_rows<512, 4>(grid, stream, p);
 }
 
 }  // namespace dsv4
