@@ -15,13 +15,14 @@
 //    512 contiguous bytes (four full 128-byte lines) and every byte is read and
 //    written exactly once, with evict-first (.cs) hints: q and kv are touched
 //    once, so they should not push the cos/sin rows out of L1/L2.
-//  * Work items: first the T KV rows (one per item), then the T*H q rows in
-//    memory order in groups of kRows (rows t*H .. t*H+H-1 are token t's
-//    heads).  A warp is uniformly on a KV row or a q group at any moment (no
-//    divergence inside a row); the KV rows, heavier than q rows, stay out of
-//    the q loop's register budget; neighbouring warps share a token's 256-byte
-//    cos/sin row in L1 (the 910B section: re-gathering cos/sin per head cost
-//    2.8x there).
+//  * Work items: the T KV rows (one per item) and the T*H q rows in memory
+//    order in groups of kRows (rows t*H .. t*H+H-1 are token t's heads),
+//    interleaved so that each KV row runs among its own token's q groups: the
+//    heavier KV rows then run under the q stream, not ahead of it.  A warp is
+//    uniformly on a KV row or a q group at any moment (no divergence inside a
+//    row); the KV rows stay out of the q loop's register budget; neighbouring
+//    warps share a token's 256-byte cos/sin row in L1 (the 910B section:
+//    re-gathering cos/sin per head cost 2.8x there).
 //  * The streaming variant runs persistent CTAs sized to the SM count and each
 //    warp issues the loads of several rows before it uses any of them, so
 //    enough bytes stay in flight per SM to cover DRAM latency (the SGLang
@@ -52,9 +53,9 @@
 namespace dsv4 {
 namespace {
 
-// Work items, handed out round-robin over all warps of the grid:
-//   items [0, T)            : the KV row of token t = item
-//   items [T, T + ceil(TH/R)): R consecutive q rows (memory order) each
+// Work items, handed out round-robin over all warps of the grid: the KV row
+// of each token t and ceil(T*H/R) groups of R consecutive q rows (memory
+// order), interleaved as described at the loop.
 template <int kStore, int kRows, bool kSmemW, bool kKvNorm>
 __global__ void __launch_bounds__(256, 3) qnorm_rope_kv_insert_kernel(const KParams p)
 {
@@ -69,21 +70,31 @@ __global__ void __launch_bounds__(256, 3) qnorm_rope_kv_insert_kernel(const KPar
     const int64_t H = p.num_heads;
     const int64_t T = p.num_tokens;
     const int64_t q_rows = T * H;
-    const int64_t items = T + (q_rows + kRows - 1) / kRows;
+    const int64_t groups = (q_rows + kRows - 1) / kRows;
+    const int64_t items = T + groups;
     const int64_t stride = int64_t(gridDim.x) * warps_per_cta;
+    // KV rows interleaved with the q groups: period k (k < T) is KV row k then q
+    // groups [k*G, k*G + G); the q groups past T*G follow.  The heavier KV rows
+    // then run under the q stream instead of ahead of it, next to their token's q.
+    const int64_t G = T > 0 ? groups / T : 0;
+    const int64_t P = G + 1;
 
     for (int64_t it = int64_t(blockIdx.x) * warps_per_cta + (threadIdx.x >> 5); it < items;
          it += stride) {
-        if (it < T) {
-            const int64_t pos = __ldg(p.pos + it);
-            const int64_t slot = __ldg(p.slot + it);
-            const uint16_t *src = p.kv + it * kHead;
+        const int64_t period = it / P;
+        const int64_t o = it - period * P;
+        if (period < T && o == 0) {
+            const int64_t t = period;
+            const int64_t pos = __ldg(p.pos + t);
+            const int64_t slot = __ldg(p.slot + t);
+            const uint16_t *src = p.kv + t * kHead;
             const uint4 xa = ld_stream16(src + 8 * lane);
             const uint4 xb = ld_stream16(src + 256 + 8 * lane);
-            kv_row<kStore, kSmemW, kKvNorm>(p, lane, it, pos, slot, xa, xb, w_smem);
+            kv_row<kStore, kSmemW, kKvNorm>(p, lane, t, pos, slot, xa, xb, w_smem);
             continue;
         }
-        const int64_t r0 = (it - T) * kRows;
+        const int64_t group = period < T ? period * G + (o - 1) : T * G + (it - T * P);
+        const int64_t r0 = group * kRows;
         // token of each row, and its position (tiny, cached loads first)
         int64_t t[kRows], pos[kRows];
         t[0] = r0 / H;
