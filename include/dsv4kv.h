@@ -268,9 +268,9 @@ typedef struct {
  * ctas_per_sm CTAs of the streaming kernel fit per SM.  variant AUTO picks
  * SMALL when there are fewer rows than a quarter of the GPU's warp slots (SGLang
  * PR #33358, "Modifications" item 3: a grid-starved multi-token layout loses at
- * small N); with q heads, HALF below 8 rounds of the streaming kernel's groups
- * (warp slots x rows_per_warp x 8; decode-sized batches, where HALF measured
- * faster); else STREAM (for num_heads 0, the KV-row kernel).  BULK runs one CTA
+ * small N); with q heads, HALF below 12 rounds of the streaming kernel's groups
+ * (warp slots x rows_per_warp x 12; decode- to mid-sized batches, where HALF
+ * measured faster); else STREAM (for num_heads 0, the KV-row kernel).  BULK runs one CTA
  * per SM (at most one per 32-row chunk).  HALF: ceil(T/2) KV row pairs and
  * groups of rows_per_warp q rows over persistent CTAs (ctas_per_sm then being
  * the HALF kernel's occupancy).  With num_heads 0, STREAM describes the

@@ -205,13 +205,13 @@ int dsv4_launch_plan(int64_t num_tokens, int32_t num_heads, int32_t sm_count, in
     if (variant == DSV4_VARIANT_AUTO) {
         // Measured on GB300 (graph-timed, cold L2): one row per warp is fastest
         // below about a quarter of the warp slots; from there, with q heads, the
-        // half-warp kernel beats both the others up to 8 rounds of the stream
-        // kernel's 3-row groups (6-35% at 2K-66K rows, a tie near 100K-130K);
-        // beyond, the whole-warp stream (2% ahead on long streams).  With no q
+        // half-warp kernel beats both the others up to 12 rounds of the stream
+        // kernel's 3-row groups (3-35% at 2K-100K rows, a tie near 130K-200K);
+        // beyond, the whole-warp stream (2.5% ahead from ~260K rows).  With no q
         // heads, STREAM runs the KV-row kernel, ahead of SMALL from ~2K rows.
         const int64_t round = warp_slots * dsv4::kStreamRowsPerWarp;
         variant = rows < warp_slots / 4                   ? DSV4_VARIANT_SMALL
-                  : num_heads > 0 && rows < 8 * round     ? DSV4_VARIANT_HALF
+                  : num_heads > 0 && rows < 12 * round    ? DSV4_VARIANT_HALF
                                                           : DSV4_VARIANT_STREAM;
     }
     plan->rows = rows;

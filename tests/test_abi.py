@@ -109,13 +109,13 @@ def test_launch_plan_small_and_stream():
     p = k.launch_plan(131072, 128, 152, 4)
     assert (p.variant, p.threads, p.ctas, p.rows) == (k.VARIANT_STREAM, 256, 608, 131072 * 129)
     # the crossovers: rows below a quarter of the warp slots go SMALL; with q heads,
-    # below 8 rounds of 3-row groups HALF; beyond, STREAM
+    # below 12 rounds of 3-row groups HALF; beyond, STREAM
     warp_slots = 152 * 4 * 8
     rnd = warp_slots * p.rows_per_warp
     assert k.launch_plan(warp_slots // 4 // 9 - 1, 8, 152, 4).variant == k.VARIANT_SMALL
     assert k.launch_plan(warp_slots // 4 // 9 + 1, 8, 152, 4).variant == k.VARIANT_HALF
-    assert k.launch_plan(8 * rnd // 65 - 1, 64, 152, 4).variant == k.VARIANT_HALF
-    assert k.launch_plan(8 * rnd // 65 + 1, 64, 152, 4).variant == k.VARIANT_STREAM
+    assert k.launch_plan(12 * rnd // 65 - 1, 64, 152, 4).variant == k.VARIANT_HALF
+    assert k.launch_plan(12 * rnd // 65 + 1, 64, 152, 4).variant == k.VARIANT_STREAM
     # KV rows only: never HALF (they have their own kernel behind STREAM)
     assert k.launch_plan(warp_slots // 4 - 1, 0, 152, 4).variant == k.VARIANT_SMALL
     assert k.launch_plan(warp_slots // 4 + 1, 0, 152, 4).variant == k.VARIANT_STREAM
