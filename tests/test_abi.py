@@ -344,3 +344,20 @@ def test_binding_rejects_mistyped_and_misshaped_tensors():
     with pytest.raises(TypeError, match="k_out"):
         k.indexer_k_gather(torch.zeros(132 * 64, dtype=torch.uint8), 1, 64, torch.zeros(3, dtype=torch.int64),
                            torch.zeros(3, 128, dtype=torch.int16), torch.zeros(3))
+
+
+def test_every_export_is_documented():
+    """The design doc's boundary table names every exported entry point, and the README
+    names every Python wrapper of a compute entry."""
+    root = os.path.dirname(HEADER).rsplit(os.sep, 1)[0]
+    design = open(os.path.join(root, "DESIGN.md")).read()
+    table = design[design.index("## 2. The path and its boundary"):design.index("## 3.")]
+    documented = set(re.findall(r"`(dsv4_[a-z0-9_]+)`", table))
+    assert set(k.EXPORTS) <= documented, sorted(set(k.EXPORTS) - documented)
+    readme = open(os.path.join(root, "README.md")).read()
+    for name in ("qnorm_rope_kv_quant_insert", "qnorm_rope_kv_bf16_insert",
+                 "qnorm_rope_kv_rope_quant_insert", "kv_norm_rope_insert", "insert",
+                 "dequant_gather", "indexer_k_quant_insert", "indexer_k_gather",
+                 "add_gemma_rmsnorm_mxfp8"):
+        assert f"`{name}`" in readme or f"k.{name}(" in readme, name
+        assert callable(getattr(k, name))
