@@ -79,8 +79,9 @@ enum {
 enum {
     DSV4_DEVERR_SLOT_RANGE = 1, /* slot_mapping[t] >= num_blocks*block_size: cache row not written */
     DSV4_DEVERR_POS_RANGE = 2,  /* positions[t] < 0 or >= max_position: token not written at all */
-    DSV4_DEVERR_TIMEOUT = 4     /* DSV4_VARIANT_BULK only: a bounded wait inside the kernel ran out
-                                   (never expected); the outputs of that launch are undefined */
+    DSV4_DEVERR_TIMEOUT = 4     /* DSV4_VARIANT_BULK and the KV-row kernel (num_heads 0, STREAM):
+                                   a bounded wait on a bulk copy inside the kernel ran out (never
+                                   expected); the outputs of that launch are undefined */
 };
 
 /* store modes and launch variants of dsv4_qnorm_rope_kv_insert_variant */
@@ -183,7 +184,7 @@ int dsv4_qnorm_rope_kv_rope_quant_insert(void *q, const void *kv, const int64_t 
  * store_mode DSV4_STORE_FP8 (kv_cache uint8, FP8 layout above, 8-byte aligned) or
  * DSV4_STORE_BF16 (kv_cache bf16 [num_blocks, block_size, 512], 16-byte aligned).
  * Other arguments as in dsv4_qnorm_rope_kv_quant_insert.  Batches that plan as
- * STREAM run a kernel laid out for KV rows alone (one row per half-warp); its cache
+ * STREAM run a kernel laid out for KV rows alone (one row per quarter-warp); its cache
  * bytes are identical to those the fused entry points write for the same rows.
  */
 int dsv4_kv_norm_rope_insert(int store_mode, const void *kv, const void *kv_norm_weight,
@@ -274,7 +275,7 @@ typedef struct {
  * per SM (at most one per 32-row chunk).  HALF: ceil(T/2) KV row pairs and
  * groups of rows_per_warp q rows over persistent CTAs (ctas_per_sm then being
  * the HALF kernel's occupancy).  With num_heads 0, STREAM describes the
- * KV-row kernel: one row per half-warp, rows_per_warp 2, and ctas_per_sm should
+ * KV-row kernel: one row per quarter-warp, rows_per_warp 4, and ctas_per_sm should
  * then be that kernel's occupancy.  Returns a dsv4_status.
  */
 int dsv4_launch_plan(int64_t num_tokens, int32_t num_heads, int32_t sm_count,

@@ -26,7 +26,7 @@ _SOURCES = ["qnorm_rope_kv_insert.cu", "qnorm_rope_kv_insert_bulk.cu", "dequant_
 _HEADERS = [os.path.join(_INCLUDE, "dsv4kv.h")] + [
     os.path.join(_CSRC, h)
     for h in ("launch.h", "ops.h", "fastdiv.h", "convert.cuh", "launch_status.h", "rowmath.cuh",
-              "halfrow.cuh")]
+              "halfrow.cuh", "bulkcopy.cuh")]
 NVCC_ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 # status codes and constants (mirrors include/dsv4kv.h)

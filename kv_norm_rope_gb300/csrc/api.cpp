@@ -177,7 +177,7 @@ int insert(int store_mode, int variant, int flags, void *q, const void *kv, cons
     if (plan.variant == DSV4_VARIANT_HALF)
         return dsv4::launch_half(store_mode, a, plan.ctas, static_cast<cudaStream_t>(stream));
     if (num_heads == 0 && plan.variant == DSV4_VARIANT_STREAM) {
-        // KV rows only: the half-warp-per-row kernel
+        // KV rows only: the quarter-warp-per-row kernel
         int64_t resident = 0;
         if (resident_ctas(kOccKvRows, &resident) != DSV4_OK)
             return DSV4_ERR_CUDA;

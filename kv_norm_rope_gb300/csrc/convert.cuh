@@ -37,6 +37,14 @@ __device__ __forceinline__ void widen8(uint4 u, float *f)
     f[7] = __uint_as_float(u.w & 0xffff0000u);
 }
 
+// element k (0..7) of 8 bf16 in one 16-byte vector as fp32, exact (selects,
+// so a run-time k stays in registers too)
+__device__ __forceinline__ float bf16_at(uint4 u, int k)
+{
+    const uint32_t w = k < 2 ? u.x : k < 4 ? u.y : k < 6 ? u.z : u.w;
+    return __uint_as_float((k & 1) ? (w & 0xffff0000u) : (w << 16));
+}
+
 // two fp32 -> bf16x2 (round to nearest even), `lo` in the low half
 __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi)
 {

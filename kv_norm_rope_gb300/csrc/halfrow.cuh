@@ -1,5 +1,5 @@
-// Row arithmetic of the half-warp layout, shared by the kernels that give
-// each 512-wide row half a warp (kv_rows.cu, qnorm_rope_kv_insert_half.cu).
+// Row arithmetic of the half-warp layout: each 512-wide row takes half a warp
+// (qnorm_rope_kv_insert_half.cu).
 //
 // Lane h = lane % 16 of half r = lane / 16 holds dims [128v + 8h, 128v + 8h + 8)
 // of its row for v = 0..3: four 16-byte vectors, so one warp-wide load covers
@@ -11,9 +11,10 @@
 // lane h's partial sums over vectors (0, 2) and (1, 3) are exactly the
 // partials of whole-warp lanes h and h + 16, their sum is the first level of
 // the whole-warp butterfly (xor 16) and the remaining levels (xor 8, 4, 2, 1)
-// are the same; the elementwise operations, the rotation, the block maxima
-// and the exact fp64 decision near a scale boundary are the same operations
-// on the same values.
+// are the same; the elementwise operations, the rotation and the block
+// maxima are the same operations on the same values, and a row with a block
+// too close to a scale boundary is handed to the whole warp, which decides it
+// in the whole-warp layout with the code every kernel uses.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -37,14 +38,6 @@ __device__ __forceinline__ float half_sum(float v)
 #pragma unroll
     for (int m = 8; m >= 1; m >>= 1)
         v = __fadd_rn(v, __shfl_xor_sync(kFull, v, m));
-    return v;
-}
-
-__device__ __forceinline__ double half_sum(double v)
-{
-#pragma unroll
-    for (int m = 8; m >= 1; m >>= 1)
-        v = __dadd_rn(v, __shfl_xor_sync(kFull, v, m));
     return v;
 }
 
@@ -120,43 +113,45 @@ __device__ __forceinline__ void half_row_values(const KParams &p, int h, const u
     }
 }
 
-// The exact decision for blocks too close to a boundary in fp32 (rare): the
-// row's norm in fp64 in the whole-warp order, then each element of a near
-// block as (x * r) * w in fp64 against 1.75 * 2^e.  Returns bit j set when
-// the lane's block of vector j exceeds its boundary (OR-ed over the block).
-__device__ __noinline__ int half_exact_bumps(const KParams &p, int h, int64_t t, const int *e,
-                                             const bool *near)
+// The exact decision for blocks too close to a boundary in fp32 (rare), for
+// the row of each half that has one: the whole warp decides it in the
+// whole-warp layout (exact_scale_bumps), the same code as every other kernel.
+// Lane h of half r holds block 2j + h/8 in vector j, with its exponent e_j
+// and near flag (bit j of near_bits); whole-warp lane l asks for blocks l/8
+// and 4 + l/8.  Returns bit j set when the lane's block of vector j exceeds
+// its boundary.
+__device__ __noinline__ int half_exact_bumps(const KParams &p, int lane, int64_t t, int e0, int e1,
+                                             int e2, int e3, int near_bits)
 {
-    const uint16_t *row = p.kv + t * kHead;
-    double sa = 0.0, sb = 0.0;
-#pragma unroll 1
-    for (int k = 0; k < 16; ++k) {
-        const int da = (k < 8 ? 0 : 248) + 8 * h + k;   // vectors 0 then 2
-        const int db = (k < 8 ? 128 : 376) + 8 * h + k; // vectors 1 then 3
-        const double xa = double(__uint_as_float(uint32_t(__ldg(row + da)) << 16));
-        const double xb = double(__uint_as_float(uint32_t(__ldg(row + db)) << 16));
-        sa = __fma_rn(xa, xa, sa);
-        sb = __fma_rn(xb, xb, sb);
-    }
-    const double ss = half_sum(__dadd_rn(sa, sb));
-    const double r = 1.0 / sqrt(ss / 512.0 + double(p.eps));
+    const unsigned halves = __ballot_sync(kFull, near_bits != 0);
+    const int h = lane & 15;
     int bits = 0;
 #pragma unroll 1
-    for (int j = 0; j < 4; ++j) {
-        bool up = false;
-        if (near[j]) {
-            const double bound = __hiloint2double(int(uint32_t(1023 + e[j]) << 20) | 0x000C0000, 0);
-#pragma unroll 1
-            for (int k = 0; k < 8; ++k) {
-                const int d = 128 * j + 8 * h + k;
-                const double x = double(__uint_as_float(uint32_t(__ldg(row + d)) << 16));
-                const double w = double(__uint_as_float(uint32_t(__ldg(p.w + d)) << 16));
-                if (fabs(__dmul_rn(__dmul_rn(x, r), w)) > bound)
-                    up = true;
-            }
+    for (int r = 0; r < 2; ++r) {
+        if (((halves >> (16 * r)) & 0xffffu) == 0u)
+            continue;
+        const int64_t tr = __shfl_sync(kFull, t, 16 * r);
+        // blocks b = lane/8 and 4 + lane/8 of half r: vector b/2 of lane 16r + 8(b%2)
+        const int b0 = lane >> 3, b1 = 4 + (lane >> 3);
+        const int s0 = 16 * r + 8 * (b0 & 1), s1 = 16 * r + 8 * (b1 & 1);
+        const int a0 = __shfl_sync(kFull, e0, s0), a1 = __shfl_sync(kFull, e1, s0);
+        const int a2 = __shfl_sync(kFull, e2, s0), a3 = __shfl_sync(kFull, e3, s0);
+        const int c0 = __shfl_sync(kFull, e0, s1), c1 = __shfl_sync(kFull, e1, s1);
+        const int c2 = __shfl_sync(kFull, e2, s1), c3 = __shfl_sync(kFull, e3, s1);
+        const int n0 = __shfl_sync(kFull, near_bits, s0), n1 = __shfl_sync(kFull, near_bits, s1);
+        const int j0 = b0 >> 1, j1 = b1 >> 1;
+        const int eb0 = j0 == 0 ? a0 : j0 == 1 ? a1 : j0 == 2 ? a2 : a3;
+        const int eb1 = j1 == 0 ? c0 : j1 == 1 ? c1 : j1 == 2 ? c2 : c3;
+        const int res = exact_scale_bumps(p, lane, tr, eb0, ((n0 >> j0) & 1) != 0, eb1,
+                                          ((n1 >> j1) & 1) != 0);
+        // block b's answer: bit 0 of lane 8b (b < 4), bit 1 of lane 8(b - 4)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int b = 2 * j + (h >> 3);
+            const int got = __shfl_sync(kFull, res, 8 * (b & 3));
+            if ((lane >> 4) == r && ((got >> (b >> 2)) & 1))
+                bits |= 1 << j;
         }
-        if (group8_any(up))
-            bits |= 1 << j;
     }
     return bits;
 }
@@ -182,9 +177,10 @@ __device__ __forceinline__ void half_row_fp8(const KParams &p, int h, bool activ
         g[j].near = g[j].near && active;
     }
     if (kKvNorm && __any_sync(kFull, g[0].near || g[1].near || g[2].near || g[3].near)) {
-        const int e[4] = {g[0].e, g[1].e, g[2].e, g[3].e};
-        const bool nr[4] = {g[0].near, g[1].near, g[2].near, g[3].near};
-        const int bumps = half_exact_bumps(p, h, active ? t : 0, e, nr);
+        const int nb = (g[0].near ? 1 : 0) | (g[1].near ? 2 : 0) | (g[2].near ? 4 : 0) |
+                       (g[3].near ? 8 : 0);
+        const int bumps = half_exact_bumps(p, threadIdx.x & 31, active ? t : 0, g[0].e, g[1].e,
+                                           g[2].e, g[3].e, nb);
 #pragma unroll
         for (int j = 0; j < 4; ++j)
             if (g[j].near)

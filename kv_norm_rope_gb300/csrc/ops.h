@@ -14,7 +14,7 @@
 
 namespace dsv4 {
 
-// KV rows with no q, one row per half-warp (kv_rows.cu); the grid is capped at max_ctas.
+// KV rows with no q, one row per quarter-warp (kv_rows.cu); the grid is capped at max_ctas.
 int kv_rows_ctas_per_sm(int *ctas_per_sm);
 int kv_rows_per_warp();
 int launch_kv_rows(int store_mode, const LaunchArgs &a, int64_t max_ctas, cudaStream_t stream);

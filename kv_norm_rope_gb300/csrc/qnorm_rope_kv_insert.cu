@@ -29,7 +29,8 @@
 //    section "Modifications": the one-token layout stalled on
 //    long_scoreboard with DRAM at 5-7% of peak).  The small variant, for tiny
 //    batches, gives every row its own warp in one wave.  (Two more layouts live
-//    in their own files: one row per half-warp, and rows staged by bulk copies.)
+//    in their own files: one row per half-warp, one KV row per quarter-warp when
+//    there are no q heads, and rows staged by bulk copies.)
 //  * Sums of squares are a fixed per-lane sequence followed by a fixed xor
 //    butterfly, and the rotation is pinned to explicit fma/mul intrinsics, so
 //    a row's bits do not depend on which warp, CTA or variant ran it (the

@@ -32,8 +32,9 @@
 
 #include <atomic>
 
-#include "rowmath.cuh"
+#include "bulkcopy.cuh"
 #include "launch_status.h"
+#include "rowmath.cuh"
 
 namespace dsv4 {
 namespace {
@@ -44,64 +45,11 @@ constexpr int kStages = 6;
 constexpr int kStoresInFlight = 2;  // bulk stores allowed to be still reading their stage
 static_assert(kStoresInFlight < kStages, "a stage must be free before it is reloaded");
 constexpr int kBulkThreadsPerCta = 32 * (kConsumers + 1);
-// Waits sleep in the barrier unit (up to kSuspendNs per try) rather than spin,
-// so waiting warps do not take issue slots from the producer and the busy
-// consumers; kSpinLimit tries bound a wait to about one second.
-constexpr uint32_t kSuspendNs = 20000;
-constexpr uint32_t kSpinLimit = 1u << 16;
+// Waits are the bounded polls of bulkcopy.cuh.
 constexpr int kWeightOffset = 256;   // after 2 * kStages mbarriers
 constexpr int kStageOffset = 1280;   // after the 1 KB weight
 constexpr uint32_t kChunkBytes = kChunkRows * 1024;
 static_assert(2 * kStages * 8 <= kWeightOffset, "barriers overlap the weight");
-
-__device__ __forceinline__ uint32_t smem_addr(const void *p)
-{
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count));
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
-                 "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-
-// wait for the completion of the phase with the given parity; false if the
-// bounded number of tries ran out
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
-{
-    for (uint32_t i = 0; i < kSpinLimit; ++i) {
-        uint32_t done;
-        asm volatile("{\n\t.reg .pred p;\n\t"
-                     "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-                     "selp.u32 %0, 1, 0, p;\n\t}"
-                     : "=r"(done)
-                     : "r"(smem_addr(bar)), "r"(parity), "r"(kSuspendNs)
-                     : "memory");
-        if (done)
-            return true;
-    }
-    return false;
-}
-
-__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
-{
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-            "r"(smem_addr(dst)),
-        "l"(src), "r"(bytes), "r"(smem_addr(bar))
-        : "memory");
-}
 
 __device__ __forceinline__ void bulk_store(void *dst, const void *src, uint32_t bytes)
 {
@@ -196,7 +144,7 @@ __global__ void __launch_bounds__(kBulkThreadsPerCta, 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kConsumers);
         }
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        mbar_init_fence();
     }
     if (kKvNorm)
         for (int i = threadIdx.x; i < 64; i += blockDim.x)
@@ -313,7 +261,7 @@ __global__ void __launch_bounds__(kBulkThreadsPerCta, 1)
             }
         }
         // make this warp's shared-memory writes visible to the bulk store, then release
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0)
             mbar_arrive(&empty[s]);

@@ -130,23 +130,131 @@ __device__ __forceinline__ ScaleGuess ue8m0_guess(float amax)
     return g;
 }
 
-// Exact decision for near blocks, taken by the whole warp when any block of
-// the KV row of token t is too close to call in fp32.  It reloads the row and
-// the weight (both still cached) rather than keep them live in registers,
-// recomputes the norm in fp64 and evaluates each element in the order of the
-// definition, (x * r) * w, against the boundary 1.75 * 2^e of its block.
-// Returns bit 0: the lane's half-0 block exceeds its boundary; bit 1: the
-// half-1 block does (both already OR-ed over the block's 8 lanes).
-__device__ __noinline__ int exact_scale_bumps(const KParams &p, int lane, int64_t t, int e0,
+// ---- Exact scale decisions in fp32 (float-float arithmetic)
+//
+// A block whose fp32 amax lies within the near band of a boundary B = 1.75 * 2^e
+// needs the exact answer to "does some |x * r * w| of the block exceed B", where
+// r = 1 / sqrt(sum(x^2) / 512 + eps) in exact arithmetic.  As r > 0 that is
+// "max |x * w| * r > B", and |x * w| is exact in fp32 (two 8-bit significands),
+// so the block's question is one comparison.  GB300's fp64 units run at a small
+// fraction of its fp32 rate, so it is first answered in fp32 with error-free
+// transformations, and fp64 is kept for what that cannot settle:
+//   * x^2 of a bf16 value is exact in fp32 when 2^-63 <= |x| < 2^59; the sum of
+//     the squares is accumulated as an unevaluated pair hi + lo (Knuth's
+//     TwoSum, Dekker's Fast2Sum), relative error below 2^-41 for 512 positive
+//     terms;
+//   * r = r0 + r1: r0 = rsqrtf(m), then one Newton step for 1/sqrt(m) with the
+//     residual m * r0^2 - 1 formed exactly by fma (Dekker's TwoProd) and the
+//     series 1 - h/2 + 3h^2/8, relative error below 2^-44 beyond that of m;
+//   * t * r - B, t = max |x * w|, is formed as (t * r0 - B) + (err(t * r0) +
+//     t * r1), where t * r0 - B is exact (Sterbenz) once t * r0 is in [B/2, 2B].
+// Its sign decides when |t * r - B| > 2^-38 B, far above the errors above and
+// those of the fp64 evaluation (about 2^-44), so both give the same answer
+// there.  Anything closer, or any value outside the ranges where the steps are
+// exact, makes the whole warp take the fp64 routine.  Kernels that lay rows out
+// otherwise hand a row with a near block to the whole warp in this layout, so
+// every kernel decides with the same code.
+
+struct FF {
+    float hi, lo;  // value hi + lo, |lo| <= ulp(hi) / 2 after renormalisation
+};
+
+__device__ __forceinline__ FF two_sum(float a, float b)
+{
+    const float s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    return FF{s, __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb))};
+}
+
+// requires |a| >= |b| (or a == 0)
+__device__ __forceinline__ FF fast_two_sum(float a, float b)
+{
+    const float s = __fadd_rn(a, b);
+    return FF{s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+
+__device__ __forceinline__ FF ff_add(FF a, float y)
+{
+    const FF s = two_sum(a.hi, y);
+    return fast_two_sum(s.hi, __fadd_rn(s.lo, a.lo));
+}
+
+__device__ __forceinline__ FF ff_add(FF a, FF b)
+{
+    const FF s = two_sum(a.hi, b.hi);
+    return fast_two_sum(s.hi, __fadd_rn(s.lo, __fadd_rn(a.lo, b.lo)));
+}
+
+__device__ __forceinline__ FF ff_add_xor(FF a, int m)
+{
+    return ff_add(a, FF{__shfl_xor_sync(kFull, a.hi, m), __shfl_xor_sync(kFull, a.lo, m)});
+}
+
+// x^2 exact in fp32 and the sum of 512 of them finite: x = 0 or 2^-63 <= |x| < 2^59
+__device__ __forceinline__ bool square_exact(float x)
+{
+    const uint32_t b = __float_as_uint(x) & 0x7fffffffu;
+    return b == 0u || b - 0x20000000u < 0x3D000000u;
+}
+
+// r = 1 / sqrt(s / 512 + eps) as r.hi + r.lo
+__device__ __forceinline__ FF ff_inv_rms(FF s, float eps, bool &ok)
+{
+    const FF m = ff_add(FF{s.hi * 0x1p-9f, s.lo * 0x1p-9f}, eps);
+    ok = ok && m.hi >= 0x1p-120f && m.hi <= 0x1p120f;
+    const float r0 = rsqrtf(m.hi);
+    const float a = __fmul_rn(r0, r0), b = __fmaf_rn(r0, r0, -a);  // r0^2 = a + b
+    const float c = __fmul_rn(m.hi, a), d = __fmaf_rn(m.hi, a, -c);  // m.hi * a = c + d
+    // h = m * r0^2 - 1 (c - 1 is exact: c is within 2^-20 of 1)
+    const float h = __fadd_rn(__fsub_rn(c, 1.0f), __fadd_rn(d, __fmaf_rn(m.hi, b, __fmul_rn(m.lo, a))));
+    return FF{r0, __fmul_rn(r0, __fmaf_rn(__fmul_rn(0.375f, h), h, __fmul_rn(-0.5f, h)))};
+}
+
+// t * r against B = 1.75 * 2^e for t = max |x * w| of a block (exact in fp32):
+// 1 above, 0 not above, -1 too close to call in fp32 (or outside the ranges
+// where the steps are exact)
+__device__ __forceinline__ int ff_exceeds(float t, FF r, float B)
+{
+    if (!(B >= 0x1p-80f))
+        return -1;
+    if (t == 0.0f)
+        return 0;
+    if (!(t >= 0x1p-100f && t <= 0x1p120f))
+        return -1;
+    const float p = __fmul_rn(t, r.hi);
+    if (p > 2.0f * B)
+        return 1;
+    if (p < 0.5f * B)
+        return 0;
+    const float tail = __fmaf_rn(t, r.lo, __fmaf_rn(t, r.hi, -p));
+    const float d = __fadd_rn(__fsub_rn(p, B), tail);
+    if (fabsf(d) <= B * 0x1p-38f)
+        return -1;
+    return d > 0.0f ? 1 : 0;
+}
+
+// 1.75 * 2^e as fp32 (e is a block amax exponent of a near block, -119..127)
+__device__ __forceinline__ float boundary_f32(int e)
+{
+    return __uint_as_float((uint32_t(e + 127) << 23) | kMant1p75);
+}
+
+// The fp64 decision for near blocks (the fallback of exact_scale_bumps): the
+// norm recomputed in fp64 in the whole-warp order and each element evaluated
+// in the order of the definition, (x * r) * w, against the boundary 1.75 * 2^e
+// of its block.  Same arguments and result as exact_scale_bumps.
+__device__ __noinline__ int exact_scale_bumps_fp64(const KParams &p, int lane, int64_t t, int e0,
                                               bool near0, int e1, bool near1)
 {
-    // rolled loops and scalar loads: this path is rare, its registers are not
-    const uint16_t *row = p.kv + t * kHead;
+    const uint4 *row = reinterpret_cast<const uint4 *>(p.kv + t * kHead);
+    const uint4 *wv = reinterpret_cast<const uint4 *>(p.w);
+    const uint4 xa = __ldg(row + lane), xb = __ldg(row + 32 + lane);
+    const uint4 wa = __ldg(wv + lane), wb = __ldg(wv + 32 + lane);
+    // rolled loops: this path is rare, its registers are not
     double ss = 0.0;
 #pragma unroll 1
     for (int k = 0; k < 16; ++k) {
-        const int d = (k < 8 ? 0 : 248) + 8 * lane + k;
-        const double x = double(__uint_as_float(uint32_t(__ldg(row + d)) << 16));
+        const double x = double(bf16_at(k < 8 ? xa : xb, k & 7));
         ss = __fma_rn(x, x, ss);
     }
     ss = warp_sum(ss);
@@ -157,10 +265,8 @@ __device__ __noinline__ int exact_scale_bumps(const KParams &p, int lane, int64_
         const bool second = k >= 8;
         if (!(second ? near1 : near0))
             continue;
-        const int d = (second ? 248 : 0) + 8 * lane + k;
-        const double x = double(__uint_as_float(uint32_t(__ldg(row + d)) << 16));
-        const double w = double(__uint_as_float(uint32_t(__ldg(p.w + d)) << 16));
-        const double v = __dmul_rn(__dmul_rn(x, r), w);
+        const double v = __dmul_rn(__dmul_rn(double(bf16_at(second ? xb : xa, k & 7)), r),
+                                   double(bf16_at(second ? wb : wa, k & 7)));
         const int e = second ? e1 : e0;
         const double bound = __hiloint2double(int(uint32_t(1023 + e) << 20) | 0x000C0000, 0);
         if (fabs(v) > bound) {
@@ -171,6 +277,57 @@ __device__ __noinline__ int exact_scale_bumps(const KParams &p, int lane, int64_
         }
     }
     return (group8_any(up0) ? 1 : 0) | (group8_any(up1) ? 2 : 0);
+}
+
+// Exact decision for near blocks, taken by the whole warp when any block of
+// the KV row of token t is too close to call in fp32 (lane l holds dims
+// [8l, 8l+8) and [256+8l, 256+8l+8) of the row).  It reloads the lane's two
+// vectors of the row and of the weight (16-byte loads, issued together; the
+// row was just read and is normally still in L2) rather than keep them live
+// in registers, and decides each near block in fp32 float-float arithmetic
+// (above); what that cannot settle goes to the fp64 routine.  Returns bit 0:
+// the lane's half-0 block exceeds its boundary; bit 1: the half-1 block does
+// (the same in the block's 8 lanes).
+__device__ __noinline__ int exact_scale_bumps(const KParams &p, int lane, int64_t t, int e0,
+                                              bool near0, int e1, bool near1)
+{
+    const uint4 *row = reinterpret_cast<const uint4 *>(p.kv + t * kHead);
+    const uint4 *wv = reinterpret_cast<const uint4 *>(p.w);
+    const uint4 xa = __ldg(row + lane), xb = __ldg(row + 32 + lane);
+    const uint4 wa = __ldg(wv + lane), wb = __ldg(wv + 32 + lane);
+    float x[16];
+    widen8(xa, x);
+    widen8(xb, x + 8);
+    // four interleaved chains (the order of a float-float sum only moves its
+    // error, which the margin covers)
+    bool ok = true;
+    FF s4[4] = {FF{0.0f, 0.0f}, FF{0.0f, 0.0f}, FF{0.0f, 0.0f}, FF{0.0f, 0.0f}};
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        ok = ok && square_exact(x[k]);
+        s4[k & 3] = ff_add(s4[k & 3], __fmul_rn(x[k], x[k]));
+    }
+    FF s = ff_add(ff_add(s4[0], s4[1]), ff_add(s4[2], s4[3]));
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1)
+        s = ff_add_xor(s, m);
+    const FF r = ff_inv_rms(s, p.eps, ok);
+    float w[16];
+    widen8(wa, w);
+    widen8(wb, w + 8);
+    float t0 = 0.0f, t1 = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        t0 = fmaxf(t0, fabsf(__fmul_rn(x[k], w[k])));
+        t1 = fmaxf(t1, fabsf(__fmul_rn(x[8 + k], w[8 + k])));
+    }
+    t0 = group8_max(t0);
+    t1 = group8_max(t1);
+    const int res0 = near0 ? ff_exceeds(t0, r, boundary_f32(e0)) : 0;
+    const int res1 = near1 ? ff_exceeds(t1, r, boundary_f32(e1)) : 0;
+    if (__any_sync(kFull, !ok || res0 < 0 || res1 < 0))
+        return exact_scale_bumps_fp64(p, lane, t, e0, near0, e1, near1);
+    return (res0 > 0 ? 1 : 0) | (res1 > 0 ? 2 : 0);
 }
 
 __device__ __forceinline__ int clamp_s(int s)

@@ -295,11 +295,11 @@ def test_fast_division_identity(d):
 
 
 def test_launch_plan_for_kv_rows_only_stream():
-    """With no q heads STREAM runs the KV-row kernel: 2 rows per warp (one per half)."""
-    plan = k.launch_plan(100000, 0, 152, 3, k.VARIANT_STREAM)
-    assert plan.rows_per_warp == 2 and plan.threads == 256 and plan.ctas == 152 * 3
-    plan = k.launch_plan(100, 0, 152, 3, k.VARIANT_STREAM)
-    assert plan.ctas == 7  # 50 row pairs, 8 warps per CTA
+    """With no q heads STREAM runs the KV-row kernel: 4 rows per warp (one per quarter)."""
+    plan = k.launch_plan(100000, 0, 152, 2, k.VARIANT_STREAM)
+    assert plan.rows_per_warp == 4 and plan.threads == 256 and plan.ctas == 152 * 2
+    plan = k.launch_plan(100, 0, 152, 2, k.VARIANT_STREAM)
+    assert plan.ctas == 4  # 25 groups of four rows, 8 warps per CTA
     plan = k.launch_plan(100000, 8, 152, 3, k.VARIANT_STREAM)
     assert plan.rows_per_warp == 3
 

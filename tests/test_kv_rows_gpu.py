@@ -1,9 +1,9 @@
-"""The KV-row kernel (calls with no q heads, one row per half-warp) on the GPU.
+"""The KV-row kernel (calls with no q heads, one row per quarter-warp) on the GPU.
 
 Its cache rows must be bit-identical to those the fused kernel writes for the
 same KV inputs (same sums, same butterfly, same elementwise operations, same
 exact decision near a scale boundary), and must meet the oracle's parity bar
-on their own, including pairs in which one half-warp's row is skipped.
+on their own, including warps in which some quarter-warps' rows are skipped.
 """
 import dataclasses
 
@@ -69,9 +69,10 @@ def test_scale_decisions_near_boundaries_kv_only():
 
 
 @pytest.mark.parametrize("store", ["fp8", "bf16"])
-def test_half_pairs_with_one_side_skipped(store):
+def test_quads_with_rows_skipped(store):
     """Tokens alternate between written and skipped rows (negative slot, slot past the
-    cache, position outside the table), so many half-warp pairs have one idle half."""
+    cache, position outside the table), so many warps' groups of four rows have one to
+    three idle quarters, and a few groups are skipped whole."""
     T = 3003
     wl = configs.generic(T, 0, store=store, seed=80, skip_frac=0.0)
     base = harness.make_inputs(wl)
@@ -81,6 +82,8 @@ def test_half_pairs_with_one_side_skipped(store):
     slots[2::8] = wl.num_slots + 7
     pos[3::8] = wl.max_position + 1
     pos[7::16] = -5
+    slots[20:24] = -1
+    slots[1000:1004] = -1
     inp = dataclasses.replace(base, slots=slots, positions=pos)
     gpu = harness.run_gpu(inp, k.VARIANT_STREAM)
     ref_q, ref_cache, ref_err = harness.run_oracle(inp)
