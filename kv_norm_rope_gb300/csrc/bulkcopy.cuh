@@ -5,9 +5,7 @@
 // Every wait is bounded: it polls the barrier with try_wait (which blocks
 // for a short, system-defined time per try) and gives up after kWaitCycles SM
 // clock cycles (about one second at 2 GHz), returning false so that the
-// caller can flag the error, let its copies in flight land and leave.  No
-// suspend-time hint is given: with one (20 us) some waits measured on GB300
-// slept 10-20 us past the completion of their phase.
+// caller can flag the error, let its copies in flight land and leave.
 #pragma once
 
 #include <cuda_runtime.h>
