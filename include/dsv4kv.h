@@ -333,6 +333,19 @@ int dsv4_indexer_k_gather(const uint8_t *indexer_cache, int64_t num_blocks, int3
 /* Bytes of an indexer cache of num_blocks x block_size slots: num_blocks*block_size*132. */
 size_t dsv4_indexer_cache_bytes(int64_t num_blocks, int32_t block_size);
 
+/*
+ * Check of the failure path of the bulk-copy kernels (DSV4_VARIANT_BULK and the
+ * KV-row kernel): their waits on mbarriers give up after a budget of SM clock
+ * cycles instead of waiting without bound.  This launches one warp that waits,
+ * through the same code, on an mbarrier whose phase nothing completes.  After
+ * max_cycles cycles (0, or anything above the kernels' own limit of 2^31 cycles,
+ * about one second at 2 GHz: that limit) it ORs DSV4_DEVERR_TIMEOUT into
+ * *device_error (device int32, nullable) and returns; the GPU context stays
+ * usable.  Asynchronous on `stream` (cudaStream_t).  Returns DSV4_ERR_VALUE for
+ * max_cycles < 0, DSV4_ERR_CUDA if the launch fails, else DSV4_OK.
+ */
+int dsv4_check_bounded_wait(int64_t max_cycles, int32_t *device_error, void *stream);
+
 /* Static string naming a dsv4_status value ("unknown status" otherwise). */
 const char *dsv4_status_string(int status);
 

@@ -22,6 +22,7 @@ _INCLUDE = os.path.join(_ROOT, "include")
 LIB_PATH = os.path.join(_HERE, "libdsv4kv.so")
 _SOURCES = ["qnorm_rope_kv_insert.cu", "qnorm_rope_kv_insert_bulk.cu", "dequant_gather.cu",
             "gemma_rmsnorm_mxfp8.cu", "indexer_k.cu", "kv_rows.cu", "qnorm_rope_kv_insert_half.cu",
+            "wait_check.cu",
             "api.cpp"]
 _HEADERS = [os.path.join(_INCLUDE, "dsv4kv.h")] + [
     os.path.join(_CSRC, h)
@@ -41,7 +42,8 @@ EXPORTS = ("dsv4_qnorm_rope_kv_quant_insert", "dsv4_qnorm_rope_kv_bf16_insert",
            "dsv4_kv_norm_rope_insert", "dsv4_insert_ex", "dsv4_dequant_gather",
            "dsv4_add_gemma_rmsnorm_mxfp8", "dsv4_mxfp8_scale_bytes", "dsv4_launch_plan",
            "dsv4_fp8_cache_bytes", "dsv4_bf16_cache_bytes", "dsv4_indexer_k_quant_insert",
-           "dsv4_indexer_k_gather", "dsv4_indexer_cache_bytes", "dsv4_status_string")
+           "dsv4_indexer_k_gather", "dsv4_indexer_cache_bytes", "dsv4_check_bounded_wait",
+           "dsv4_status_string")
 
 
 class Dsv4Error(RuntimeError):
@@ -138,6 +140,8 @@ def lib():
         L.dsv4_indexer_k_gather.restype = c_int
         L.dsv4_indexer_cache_bytes.argtypes = [i64, i32]
         L.dsv4_indexer_cache_bytes.restype = ctypes.c_size_t
+        L.dsv4_check_bounded_wait.argtypes = [i64, vp, vp]
+        L.dsv4_check_bounded_wait.restype = c_int
         L.dsv4_status_string.argtypes = [c_int]
         L.dsv4_status_string.restype = ctypes.c_char_p
         _lib = L
@@ -352,6 +356,19 @@ def dequant_gather(kv_cache, num_blocks: int, block_size: int, slots, out, devic
                                    _stream_handle(stream))
     if st != OK:
         raise Dsv4Error(st, "dsv4_dequant_gather")
+
+
+def check_bounded_wait(max_cycles: int = 0, device_error=None, stream=None) -> None:
+    """dsv4_check_bounded_wait: one warp waits, through the bulk-copy kernels' bounded
+    wait, on an mbarrier nothing completes; after max_cycles SM cycles (0: the kernels'
+    own limit, about a second) it ORs DEVERR_TIMEOUT into device_error (int32 [1])."""
+    if max_cycles < 0:
+        raise ValueError("max_cycles must be >= 0")
+    _check("device_error", device_error, "i32")
+    _on_cuda(device_error=device_error)
+    st = lib().dsv4_check_bounded_wait(int(max_cycles), _ptr(device_error), _stream_handle(stream))
+    if st != OK:
+        raise Dsv4Error(st, "dsv4_check_bounded_wait")
 
 
 def indexer_cache_bytes(num_blocks: int, block_size: int) -> int:

@@ -452,6 +452,13 @@ size_t dsv4_bf16_cache_bytes(int64_t num_blocks, int32_t block_size)
     return size_t(num_blocks) * size_t(block_size) * DSV4_BF16_SLOT_BYTES;
 }
 
+int dsv4_check_bounded_wait(int64_t max_cycles, int32_t *device_error, void *stream)
+{
+    if (max_cycles < 0)
+        return DSV4_ERR_VALUE;
+    return dsv4::launch_wait_check(max_cycles, device_error, static_cast<cudaStream_t>(stream));
+}
+
 const char *dsv4_status_string(int status)
 {
     switch (status) {

@@ -44,9 +44,10 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
-// wait for the completion of the phase with the given parity; false if the
-// bounded number of tries ran out
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
+// wait for the completion of the phase with the given parity; false once
+// max_cycles SM clock cycles have passed without it
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
+                                          long long max_cycles = kWaitCycles)
 {
     const long long t0 = clock64();
     for (;;) {
@@ -59,7 +60,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
                      : "memory");
         if (done)
             return true;
-        if (clock64() - t0 > kWaitCycles)
+        if (clock64() - t0 > max_cycles)
             return false;
     }
 }

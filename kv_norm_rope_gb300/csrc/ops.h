@@ -1,8 +1,9 @@
 // Internal interface between the C-ABI layer (api.cpp) and the kernels of the
 // operations beside the whole-warp fused kernels: the half-warp fused kernel
 // (qnorm_rope_kv_insert_half.cu), the KV-row kernel for calls with no q
-// (kv_rows.cu), the MXFP8 activation quantiser (gemma_rmsnorm_mxfp8.cu) and the
-// indexer-K insert and gather (indexer_k.cu).
+// (kv_rows.cu), the MXFP8 activation quantiser (gemma_rmsnorm_mxfp8.cu), the
+// indexer-K insert and gather (indexer_k.cu) and the check of the bounded waits
+// (wait_check.cu).
 // Not installed; not part of the ABI.
 #pragma once
 
@@ -37,5 +38,9 @@ int launch_indexer_insert(const uint16_t *k, const int64_t *slots, uint8_t *cach
 int launch_indexer_gather(const uint8_t *cache, int64_t num_blocks, int32_t block_size,
                           const int64_t *slots, int64_t rows, uint8_t *k_out, float *scale_out,
                           int32_t *err, int64_t max_ctas, cudaStream_t stream);
+
+// One warp waits on an mbarrier nothing completes, for at most max_cycles SM
+// cycles (clamped to the kernels' own limit), then flags DSV4_DEVERR_TIMEOUT.
+int launch_wait_check(int64_t max_cycles, int32_t *err, cudaStream_t stream);
 
 }  // namespace dsv4

@@ -361,3 +361,10 @@ def test_every_export_is_documented():
                  "add_gemma_rmsnorm_mxfp8"):
         assert f"`{name}`" in readme or f"k.{name}(" in readme, name
         assert callable(getattr(k, name))
+
+
+def test_bounded_wait_check_rejects_negative_budget():
+    lib = k.lib()
+    assert lib.dsv4_check_bounded_wait(-1, None, None) == k.ERR_VALUE
+    with pytest.raises(ValueError):
+        k.check_bounded_wait(-5)

@@ -74,3 +74,22 @@ def test_rejected_call_launches_nothing():
     assert ex.value.status == k.ERR_VALUE
     torch.cuda.synchronize()
     assert bool((cache == 0x5A).all()) and bool((q == 1).all())
+
+
+def test_bounded_wait_runs_out_and_reports():
+    """A wait that nothing completes gives up after its cycle budget, ORs the timeout bit
+    into the error word and returns; the context stays usable for the next launch."""
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    k.check_bounded_wait(1 << 24, err)  # ~8 ms at 2 GHz
+    t1.record()
+    torch.cuda.synchronize()
+    assert int(err.item()) == k.DEVERR_TIMEOUT
+    ms = t0.elapsed_time(t1)
+    assert 1e3 * (1 << 24) / 2.2e9 <= ms < 1000.0, ms
+    # the kernels' own limit (about a second), with no error word
+    k.check_bounded_wait(0, None)
+    torch.cuda.synchronize()
+    rep = harness.check(configs.TINY)
+    assert rep.ok, str(rep)
