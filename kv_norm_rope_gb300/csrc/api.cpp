@@ -208,9 +208,13 @@ int dsv4_launch_plan(int64_t num_tokens, int32_t num_heads, int32_t sm_count, in
         // half-warp kernel beats both the others up to 12 rounds of the stream
         // kernel's 3-row groups (3-35% at 2K-100K rows, a tie near 130K-200K);
         // beyond, the whole-warp stream (2.5% ahead from ~260K rows).  With no q
-        // heads, STREAM runs the KV-row kernel, ahead of SMALL from ~2K rows.
+        // heads, STREAM runs the KV-row kernel, whose bulk-copy pipeline costs
+        // ~1.7 us more to start: SMALL is ahead up to ~2.4K rows (two thirds of
+        // the warp slots), the KV-row kernel from there (by 20% at 4K rows, 2x at
+        // 64K).
         const int64_t round = warp_slots * dsv4::kStreamRowsPerWarp;
-        variant = rows < warp_slots / 4                   ? DSV4_VARIANT_SMALL
+        const int64_t small_below = num_heads > 0 ? warp_slots / 4 : 2 * warp_slots / 3;
+        variant = rows < small_below                      ? DSV4_VARIANT_SMALL
                   : num_heads > 0 && rows < 12 * round    ? DSV4_VARIANT_HALF
                                                           : DSV4_VARIANT_STREAM;
     }
