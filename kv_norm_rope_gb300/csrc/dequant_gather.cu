@@ -9,10 +9,13 @@
 // HBM-bound: per row 584 bytes read and 1024 written.  One warp per row with
 // the insert kernels' lane layout (lane l: dims [8l, 8l+8) and [256+8l,
 // 256+8l+8)), so each 8-byte load instruction covers 256 contiguous cache
-// bytes and each 16-byte store 512 contiguous output bytes; several rows per
-// warp are loaded back to back before any is used.  Every value is exact:
-// an E4M3 code times a power of two fits fp32 for every scale the writer
-// emits, so the one rounding is the final bf16 conversion.
+// bytes and each 16-byte store 512 contiguous output bytes.  A warp takes
+// groups of kGatherRows rows and keeps the next group's loads in flight
+// while it converts and stores the current one (software pipelining in
+// registers): the slot ids are loaded two groups ahead, the rows one group
+// ahead.  Every value is exact: an E4M3 code times a power of two fits fp32
+// for every scale the writer emits, so the one rounding is the final bf16
+// conversion.
 
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -25,7 +28,7 @@
 namespace dsv4 {
 namespace {
 
-constexpr int kGatherRows = 4;
+constexpr int kGatherRows = 1;  // rows per group: 1-4 measured, 1 best (40 registers, 6 CTAs per SM)
 
 struct GParams {
     const uint8_t *cache;
@@ -68,63 +71,99 @@ __device__ __forceinline__ uint2 ld8(const uint8_t *p)
     return __ldcs(reinterpret_cast<const uint2 *>(p));
 }
 
+// one group of rows as loaded by one lane
+struct Group {
+    int64_t slot[kGatherRows];
+    uint2 lo[kGatherRows], hi0[kGatherRows], hi1[kGatherRows], sc[kGatherRows];
+};
+
+// slot ids of group g (-1 past the end, so nothing is read for them)
+__device__ __forceinline__ void load_slots(const GParams &p, int64_t g, int64_t *slot)
+{
+#pragma unroll
+    for (int j = 0; j < kGatherRows; ++j) {
+        const int64_t r = g * kGatherRows + j;
+        slot[j] = r < p.rows ? __ldg(p.slots + r) : -1;
+    }
+}
+
+// issue the lane's loads of the rows at `slot` (zeros for rows that read nothing)
+__device__ __forceinline__ void load_rows(const GParams &p, int lane, Group &q)
+{
+    const bool rope_lane = lane >= 24;
+#pragma unroll
+    for (int j = 0; j < kGatherRows; ++j) {
+        q.lo[j] = q.hi0[j] = q.hi1[j] = q.sc[j] = make_uint2(0u, 0u);
+        const int64_t slot = q.slot[j];
+        if (slot >= 0 && slot < p.num_slots) {
+            const int64_t blk = fastdiv(static_cast<uint32_t>(slot), p.slot_div);
+            const int64_t off = slot - blk * p.block_size;
+            const uint8_t *base = p.cache + blk * int64_t(p.block_size) * DSV4_FP8_SLOT_BYTES;
+            const uint8_t *data = base + off * DSV4_FP8_DATA_BYTES;
+            q.lo[j] = ld8(data + 8 * lane);
+            if (!rope_lane) {
+                q.hi0[j] = ld8(data + 256 + 8 * lane);
+            } else {
+                q.hi0[j] = ld8(data + DSV4_NOPE_DIM + 16 * (lane - 24));
+                q.hi1[j] = ld8(data + DSV4_NOPE_DIM + 16 * (lane - 24) + 8);
+            }
+            q.sc[j] = __ldg(reinterpret_cast<const uint2 *>(
+                base + int64_t(p.block_size) * DSV4_FP8_DATA_BYTES + off * DSV4_FP8_SCALE_BYTES));
+        }
+    }
+}
+
+// convert and store group g
+__device__ __forceinline__ void emit_rows(const GParams &p, int lane, int64_t g, const Group &q)
+{
+    const bool rope_lane = lane >= 24;
+    const int64_t r0 = g * kGatherRows;
+#pragma unroll
+    for (int j = 0; j < kGatherRows; ++j) {
+        if (r0 + j >= p.rows)
+            break;
+        uint16_t *row = p.out + (r0 + j) * DSV4_HEAD_DIM;
+        uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
+        if (q.slot[j] >= p.num_slots) {
+            if (lane == 0 && p.err != nullptr)
+                atomicOr(p.err, DSV4_DEVERR_SLOT_RANGE);
+        } else if (q.slot[j] >= 0) {
+            // scale byte of block lane/8 (half 0) and 4 + lane/8 (half 1)
+            const int b0 = lane >> 3, b1 = 4 + (lane >> 3);
+            const uint32_t e0 = (q.sc[j].x >> (8 * b0)) & 0xFFu;
+            const uint32_t e1 = (q.sc[j].y >> (8 * (b1 - 4))) & 0xFFu;
+            a = dequant8(q.lo[j], e0);
+            b = rope_lane ? make_uint4(q.hi0[j].x, q.hi0[j].y, q.hi1[j].x, q.hi1[j].y)
+                          : dequant8(q.hi0[j], e1);
+        }
+        __stcs(reinterpret_cast<uint4 *>(row + 8 * lane), a);
+        __stcs(reinterpret_cast<uint4 *>(row + 256 + 8 * lane), b);
+    }
+}
+
 __global__ void __launch_bounds__(256) dequant_gather_kernel(const GParams p)
 {
     const int lane = threadIdx.x & 31;
     const int warps_per_cta = blockDim.x >> 5;
     const int64_t groups = (p.rows + kGatherRows - 1) / kGatherRows;
     const int64_t stride = int64_t(gridDim.x) * warps_per_cta;
-    const bool rope_lane = lane >= 24;
-
-    for (int64_t g = int64_t(blockIdx.x) * warps_per_cta + (threadIdx.x >> 5); g < groups;
-         g += stride) {
-        const int64_t r0 = g * kGatherRows;
-        int64_t slot[kGatherRows];
+    int64_t g = int64_t(blockIdx.x) * warps_per_cta + (threadIdx.x >> 5);
+    if (g >= groups)
+        return;
+    Group cur;
+    load_slots(p, g, cur.slot);
+    load_rows(p, lane, cur);
+    int64_t ahead[kGatherRows];  // slot ids of the group after the next one
+    load_slots(p, g + stride, ahead);
+    for (; g < groups; g += stride) {
+        Group nxt;
 #pragma unroll
         for (int j = 0; j < kGatherRows; ++j)
-            slot[j] = r0 + j < p.rows ? __ldg(p.slots + r0 + j) : -1;
-        // all loads of the group back to back
-        uint2 lo[kGatherRows], hi0[kGatherRows], hi1[kGatherRows], sc[kGatherRows];
-#pragma unroll
-        for (int j = 0; j < kGatherRows; ++j) {
-            lo[j] = hi0[j] = hi1[j] = sc[j] = make_uint2(0u, 0u);
-            if (slot[j] >= 0 && slot[j] < p.num_slots) {
-                const int64_t blk = fastdiv(static_cast<uint32_t>(slot[j]), p.slot_div);
-                const int64_t off = slot[j] - blk * p.block_size;
-                const uint8_t *base = p.cache + blk * int64_t(p.block_size) * DSV4_FP8_SLOT_BYTES;
-                const uint8_t *data = base + off * DSV4_FP8_DATA_BYTES;
-                lo[j] = ld8(data + 8 * lane);
-                if (!rope_lane) {
-                    hi0[j] = ld8(data + 256 + 8 * lane);
-                } else {
-                    hi0[j] = ld8(data + DSV4_NOPE_DIM + 16 * (lane - 24));
-                    hi1[j] = ld8(data + DSV4_NOPE_DIM + 16 * (lane - 24) + 8);
-                }
-                sc[j] = __ldg(reinterpret_cast<const uint2 *>(
-                    base + int64_t(p.block_size) * DSV4_FP8_DATA_BYTES + off * DSV4_FP8_SCALE_BYTES));
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < kGatherRows; ++j) {
-            if (r0 + j >= p.rows)
-                break;
-            uint16_t *row = p.out + (r0 + j) * DSV4_HEAD_DIM;
-            uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
-            if (slot[j] >= p.num_slots) {
-                if (lane == 0 && p.err != nullptr)
-                    atomicOr(p.err, DSV4_DEVERR_SLOT_RANGE);
-            } else if (slot[j] >= 0) {
-                // scale byte of block lane/8 (half 0) and 4 + lane/8 (half 1)
-                const int b0 = lane >> 3, b1 = 4 + (lane >> 3);
-                const uint32_t e0 = (b0 < 4 ? sc[j].x >> (8 * b0) : 0u) & 0xFFu;
-                const uint32_t e1 = (sc[j].y >> (8 * (b1 - 4))) & 0xFFu;
-                a = dequant8(lo[j], e0);
-                b = rope_lane ? make_uint4(hi0[j].x, hi0[j].y, hi1[j].x, hi1[j].y)
-                              : dequant8(hi0[j], e1);
-            }
-            __stcs(reinterpret_cast<uint4 *>(row + 8 * lane), a);
-            __stcs(reinterpret_cast<uint4 *>(row + 256 + 8 * lane), b);
-        }
+            nxt.slot[j] = ahead[j];
+        load_rows(p, lane, nxt);  // nothing is read for a group past the end
+        load_slots(p, g + 2 * stride, ahead);
+        emit_rows(p, lane, g, cur);
+        cur = nxt;
     }
 }
 
