@@ -63,7 +63,8 @@ int device_shape(int store_mode, int32_t *sms, int32_t *ctas)
 
 // CTAs per SM of the reader and indexer kernels, cached per device beside the
 // SM count; resident = SMs x CTAs per SM, the cap of their persistent grids.
-enum { kOccGather = 0, kOccIndexer = 1, kOccKvRows = 2, kOccHalf = 3, kOccKinds = 4 };
+enum { kOccGather = 0, kOccIndexer = 1, kOccKvRows = 2, kOccHalf = 3, kOccIndexerGather = 4,
+       kOccKinds = 5 };
 std::atomic<int32_t> g_occ[kMaxDevices][kOccKinds];
 
 int resident_ctas(int kind, int64_t *resident)
@@ -83,7 +84,8 @@ int resident_ctas(int kind, int64_t *resident)
     }
     if (per < 1) {
         const int rc = kind == kOccGather    ? dsv4::gather_ctas_per_sm(&per)
-                       : kind == kOccIndexer ? dsv4::indexer_ctas_per_sm(&per)
+                       : kind == kOccIndexer ? dsv4::indexer_ctas_per_sm(&per, false)
+                       : kind == kOccIndexerGather ? dsv4::indexer_ctas_per_sm(&per, true)
                        : kind == kOccKvRows  ? dsv4::kv_rows_ctas_per_sm(&per)
                                              : dsv4::half_ctas_per_sm(&per);
         if (rc != DSV4_OK || per < 1)
@@ -428,7 +430,7 @@ int dsv4_indexer_k_gather(const uint8_t *indexer_cache, int64_t num_blocks, int3
         !aligned(scale_out, 4) || !aligned(device_error, 4))
         return DSV4_ERR_ALIGN;
     int64_t resident = 0;
-    if (resident_ctas(kOccIndexer, &resident) != DSV4_OK)
+    if (resident_ctas(kOccIndexerGather, &resident) != DSV4_OK)
         return DSV4_ERR_CUDA;
     return dsv4::launch_indexer_gather(indexer_cache, num_blocks, block_size, slots, num_rows,
                                        k_out, scale_out, device_error, resident,

@@ -21,7 +21,8 @@
 // point: for non-negative bf16 bit patterns integer order is magnitude order,
 // so amax is an integer max of (bits & 0x7fff), and with amax = (1 + m/128) *
 // 2^(E - 127), s = E - 135 + (m > 0x60) (the mantissa above 1.75 = 448 / 256).
-// Each warp loads kPairs row pairs before it uses any of them.
+// The insert loads kPairs row pairs per warp before it uses any of them; the
+// gather is software-pipelined (below).
 
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -142,68 +143,112 @@ __global__ void __launch_bounds__(kThreads) indexer_k_insert_kernel(const IParam
     }
 }
 
+// The gather, software-pipelined in registers: a warp takes groups of
+// kGatherPairs row pairs (one row per half) and keeps the next group's loads
+// in flight while it stores the current one; the slot ids are loaded two
+// groups ahead, the codes and scales one group ahead.
+constexpr int kGatherPairs = 2;  // 1-4 measured: 2 best (48 registers)
+
+__device__ __forceinline__ void gather_slots(const IParams &p, int64_t g, int half, int64_t *slot)
+{
+#pragma unroll
+    for (int j = 0; j < kGatherPairs; ++j) {
+        const int64_t n = g * 2 * kGatherPairs + half + 2 * j;
+        slot[j] = n < p.rows ? __ldg(p.slots + n) : -1;
+    }
+}
+
+template <bool kWide>
+__device__ __forceinline__ void gather_load(const IParams &p, int h, const int64_t *slot, uint2 *c,
+                                            unsigned *sc)
+{
+#pragma unroll
+    for (int j = 0; j < kGatherPairs; ++j) {
+        c[j] = make_uint2(0u, 0u);
+        sc[j] = 0u;
+        if (slot[j] >= 0 && slot[j] < p.num_slots) {
+            const int64_t blk = fastdiv(static_cast<uint32_t>(slot[j]), p.slot_div);
+            const int64_t off = slot[j] - blk * p.block_size;
+            const uint8_t *base = p.src + blk * int64_t(p.block_size) * kSlotBytes;
+            c[j] = load_codes<kWide>(base + off * kDim + 8 * h);
+            if (h == 0)
+                sc[j] = __ldcs(reinterpret_cast<const unsigned *>(
+                    base + int64_t(p.block_size) * kDim + off * 4));
+        }
+    }
+}
+
+__device__ __forceinline__ void gather_store(const IParams &p, int h, int half, int64_t g,
+                                             const int64_t *slot, const uint2 *c, const unsigned *sc)
+{
+#pragma unroll
+    for (int j = 0; j < kGatherPairs; ++j) {
+        const int64_t n = g * 2 * kGatherPairs + half + 2 * j;
+        if (n >= p.rows)
+            continue;
+        if (slot[j] >= p.num_slots && h == 0 && p.err != nullptr)
+            atomicOr(p.err, DSV4_DEVERR_SLOT_RANGE);
+        __stcs(reinterpret_cast<uint2 *>(p.k_out + n * kDim) + h, c[j]);
+        if (h == 0)
+            __stcs(reinterpret_cast<unsigned *>(p.scale_out) + n, sc[j]);
+    }
+}
+
 template <bool kWide>
 __global__ void __launch_bounds__(kThreads) indexer_k_gather_kernel(const IParams p)
 {
     const int lane = threadIdx.x & 31, half = lane >> 4, h = lane & 15;
     const int64_t warps = int64_t(gridDim.x) * (kThreads / 32);
-    const int64_t groups = (p.rows + 2 * kPairs - 1) / (2 * kPairs);
-    for (int64_t g = int64_t(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5); g < groups;
-         g += warps) {
-        const int64_t n0 = g * 2 * kPairs + half;
-        int64_t slot[kPairs];
+    const int64_t groups = (p.rows + 2 * kGatherPairs - 1) / (2 * kGatherPairs);
+    int64_t g = int64_t(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5);
+    if (g >= groups)
+        return;
+    int64_t slot[kGatherPairs], ahead[kGatherPairs];
+    uint2 c[kGatherPairs];
+    unsigned sc[kGatherPairs];
+    gather_slots(p, g, half, slot);
+    gather_load<kWide>(p, h, slot, c, sc);
+    gather_slots(p, g + warps, half, ahead);
+    for (; g < groups; g += warps) {
+        int64_t slot_n[kGatherPairs];
+        uint2 c_n[kGatherPairs];
+        unsigned sc_n[kGatherPairs];
 #pragma unroll
-        for (int j = 0; j < kPairs; ++j)
-            slot[j] = n0 + 2 * j < p.rows ? __ldg(p.slots + n0 + 2 * j) : -1;
-        uint2 c[kPairs];
-        unsigned sc[kPairs];
+        for (int j = 0; j < kGatherPairs; ++j)
+            slot_n[j] = ahead[j];
+        gather_load<kWide>(p, h, slot_n, c_n, sc_n);  // nothing is read past the end
+        gather_slots(p, g + 2 * warps, half, ahead);
+        gather_store(p, h, half, g, slot, c, sc);
 #pragma unroll
-        for (int j = 0; j < kPairs; ++j) {
-            c[j] = make_uint2(0u, 0u);
-            sc[j] = 0u;
-            if (slot[j] >= 0 && slot[j] < p.num_slots) {
-                const int64_t blk = fastdiv(static_cast<uint32_t>(slot[j]), p.slot_div);
-                const int64_t off = slot[j] - blk * p.block_size;
-                const uint8_t *base = p.src + blk * int64_t(p.block_size) * kSlotBytes;
-                c[j] = load_codes<kWide>(base + off * kDim + 8 * h);
-                if (h == 0)
-                    sc[j] = __ldcs(reinterpret_cast<const unsigned *>(
-                        base + int64_t(p.block_size) * kDim + off * 4));
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < kPairs; ++j) {
-            const int64_t n = n0 + 2 * j;
-            if (n >= p.rows)
-                continue;
-            if (slot[j] >= p.num_slots && h == 0 && p.err != nullptr)
-                atomicOr(p.err, DSV4_DEVERR_SLOT_RANGE);
-            __stcs(reinterpret_cast<uint2 *>(p.k_out + n * kDim) + h, c[j]);
-            if (h == 0)
-                __stcs(reinterpret_cast<unsigned *>(p.scale_out) + n, sc[j]);
+        for (int j = 0; j < kGatherPairs; ++j) {
+            slot[j] = slot_n[j];
+            c[j] = c_n[j];
+            sc[j] = sc_n[j];
         }
     }
 }
 
-int64_t grid_for(int64_t rows, int64_t max_ctas)
+int64_t grid_for(int64_t rows, int64_t max_ctas, int pairs)
 {
-    const int64_t groups = (rows + 2 * kPairs - 1) / (2 * kPairs);
+    const int64_t groups = (rows + 2 * pairs - 1) / (2 * pairs);
     const int64_t need = (groups + kThreads / 32 - 1) / (kThreads / 32);
     return need < max_ctas ? need : max_ctas;
 }
 
 }  // namespace
 
-int indexer_ctas_per_sm(int *ctas_per_sm)
+int indexer_ctas_per_sm(int *ctas_per_sm, bool gather)
 {
-    // the four kernels use the same block size; take the smallest occupancy
-    int a = 0, b = 0, c = 0, d = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, indexer_k_insert_kernel<true>, kThreads, 0) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, indexer_k_insert_kernel<false>, kThreads, 0) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c, indexer_k_gather_kernel<true>, kThreads, 0) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d, indexer_k_gather_kernel<false>, kThreads, 0) != cudaSuccess)
+    // each kernel's two forms use the same block size; take the smaller occupancy
+    int a = 0, b = 0;
+    const bool ok =
+        gather ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, indexer_k_gather_kernel<true>, kThreads, 0) == cudaSuccess &&
+                     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, indexer_k_gather_kernel<false>, kThreads, 0) == cudaSuccess
+               : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, indexer_k_insert_kernel<true>, kThreads, 0) == cudaSuccess &&
+                     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, indexer_k_insert_kernel<false>, kThreads, 0) == cudaSuccess;
+    if (!ok)
         return DSV4_ERR_CUDA;
-    *ctas_per_sm = min(min(a, b), min(c, d));
+    *ctas_per_sm = min(a, b);
     return DSV4_OK;
 }
 
@@ -220,7 +265,7 @@ int launch_indexer_insert(const uint16_t *k, const int64_t *slots, uint8_t *cach
     p.block_size = block_size;
     p.slot_div = fastdiv_magic(static_cast<uint32_t>(block_size));
     p.err = err;
-    const unsigned grid = static_cast<unsigned>(grid_for(rows, max_ctas));
+    const unsigned grid = static_cast<unsigned>(grid_for(rows, max_ctas, kPairs));
     const bool wide = (reinterpret_cast<uintptr_t>(cache) & 7u) == 0 && block_size % 2 == 0;
     return launch_kernel(wide ? indexer_k_insert_kernel<true> : indexer_k_insert_kernel<false>,
                          dim3(grid), dim3(kThreads), 0, stream, p);
@@ -240,7 +285,7 @@ int launch_indexer_gather(const uint8_t *cache, int64_t num_blocks, int32_t bloc
     p.block_size = block_size;
     p.slot_div = fastdiv_magic(static_cast<uint32_t>(block_size));
     p.err = err;
-    const unsigned grid = static_cast<unsigned>(grid_for(rows, max_ctas));
+    const unsigned grid = static_cast<unsigned>(grid_for(rows, max_ctas, kGatherPairs));
     const bool wide = (reinterpret_cast<uintptr_t>(cache) & 7u) == 0 && block_size % 2 == 0;
     return launch_kernel(wide ? indexer_k_gather_kernel<true> : indexer_k_gather_kernel<false>,
                          dim3(grid), dim3(kThreads), 0, stream, p);

@@ -31,7 +31,7 @@ int launch_gemma_rmsnorm_mxfp8(const uint16_t *x, const uint16_t *residual, cons
                                uint8_t *codes, uint8_t *scales, cudaStream_t stream);
 
 // Indexer-K quant-insert and gather; grids are capped at max_ctas.
-int indexer_ctas_per_sm(int *ctas_per_sm);
+int indexer_ctas_per_sm(int *ctas_per_sm, bool gather);
 int launch_indexer_insert(const uint16_t *k, const int64_t *slots, uint8_t *cache,
                           int64_t num_blocks, int32_t block_size, int64_t rows, int32_t *err,
                           int64_t max_ctas, cudaStream_t stream);
