@@ -21,8 +21,8 @@
 // point: for non-negative bf16 bit patterns integer order is magnitude order,
 // so amax is an integer max of (bits & 0x7fff), and with amax = (1 + m/128) *
 // 2^(E - 127), s = E - 135 + (m > 0x60) (the mantissa above 1.75 = 448 / 256).
-// The insert loads kPairs row pairs per warp before it uses any of them; the
-// gather is software-pipelined (below).
+// Both kernels are software-pipelined in registers: a warp's next group of
+// row pairs is loaded before it stores the current one.
 
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -37,7 +37,7 @@ namespace {
 
 constexpr int kDim = DSV4_INDEXER_DIM;                // 128 dims, 256 bf16 bytes
 constexpr int kSlotBytes = DSV4_INDEXER_SLOT_BYTES;   // 128 codes + 4 scale bytes
-constexpr int kPairs = 4;                             // row pairs a warp loads together
+constexpr int kPairs = 2;  // row pairs per insert group: 1, 2, 4 measured, 2 best (48 registers)
 constexpr int kThreads = 256;
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -94,51 +94,75 @@ __device__ __forceinline__ uint2 load_codes(const uint8_t *p)
                       __ldcs(reinterpret_cast<const unsigned *>(p + 4)));
 }
 
+// The insert, software-pipelined in registers: a warp takes groups of kPairs
+// row pairs (one row per half) and loads the next group's rows and slots
+// before it quantises and stores the current one.
+__device__ __forceinline__ void insert_load(const IParams &p, int64_t g, int half, int h,
+                                            int64_t *slot, uint4 *x)
+{
+#pragma unroll
+    for (int j = 0; j < kPairs; ++j) {
+        const int64_t t = g * 2 * kPairs + half + 2 * j;
+        slot[j] = t < p.rows ? __ldg(p.slots + t) : -1;
+        x[j] = t < p.rows ? __ldcs(reinterpret_cast<const uint4 *>(p.k + t * kDim) + h)
+                          : make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
 // kWide: every code row starts on an 8-byte boundary (the cache is 8-byte
 // aligned and the block size even), so each lane stores its 8 codes at once
+template <bool kWide>
+__device__ __forceinline__ void insert_store(const IParams &p, int h, const int64_t *slot,
+                                             const uint4 *x)
+{
+#pragma unroll
+    for (int j = 0; j < kPairs; ++j) {
+        const uint32_t m2 = __vmaxu2(__vmaxu2(x[j].x & 0x7fff7fffu, x[j].y & 0x7fff7fffu),
+                                     __vmaxu2(x[j].z & 0x7fff7fffu, x[j].w & 0x7fff7fffu));
+        uint32_t amax = max(m2 & 0xffffu, m2 >> 16);
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1)  // xor below 16 stays inside the half-warp
+            amax = max(amax, __shfl_xor_sync(kFull, amax, o));
+        if (slot[j] < 0)
+            continue;
+        if (slot[j] >= p.num_slots) {
+            if (h == 0 && p.err != nullptr)
+                atomicOr(p.err, DSV4_DEVERR_SLOT_RANGE);
+            continue;
+        }
+        const int s = row_exponent(amax);
+        const float inv = __uint_as_float(uint32_t(127 - s) << 23);  // 2^-s, normal
+        const int64_t blk = fastdiv(static_cast<uint32_t>(slot[j]), p.slot_div);
+        const int64_t off = slot[j] - blk * p.block_size;
+        uint8_t *base = p.cache + blk * int64_t(p.block_size) * kSlotBytes;
+        store_codes<kWide>(base + off * kDim + 8 * h, encode8(x[j], inv));
+        if (h == 0)
+            __stcs(reinterpret_cast<unsigned *>(base + int64_t(p.block_size) * kDim + off * 4),
+                   s > -127 ? uint32_t(s + 127) << 23 : 0x00400000u);
+    }
+}
+
 template <bool kWide>
 __global__ void __launch_bounds__(kThreads) indexer_k_insert_kernel(const IParams p)
 {
     const int lane = threadIdx.x & 31, half = lane >> 4, h = lane & 15;
     const int64_t warps = int64_t(gridDim.x) * (kThreads / 32);
     const int64_t groups = (p.rows + 2 * kPairs - 1) / (2 * kPairs);
-    for (int64_t g = int64_t(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5); g < groups;
-         g += warps) {
-        const int64_t t0 = g * 2 * kPairs + half;
-        int64_t slot[kPairs];
-        uint4 x[kPairs];
-#pragma unroll
-        for (int j = 0; j < kPairs; ++j)
-            slot[j] = t0 + 2 * j < p.rows ? __ldg(p.slots + t0 + 2 * j) : -1;
-#pragma unroll
-        for (int j = 0; j < kPairs; ++j)
-            x[j] = t0 + 2 * j < p.rows
-                       ? __ldcs(reinterpret_cast<const uint4 *>(p.k + (t0 + 2 * j) * kDim) + h)
-                       : make_uint4(0u, 0u, 0u, 0u);
+    int64_t g = int64_t(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5);
+    if (g >= groups)
+        return;
+    int64_t slot[kPairs];
+    uint4 x[kPairs];
+    insert_load(p, g, half, h, slot, x);
+    for (; g < groups; g += warps) {
+        int64_t slot_n[kPairs];
+        uint4 x_n[kPairs];
+        insert_load(p, g + warps, half, h, slot_n, x_n);  // nothing is read past the end
+        insert_store<kWide>(p, h, slot, x);
 #pragma unroll
         for (int j = 0; j < kPairs; ++j) {
-            const uint32_t m2 = __vmaxu2(__vmaxu2(x[j].x & 0x7fff7fffu, x[j].y & 0x7fff7fffu),
-                                         __vmaxu2(x[j].z & 0x7fff7fffu, x[j].w & 0x7fff7fffu));
-            uint32_t amax = max(m2 & 0xffffu, m2 >> 16);
-#pragma unroll
-            for (int o = 1; o < 16; o <<= 1)  // xor below 16 stays inside the half-warp
-                amax = max(amax, __shfl_xor_sync(kFull, amax, o));
-            if (slot[j] < 0)
-                continue;
-            if (slot[j] >= p.num_slots) {
-                if (h == 0 && p.err != nullptr)
-                    atomicOr(p.err, DSV4_DEVERR_SLOT_RANGE);
-                continue;
-            }
-            const int s = row_exponent(amax);
-            const float inv = __uint_as_float(uint32_t(127 - s) << 23);  // 2^-s, normal
-            const int64_t blk = fastdiv(static_cast<uint32_t>(slot[j]), p.slot_div);
-            const int64_t off = slot[j] - blk * p.block_size;
-            uint8_t *base = p.cache + blk * int64_t(p.block_size) * kSlotBytes;
-            store_codes<kWide>(base + off * kDim + 8 * h, encode8(x[j], inv));
-            if (h == 0)
-                __stcs(reinterpret_cast<unsigned *>(base + int64_t(p.block_size) * kDim + off * 4),
-                       s > -127 ? uint32_t(s + 127) << 23 : 0x00400000u);
+            slot[j] = slot_n[j];
+            x[j] = x_n[j];
         }
     }
 }
