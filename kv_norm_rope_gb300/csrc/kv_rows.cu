@@ -304,11 +304,6 @@ __global__ void __launch_bounds__(kKvThreads, kKvCtasPerSm) kv_rows_kernel(const
             mbar_init(&bars[s], 1);
         mbar_init_fence();
     }
-    if (kKvNorm) {
-        for (int i = threadIdx.x; i < 64; i += kKvThreads)
-            stage_weight_q(p.w, i, w_smem);
-    }
-    __syncthreads();
 
     const int64_t T = p.num_tokens;
     const int64_t items = (T + 3) / 4;
@@ -331,6 +326,13 @@ __global__ void __launch_bounds__(kKvThreads, kKvCtasPerSm) kv_rows_kernel(const
     int64_t t = 4 * first + c;
     int64_t pos = t < T ? __ldg(p.pos + t) : 0;
     int64_t slot = t < T ? __ldg(p.slot + t) : -1;
+    // the first copies and metadata are in flight while the CTA stages the
+    // weight; the barriers' other lanes and the weight wait for the CTA barrier
+    if (kKvNorm) {
+        for (int i = threadIdx.x; i < 64; i += kKvThreads)
+            stage_weight_q(p.w, i, w_smem);
+    }
+    __syncthreads();
     for (int64_t j = 0; j < mine; ++j) {
         // the next item's metadata, one item ahead
         const int64_t tn = t + 4 * total;
