@@ -37,11 +37,12 @@
 //    SGLang section "Modifications", item 4).  The rotation is applied to the
 //    unscaled inputs with a compensated a*c - b*s and the norm factor after
 //    it, so a pair that nearly cancels still lands within a bf16 ulp.
-//  * The UE8M0 exponent must agree with an exact (fp64) evaluation.  fp32 is
-//    enough except when a block's amax lies within a relative 2^-14 of a
-//    boundary 448*2^k; only then does the warp recompute the row's norm and
-//    the affected elements in fp64 (GB300's fp64 rate is low, so this is kept
-//    off the common path: about 3e-4 of KV rows take it on Gaussian data).
+//  * The UE8M0 exponent must agree with an exact evaluation.  fp32 is enough
+//    except when a block's amax lies within a relative 2^-14 of a boundary
+//    448*2^k; only then does the warp settle it (exact_scale_bumps): in fp32
+//    float-float arithmetic, and in fp64 for the values it cannot settle
+//    (GB300's fp64 rate is low; about 3e-4 of KV rows take the path on
+//    Gaussian data).
 //  * Nothing here waits, spins or traps.  Out-of-range positions or slots set
 //    a bit in the caller's error word and the affected writes are skipped.
 
