@@ -97,3 +97,11 @@ def test_ragged_token_counts(T):
     rep = harness.check(configs.generic(T, 0, seed=90 + T), k.VARIANT_STREAM)
     assert rep.ok, str(rep)
 
+
+
+def test_offsets_past_2_gib():
+    """2^21 + 5 KV rows through the bulk-copy kernel: kv offsets reach 2.15 GB and cache
+    offsets 2.45 GB, past 2^31 bytes; every cache row against the oracle."""
+    wl = configs.generic(2 ** 21 + 5, 0, seed=95, skip_frac=0.01)
+    rep = harness.check(wl, k.VARIANT_STREAM)
+    assert rep.ok, str(rep)
