@@ -106,3 +106,18 @@ def test_gather_empty_and_rejected():
     with pytest.raises(k.Dsv4Error):
         k.dequant_gather(c, 0, 1, torch.zeros(3, dtype=torch.int64, device=DEV),
                          torch.zeros((3, 512), dtype=torch.int16, device=DEV))
+
+
+def test_gather_past_2_gib_offsets():
+    """A 2.45 GB cache written by the KV-row kernel (2^21 + 5 rows, random slots over
+    4.2 M), 262144 of its rows read back in a random order: about 12% of them lie past
+    2^31 bytes (slot >= 3.68 M); every row against the oracle's reader."""
+    wl = configs.generic(2 ** 21 + 5, 0, seed=96, skip_frac=0.01)
+    inp = harness.make_inputs(wl)
+    gpu = harness.run_gpu(inp)
+    slots = inp.slots[synth.permutation(wl.T, 96, 13)[:262144]]
+    assert int((slots >= (2 ** 31) // 584).sum()) > 10000
+    got, err = _gather_gpu(gpu.cache, wl.num_blocks, wl.block_size, slots)
+    ref, ref_err = oracle.dequant_gather(gpu.cache, wl.num_blocks, wl.block_size, slots)
+    assert err == ref_err == 0
+    assert np.array_equal(got, ref)
