@@ -51,9 +51,39 @@ __device__ __forceinline__ float scaled(float p, uint32_t e)
     return __fmul_rn(__fmul_rn(p, 0x1p64f), 0x1p64f);  // 2^128: beyond bf16, becomes inf
 }
 
+// 8 payload bytes with scale byte e -> 8 bf16 by integer arithmetic, when every
+// code is a normal E4M3 number (exponent field 1..15, not NaN) and 7 <= e <= 246:
+// (1 + m/8) * 2^(E - 7) * 2^(e - 127) is then exactly the bf16 with exponent field
+// E + e - 7 (1..254), mantissa m << 4 and the code's sign.  Returns false, leaving
+// out unset, when any code or the scale is outside that range.
+__device__ __forceinline__ bool dequant8_normal(uint2 codes, uint32_t e, uint4 &out)
+{
+    // a byte with exponent field 0 (zero, subnormal) or equal to 0x7f / 0xff (NaN):
+    // a zero byte of (code & 0x78) or of (code & 0x7f) ^ 0x7f (all bytes < 0x80)
+    const uint32_t xe = codes.x & 0x78787878u, ye = codes.y & 0x78787878u;
+    const uint32_t xn = (codes.x & 0x7f7f7f7fu) ^ 0x7f7f7f7fu;
+    const uint32_t yn = (codes.y & 0x7f7f7f7fu) ^ 0x7f7f7f7fu;
+    const uint32_t special = ((xe - 0x01010101u) & ~xe) | ((ye - 0x01010101u) & ~ye) |
+                             ((xn - 0x01010101u) & ~xn) | ((yn - 0x01010101u) & ~yn);
+    if ((special & 0x80808080u) != 0u || e - 7u > 239u)
+        return false;
+    const uint32_t off = ((e - 7u) << 7) * 0x00010001u;  // added to both exponent fields
+    // two codes, one per 16-bit half (the first in the low half), to two bf16
+    const auto pair = [off](uint32_t w, uint32_t sel) {
+        const uint32_t h = __byte_perm(w, 0u, sel);
+        return (((h & 0x007f007fu) << 4) + off) | ((h & 0x00800080u) << 8);
+    };
+    out = make_uint4(pair(codes.x, 0x4140u), pair(codes.x, 0x4342u), pair(codes.y, 0x4140u),
+                     pair(codes.y, 0x4342u));
+    return true;
+}
+
 // 8 payload bytes (one 64-bit word) with scale byte e -> 8 bf16 (one 16-byte vector)
 __device__ __forceinline__ uint4 dequant8(uint2 codes, uint32_t e)
 {
+    uint4 fast;
+    if (dequant8_normal(codes, e, fast))
+        return fast;
     float2 f[4];
     f[0] = e4m3x2_to_f32(codes.x);
     f[1] = e4m3x2_to_f32(codes.x >> 16);
