@@ -29,8 +29,9 @@
  *    status means nothing was launched and no buffer was touched.
  *  - Conditions that need device data (a slot or a position out of range) are
  *    reported by OR-ing DSV4_DEVERR_* bits into *device_error (device int32,
- *    may be NULL) and skipping the affected writes.  Nothing traps, asserts or
- *    waits on the device.
+ *    may be NULL) and skipping the affected writes.  Nothing traps or asserts
+ *    on the device; the one kernel that waits on its own bulk copies bounds
+ *    every wait (DSV4_DEVERR_TIMEOUT).
  *  - Preconditions that are not checked: non-negative slots are distinct (if
  *    two tokens share a slot, which one's row lands is unspecified); q does
  *    not overlap kv, the cache or the metadata arrays; inputs are finite and
@@ -79,9 +80,9 @@ enum {
 enum {
     DSV4_DEVERR_SLOT_RANGE = 1, /* slot_mapping[t] >= num_blocks*block_size: cache row not written */
     DSV4_DEVERR_POS_RANGE = 2,  /* positions[t] < 0 or >= max_position: token not written at all */
-    DSV4_DEVERR_TIMEOUT = 4     /* DSV4_VARIANT_BULK and the KV-row kernel (num_heads 0, STREAM):
-                                   a bounded wait on a bulk copy inside the kernel ran out (never
-                                   expected); the outputs of that launch are undefined */
+    DSV4_DEVERR_TIMEOUT = 4     /* the KV-row kernel (num_heads 0, STREAM): a bounded wait on a
+                                   bulk copy inside the kernel ran out (never expected); the
+                                   outputs of that launch are undefined */
 };
 
 /* store modes and launch variants of dsv4_qnorm_rope_kv_insert_variant */
@@ -90,8 +91,7 @@ enum {
     DSV4_VARIANT_AUTO = 0,    /* pick from the row count and the SM count (below) */
     DSV4_VARIANT_SMALL = 1,   /* one row per warp, 2-warp CTAs, one wave: small batches */
     DSV4_VARIANT_STREAM = 2,  /* persistent CTAs sized to the SMs, several rows in flight per warp */
-    DSV4_VARIANT_BULK = 3,    /* one CTA per SM; 32-row chunks staged through shared memory by the
-                                 bulk-copy (TMA) engine, 6 in flight; q chunks written back in bulk */
+    /* 3 is not a variant (DSV4_ERR_VALUE) */
     DSV4_VARIANT_HALF = 4     /* persistent CTAs sized to the SMs, one row per half-warp (q and KV) */
 };
 
@@ -257,7 +257,7 @@ size_t dsv4_mxfp8_scale_bytes(int64_t num_rows, int32_t hidden);
 
 /* Launch plan of a call (pure host arithmetic, no CUDA call). */
 typedef struct {
-    int32_t variant;        /* DSV4_VARIANT_SMALL or DSV4_VARIANT_STREAM */
+    int32_t variant;        /* DSV4_VARIANT_SMALL, DSV4_VARIANT_STREAM or DSV4_VARIANT_HALF */
     int32_t threads;        /* threads per CTA */
     int64_t ctas;           /* grid size */
     int32_t rows_per_warp;  /* rows each warp loads together */
@@ -272,8 +272,7 @@ typedef struct {
  * grid-starved multi-token layout loses at small N); with q heads, HALF below 12
  * rounds of the streaming kernel's groups
  * (warp slots x rows_per_warp x 12; decode- to mid-sized batches, where HALF
- * measured faster); else STREAM (for num_heads 0, the KV-row kernel).  BULK runs one CTA
- * per SM (at most one per 32-row chunk).  HALF: ceil(T/2) KV row pairs and
+ * measured faster); else STREAM (for num_heads 0, the KV-row kernel).  HALF: ceil(T/2) KV row pairs and
  * groups of rows_per_warp q rows over persistent CTAs (ctas_per_sm then being
  * the HALF kernel's occupancy).  With num_heads 0, STREAM describes the
  * KV-row kernel: one row per quarter-warp, rows_per_warp 4, and ctas_per_sm should
@@ -335,8 +334,8 @@ int dsv4_indexer_k_gather(const uint8_t *indexer_cache, int64_t num_blocks, int3
 size_t dsv4_indexer_cache_bytes(int64_t num_blocks, int32_t block_size);
 
 /*
- * Check of the failure path of the bulk-copy kernels (DSV4_VARIANT_BULK and the
- * KV-row kernel): their waits on mbarriers give up after a budget of SM clock
+ * Check of the failure path of the bulk-copy kernel (the KV-row kernel that
+ * KV-only batches run): its waits on mbarriers give up after a budget of SM clock
  * cycles instead of waiting without bound.  This launches one warp that waits,
  * through the same code, on an mbarrier whose phase nothing completes.  After
  * max_cycles cycles (0, or anything above the kernels' own limit of 2^31 cycles,

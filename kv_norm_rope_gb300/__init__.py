@@ -20,7 +20,7 @@ _ROOT = os.path.dirname(_HERE)
 _CSRC = os.path.join(_HERE, "csrc")
 _INCLUDE = os.path.join(_ROOT, "include")
 LIB_PATH = os.path.join(_HERE, "libdsv4kv.so")
-_SOURCES = ["qnorm_rope_kv_insert.cu", "qnorm_rope_kv_insert_bulk.cu", "dequant_gather.cu",
+_SOURCES = ["qnorm_rope_kv_insert.cu", "dequant_gather.cu",
             "gemma_rmsnorm_mxfp8.cu", "indexer_k.cu", "kv_rows.cu", "qnorm_rope_kv_insert_half.cu",
             "wait_check.cu",
             "api.cpp"]
@@ -34,7 +34,7 @@ NVCC_ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_VALUE, ERR_CUDA = range(6)
 DEVERR_SLOT_RANGE, DEVERR_POS_RANGE, DEVERR_TIMEOUT = 1, 2, 4
 STORE_FP8, STORE_BF16 = 0, 1
-VARIANT_AUTO, VARIANT_SMALL, VARIANT_STREAM, VARIANT_BULK, VARIANT_HALF = 0, 1, 2, 3, 4
+VARIANT_AUTO, VARIANT_SMALL, VARIANT_STREAM, VARIANT_HALF = 0, 1, 2, 4
 FP8_SLOT_BYTES, BF16_SLOT_BYTES = 584, 1024
 
 EXPORTS = ("dsv4_qnorm_rope_kv_quant_insert", "dsv4_qnorm_rope_kv_bf16_insert",

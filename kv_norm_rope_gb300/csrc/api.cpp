@@ -110,8 +110,7 @@ int insert(int store_mode, int variant, int flags, void *q, const void *kv, cons
     if (store_mode != DSV4_STORE_FP8 && store_mode != DSV4_STORE_BF16)
         return DSV4_ERR_VALUE;
     if (variant != DSV4_VARIANT_AUTO && variant != DSV4_VARIANT_SMALL &&
-        variant != DSV4_VARIANT_STREAM && variant != DSV4_VARIANT_BULK &&
-        variant != DSV4_VARIANT_HALF)
+        variant != DSV4_VARIANT_STREAM && variant != DSV4_VARIANT_HALF)
         return DSV4_ERR_VALUE;
     const int32_t min_heads = (flags & kNoQ) ? 0 : 1;
     if (num_tokens < 0 || num_heads < min_heads || num_blocks < 1 || block_size < 1 ||
@@ -229,13 +228,6 @@ int dsv4_launch_plan(int64_t num_tokens, int32_t num_heads, int32_t sm_count, in
         plan->ctas = rows > 0 ? (rows + warps - 1) / warps : 1;
         if (plan->ctas > INT32_MAX)
             return DSV4_ERR_SHAPE;
-    } else if (variant == DSV4_VARIANT_BULK) {
-        const int64_t cr = dsv4::bulk_chunk_rows();
-        const int64_t chunks = (num_tokens + cr - 1) / cr + (rows - num_tokens + cr - 1) / cr;
-        plan->variant = DSV4_VARIANT_BULK;
-        plan->threads = dsv4::bulk_threads();
-        plan->rows_per_warp = 1;
-        plan->ctas = chunks < sm_count ? (chunks > 0 ? chunks : 1) : sm_count;
     } else if (variant == DSV4_VARIANT_STREAM) {
         // with no q heads the KV-row kernel runs: same CTA size, its own rows per warp
         const int per_warp = num_heads == 0 ? dsv4::kv_rows_per_warp() : dsv4::kStreamRowsPerWarp;

@@ -1,5 +1,5 @@
 // Internal interface between the C-ABI layer (api.cpp) and the whole-warp
-// fused kernels (qnorm_rope_kv_insert.cu, qnorm_rope_kv_insert_bulk.cu), plus
+// fused kernels (qnorm_rope_kv_insert.cu), plus
 // the kernel arguments every fused kernel takes.  Not installed; not part of
 // the ABI.
 #pragma once
@@ -59,12 +59,6 @@ int stream_ctas_per_sm(int store_mode, int *ctas_per_sm);
 
 // Enqueue the kernel described by `plan` on `stream`; returns a dsv4_status.
 int launch(int store_mode, const dsv4_plan &plan, const LaunchArgs &args, cudaStream_t stream);
-
-// The shared-memory-staged variant (qnorm_rope_kv_insert_bulk.cu): one CTA per SM.
-size_t bulk_smem_bytes();
-int bulk_threads();
-int bulk_chunk_rows();
-int launch_bulk(int store_mode, bool kv_norm, int64_t ctas, const KParams &p, cudaStream_t stream);
 
 // The FP8 cache reader (dequant_gather.cu).
 int gather_ctas_per_sm(int *ctas_per_sm);

@@ -29,8 +29,8 @@
 //    section "Modifications": the one-token layout stalled on
 //    long_scoreboard with DRAM at 5-7% of peak).  The small variant, for tiny
 //    batches, gives every row its own warp in one wave.  (Two more layouts live
-//    in their own files: one row per half-warp, one KV row per quarter-warp when
-//    there are no q heads, and rows staged by bulk copies.)
+//    in their own files: one row per half-warp, and one KV row per quarter-warp
+//    fed by bulk copies when there are no q heads.)
 //  * Sums of squares are a fixed per-lane sequence followed by a fixed xor
 //    butterfly, and the rotation is pinned to explicit fma/mul intrinsics, so
 //    a row's bits do not depend on which warp, CTA or variant ran it (the
@@ -190,8 +190,6 @@ int launch(int store_mode, const dsv4_plan &plan, const LaunchArgs &a, cudaStrea
     p.eps = a.eps;
     p.err = a.err;
     p.slot_div = fastdiv_magic(static_cast<uint32_t>(a.block_size));
-    if (plan.variant == DSV4_VARIANT_BULK)
-        return launch_bulk(store_mode, a.kv_norm, plan.ctas, p, stream);
     const dim3 grid(unsigned(plan.ctas)), block(unsigned(plan.threads));
     const bool small = plan.variant == DSV4_VARIANT_SMALL;
     if (store_mode == DSV4_STORE_BF16)

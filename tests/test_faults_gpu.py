@@ -30,7 +30,7 @@ def _faulty_inputs(store):
 
 
 @pytest.mark.parametrize("variant", [k.VARIANT_AUTO, k.VARIANT_SMALL, k.VARIANT_STREAM,
-                                     k.VARIANT_BULK])
+                                     k.VARIANT_HALF])
 @pytest.mark.parametrize("store", ["fp8", "bf16"])
 def test_out_of_range_flagged_and_skipped(store, variant):
     inp = _faulty_inputs(store)

@@ -21,7 +21,7 @@ if not torch.cuda.is_available():  # pragma: no cover
 
 import kv_norm_rope_gb300 as k  # noqa: E402
 
-VARIANTS = [k.VARIANT_AUTO, k.VARIANT_SMALL, k.VARIANT_STREAM, k.VARIANT_BULK, k.VARIANT_HALF]
+VARIANTS = [k.VARIANT_AUTO, k.VARIANT_SMALL, k.VARIANT_STREAM, k.VARIANT_HALF]
 
 
 def _case(i):

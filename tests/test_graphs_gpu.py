@@ -42,7 +42,7 @@ def _replay(fn, fresh):
 
 
 @pytest.mark.parametrize("variant", [k.VARIANT_AUTO, k.VARIANT_SMALL, k.VARIANT_STREAM,
-                                     k.VARIANT_BULK, k.VARIANT_HALF])
+                                     k.VARIANT_HALF])
 @pytest.mark.parametrize("H", [64, 0])
 def test_fused_step_in_a_graph(variant, H):
     wl = configs.generic(256, H, seed=120 + H)

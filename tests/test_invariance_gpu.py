@@ -22,8 +22,8 @@ import kv_norm_rope_gb300 as k  # noqa: E402
                          ids=lambda w: w.name)
 def test_variants_bit_identical(wl):
     inp = harness.make_inputs(wl)
-    outs = [harness.run_gpu(inp, v) for v in (k.VARIANT_SMALL, k.VARIANT_STREAM, k.VARIANT_BULK,
-                                              k.VARIANT_HALF, k.VARIANT_AUTO)]
+    outs = [harness.run_gpu(inp, v) for v in (k.VARIANT_SMALL, k.VARIANT_STREAM, k.VARIANT_HALF,
+                                              k.VARIANT_AUTO)]
     for o in outs[1:]:
         assert np.array_equal(o.q, outs[0].q)
         assert np.array_equal(o.cache, outs[0].cache)
