@@ -94,9 +94,57 @@ __device__ __forceinline__ void rope8_scaled(const float *u, float4 c, float4 s,
 
 // 1 / sqrt(sum/512 + eps): the mean and the sum correctly rounded, then one
 // correctly rounded reciprocal square root
+__device__ __forceinline__ float mean_sq(float sum_sq, float eps)
+{
+    return __fadd_rn(__fmul_rn(sum_sq, 1.0f / 512.0f), eps);
+}
+
 __device__ __forceinline__ float inv_rms(float sum_sq, float eps)
 {
-    return __frsqrt_rn(__fadd_rn(__fmul_rn(sum_sq, 1.0f / 512.0f), eps));
+    return __frsqrt_rn(mean_sq(sum_sq, eps));
+}
+
+// Rows whose mean square (eps included) is below 2^-100 are normalised on a
+// copy scaled by 2^64, twice at most.  In fp32 the square of an element below
+// 2^-63 is subnormal and keeps fewer bits than its exact 16; that error is
+// negligible beside a sum of 2^-100 or more, but decides r when such elements
+// make up the whole sum and eps is tiny too (eps = 0).  Scaling by 2^64 is
+// exact and commutes with every rounding while nothing is subnormal, so the
+// scaled row gives (2^64 x) * (2^-64 r) = x * r with r as accurate as for any
+// other row; the second step (by 2^128 in all) makes every nonzero bf16
+// element's square a normal fp32 number.  2^64 x stays below 2^19 because
+// the mean square was below 2^-100.
+constexpr float kTinyMeanSq = 0x1p-100f;
+
+// r = 1 / sqrt(sum(x^2)/512 + eps) of the row held in part by this lane.
+// sum() returns the row's sum of squares in the layout's fixed order (the same
+// bits on every lane of the row; every lane of the warp calls it together, so
+// it may shuffle); scale() multiplies this lane's elements of the row by 2^64.
+// On return the lane's elements may have been scaled by 2^64 or 2^128, and r by
+// the inverse, so that (element * r) is unchanged.  Rows of normal size take
+// one compare and one vote more than inv_rms.
+template <typename Sum, typename Scale>
+__device__ __forceinline__ float row_inv_rms(float eps, Sum sum, Scale scale)
+{
+    float m = mean_sq(sum(), eps);
+    bool tiny = m < kTinyMeanSq;
+    if (__any_sync(kFull, tiny)) {
+        float e = eps;
+#pragma unroll 1
+        for (int i = 0; i < 2; ++i) {
+            if (tiny) {
+                scale();
+                e = __fmul_rn(__fmul_rn(e, 0x1p64f), 0x1p64f);
+            }
+            const float s = sum();
+            if (tiny)
+                m = mean_sq(s, e);
+            tiny = tiny && m < kTinyMeanSq;
+            if (!__any_sync(kFull, tiny))
+                break;
+        }
+    }
+    return __frsqrt_rn(m);
 }
 
 // 2^-s as fp32 for s in [-127, 127]
@@ -341,6 +389,24 @@ __device__ __forceinline__ void flag_error(int32_t *err, int bit)
         atomicOr(err, bit);
 }
 
+// the whole-warp layout's sum of squares: 16 sequential fmas per lane, then
+// the xor butterfly
+__device__ __forceinline__ float warp_sumsq16(const float *y)
+{
+    float ss = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+        ss = __fmaf_rn(y[k], y[k], ss);
+    return warp_sum(ss);
+}
+
+__device__ __forceinline__ void scale_16(float *y)
+{
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+        y[k] = __fmul_rn(y[k], 0x1p64f);
+}
+
 // v = x * r * w for the lane's 16 dims of the KV row, then the rotation of
 // the rope dims (lanes 24..31).  Deterministic: calling it twice on the same
 // data gives the same bits.
@@ -361,11 +427,7 @@ __device__ __forceinline__ void kv_values(const KParams &p, int lane, uint4 xa, 
         }
         return;
     }
-    float ss = 0.0f;
-#pragma unroll
-    for (int k = 0; k < 16; ++k)
-        ss = __fmaf_rn(v[k], v[k], ss);
-    const float r = inv_rms(warp_sum(ss), p.eps);
+    const float r = row_inv_rms(p.eps, [&] { return warp_sumsq16(v); }, [&] { scale_16(v); });
     const uint4 wa = kSmemW ? w_smem[lane] : __ldg(reinterpret_cast<const uint4 *>(p.w) + lane);
     const uint4 wb =
         kSmemW ? w_smem[32 + lane] : __ldg(reinterpret_cast<const uint4 *>(p.w) + 32 + lane);
@@ -495,11 +557,7 @@ __device__ __forceinline__ void q_row(const KParams &p, int lane, uint4 a, uint4
     float y[16];
     widen8(a, y);
     widen8(b, y + 8);
-    float ss = 0.0f;
-#pragma unroll
-    for (int k = 0; k < 16; ++k)
-        ss = __fmaf_rn(y[k], y[k], ss);
-    const float r = inv_rms(warp_sum(ss), p.eps);
+    const float r = row_inv_rms(p.eps, [&] { return warp_sumsq16(y); }, [&] { scale_16(y); });
 #pragma unroll
     for (int k = 0; k < 8; ++k)
         y[k] = __fmul_rn(y[k], r);
@@ -516,61 +574,6 @@ __device__ __forceinline__ void q_row(const KParams &p, int lane, uint4 a, uint4
     }
     out_a = bf16x8_rn(y);
     out_b = bf16x8_rn(y + 8);
-}
-
-// Two q head rows at once, their dependency chains interleaved (the same
-// operations in the same order per row as q_row, so the same bits).
-__device__ __forceinline__ void q_row2(const KParams &p, int lane, const uint4 *in, const float4 *cv,
-                                       const float4 *sv, uint4 *out)
-{
-    float y[2][16];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        widen8(in[2 * j], y[j]);
-        widen8(in[2 * j + 1], y[j] + 8);
-    }
-    float ss[2] = {0.0f, 0.0f};
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-        ss[0] = __fmaf_rn(y[0][k], y[0][k], ss[0]);
-        ss[1] = __fmaf_rn(y[1][k], y[1][k], ss[1]);
-    }
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) {
-        const float o0 = __shfl_xor_sync(kFull, ss[0], m);
-        const float o1 = __shfl_xor_sync(kFull, ss[1], m);
-        ss[0] = __fadd_rn(ss[0], o0);
-        ss[1] = __fadd_rn(ss[1], o1);
-    }
-    const float r[2] = {inv_rms(ss[0], p.eps), inv_rms(ss[1], p.eps)};
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            y[j][k] = __fmul_rn(y[j][k], r[j]);
-    }
-    if (lane < 24) {
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-#pragma unroll
-            for (int k = 8; k < 16; ++k)
-                y[j][k] = __fmul_rn(y[j][k], r[j]);
-        }
-    } else {
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            float u[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                u[k] = y[j][8 + k];
-            rope8_scaled(u, cv[j], sv[j], r[j], y[j] + 8);
-        }
-    }
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        out[2 * j] = bf16x8_rn(y[j]);
-        out[2 * j + 1] = bf16x8_rn(y[j] + 8);
-    }
 }
 
 // cos and sin of the 4 pairs held by a rope lane (lanes 24..31) at row pos

@@ -116,3 +116,45 @@ def test_near_boundary_rows_agree_across_kernels():
                          np.arange(T, dtype=np.int64), IDENT,
                          synth.poison_bytes(wl.num_slots * 584, seed=5))
     _check_everywhere(inp)
+
+
+# row scales of the tiny-row test: normal rows, rows whose squares are still normal in
+# fp32, rows whose squares are subnormal (below 2^-63) and rows of bf16 subnormals
+TINY_SCALES = [1.0, 2.0**-50, 2.0**-64, 2.0**-70, 2.0**-100, 2.0**-115, 2.0**-124, 2.0**-128]
+
+
+def _scaled_bits(bits: np.ndarray, scale: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns times a per-row power of two, rounded to bf16 (nearest even)."""
+    f = synth.bf16_bits_to_f32(bits).reshape(scale.shape[0], -1) * scale[:, None].astype(np.float32)
+    t = torch.from_numpy(np.ascontiguousarray(f, np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16).reshape(bits.shape)
+
+
+@pytest.mark.parametrize("kv_norm", [True, False])
+@pytest.mark.parametrize("store", ["fp8", "bf16"])
+def test_tiny_rows_with_eps_zero(store, kv_norm):
+    """With eps = 0, rows scaled down by 2^-50 .. 2^-128 normalise like their unscaled
+    selves: squares below the fp32 normal range must not decide r.  Every variant and the
+    KV-only kernel against the oracle, and all caches equal."""
+    wl = dataclasses.replace(configs.generic(64, 3, store=store, seed=151), eps=0.0)
+    base = harness.make_inputs(wl)
+    tok_scale = np.array([TINY_SCALES[t % len(TINY_SCALES)] for t in range(wl.T)])
+    q = _scaled_bits(base.q.reshape(wl.T, -1), tok_scale).reshape(base.q.shape)
+    # the KV rows run through the scales in another order than the q rows of their token
+    kv = _scaled_bits(base.kv, tok_scale[::-1].copy())
+    inp = dataclasses.replace(base, q=q, kv=kv)
+    assert np.all((kv & 0x7FFF).reshape(wl.T, -1).max(axis=1) > 0)  # no all-zero row
+    ref_q, ref_cache, ref_err = harness.run_oracle(inp, kv_norm=kv_norm)
+    caches = []
+    for v in VARIANTS:
+        gpu = harness.run_gpu(inp, v, kv_norm=kv_norm)
+        rep = harness.compare_results(inp, gpu, ref_q, ref_cache)
+        assert rep.ok, f"variant {v}: {rep}"
+        assert gpu.err == ref_err == 0
+        caches.append(gpu.cache)
+    wl0 = dataclasses.replace(wl, H=0, name=wl.name + "_h0")
+    alone = harness.run_gpu(dataclasses.replace(inp, wl=wl0, q=np.empty((wl0.T, 0, 512), np.uint16)),
+                            k.VARIANT_STREAM, kv_norm=kv_norm)
+    caches.append(alone.cache)
+    for c in caches[1:]:
+        assert np.array_equal(c, caches[0])
