@@ -65,9 +65,24 @@ def compare_bf16(got: np.ndarray, ref: np.ndarray, what: str, rep: Report) -> Re
     return rep
 
 
+def written_slots(slots: np.ndarray, positions: np.ndarray, max_position: int,
+                  num_slots: int) -> np.ndarray:
+    """Mask of the cache slots a step writes: the slot of every token whose slot is in
+    the cache and whose position is inside the cos/sin table.  A token with an
+    out-of-range position writes nothing, so its slot must keep its old bytes."""
+    slots = np.asarray(slots, np.int64)
+    positions = np.asarray(positions, np.int64)
+    ok = (slots >= 0) & (slots < num_slots) & (positions >= 0) & (positions < max_position)
+    written = np.zeros(num_slots, dtype=bool)
+    written[slots[ok]] = True
+    return written
+
+
 def compare_fp8_cache(got: np.ndarray, ref: np.ndarray, poison: np.ndarray, slots: np.ndarray,
-                      num_blocks: int, block_size: int, rep: Report) -> Report:
-    """Compare two FP8 cache images (uint8, num_blocks*block_size*584 bytes)."""
+                      positions: np.ndarray, max_position: int, num_blocks: int,
+                      block_size: int, rep: Report) -> Report:
+    """Compare two FP8 cache images (uint8, num_blocks*block_size*584 bytes);
+    slots and positions are the step's per-token inputs."""
     got = np.ascontiguousarray(got).view(np.uint8).ravel()
     ref = np.ascontiguousarray(ref).view(np.uint8).ravel()
     nbs = block_size
@@ -78,9 +93,7 @@ def compare_fp8_cache(got: np.ndarray, ref: np.ndarray, poison: np.ndarray, slot
     g_scale = blocks[:, nbs * 576:].reshape(num_blocks * nbs, 8)
     r_scale = rblocks[:, nbs * 576:].reshape(num_blocks * nbs, 8)
 
-    written = np.zeros(num_blocks * nbs, dtype=bool)
-    valid = slots[(slots >= 0) & (slots < num_blocks * nbs)]
-    written[valid] = True
+    written = written_slots(slots, positions, max_position, num_blocks * nbs)
     # untouched slots: every byte equals the poison (and the oracle's image)
     pb = poison.reshape(num_blocks, nbs * 584)
     p_data = pb[:, : nbs * 576].reshape(num_blocks * nbs, 576)
@@ -112,13 +125,15 @@ def compare_fp8_cache(got: np.ndarray, ref: np.ndarray, poison: np.ndarray, slot
 
 
 def compare_bf16_cache(got: np.ndarray, ref: np.ndarray, poison: np.ndarray, slots: np.ndarray,
-                       num_slots: int, rep: Report) -> Report:
+                       positions: np.ndarray, max_position: int, num_slots: int,
+                       rep: Report) -> Report:
     g = np.ascontiguousarray(got).view(np.uint16).reshape(num_slots, 512)
     r = np.ascontiguousarray(ref).view(np.uint16).reshape(num_slots, 512)
     p = np.ascontiguousarray(poison).view(np.uint16).reshape(num_slots, 512)
-    written = np.zeros(num_slots, dtype=bool)
-    written[slots[(slots >= 0) & (slots < num_slots)]] = True
+    written = written_slots(slots, positions, max_position, num_slots)
     if not np.array_equal(g[~written], p[~written]):
         rep.fail("bytes of unwritten bf16 slots changed")
+    if not np.array_equal(r[~written], p[~written]):
+        rep.fail("oracle changed bytes of unwritten bf16 slots")
     compare_bf16(g[written], r[written], "bf16 cache rows", rep)
     return rep

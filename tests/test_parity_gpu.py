@@ -23,16 +23,12 @@ if not torch.cuda.is_available():  # pragma: no cover - CPU runs deselect the gp
 
 import kv_norm_rope_gb300 as k  # noqa: E402
 
-VARIANTS = [k.VARIANT_AUTO, k.VARIANT_SMALL, k.VARIANT_STREAM, k.VARIANT_BULK, k.VARIANT_HALF]
-# q rows beyond this many elements are compared on a token sample (the KV side,
-# i.e. the whole cache image, is always compared in full)
-FULL_Q_ELEMS = 1 << 27
+VARIANTS = [k.VARIANT_AUTO, k.VARIANT_SMALL, k.VARIANT_STREAM, k.VARIANT_HALF]
 
 
-def _check(wl, variant=k.VARIANT_AUTO, n_sample=None, inp=None, store=None):
-    if n_sample is None and wl.T * wl.H * 512 > FULL_Q_ELEMS:
-        n_sample = 1024
-    rep = harness.check(wl, variant, n_sample, inp, store)
+def _check(wl, variant=k.VARIANT_AUTO, inp=None, store=None):
+    """Every q row of every token and every cache byte against the oracle."""
+    rep = harness.check(wl, variant, inp, store)
     assert rep.ok, str(rep)
     return rep
 
@@ -53,8 +49,11 @@ def test_shape_sweep(T, H, store):
 @pytest.mark.parametrize("name", ["prefill", "bf16_store", "stress"])
 def test_full_size_workloads(name):
     """Full sizes in the launch configuration the benchmark times (AUTO): every
-    cache byte compared, q on 1024 sampled tokens (first/last 8 included)."""
-    _check(configs.WORKLOADS[name], k.VARIANT_AUTO, n_sample=1024)
+    cache byte and every token's q rows compared (q checked in token chunks after
+    the one whole-batch launch)."""
+    rep = _check(configs.WORKLOADS[name], k.VARIANT_AUTO)
+    wl = configs.WORKLOADS[name]
+    assert rep.q_elems == wl.T * wl.H * 512, rep.q_elems
 
 
 def test_heavy_tails_all_variants():
@@ -300,7 +299,7 @@ def test_full_size_kv_only_and_prenormalised(name):
     rep = harness.check(kv_wl, k.VARIANT_AUTO)
     assert rep.ok, str(rep)
     if name == "prefill":
-        rep = harness.check(wl, k.VARIANT_AUTO, n_sample=1024, kv_norm=False)
+        rep = harness.check(wl, k.VARIANT_AUTO, kv_norm=False)
         assert rep.ok, str(rep)
 
 
@@ -327,13 +326,6 @@ def test_public_entries_match_ex():
     torch.cuda.synchronize()
     ref2 = harness.run_gpu(inp)
     assert np.array_equal(cache2.cpu().numpy(), ref2.cache)
-
-
-@pytest.mark.parametrize("name", ["prefill", "bf16_store", "stress"])
-def test_full_size_workloads_bulk(name):
-    """The shared-memory-staged variant at full size (every cache byte, 1024 sampled
-    tokens' q)."""
-    _check(configs.WORKLOADS[name], k.VARIANT_BULK, n_sample=1024)
 
 
 @pytest.mark.parametrize("variant", VARIANTS)
