@@ -250,7 +250,7 @@ IO_OF_OP = {
     "indexer_gather": "indexer cache rows in; contiguous e4m3 [T, 128] + fp32 [T] out",
 }
 MXFP8_HIDDEN = 7168
-VARIANTS = {"auto": 0, "small": 1, "stream": 2, "bulk": 3, "half": 4}
+VARIANTS = {"auto": 0, "small": 1, "stream": 2, "half": 4}
 
 
 class DeviceBatch:
@@ -467,6 +467,135 @@ def known_answer_check() -> str:
 
 # ------------------------------------------------------------------ end to end
 
+def _cpulist(text: str) -> list:
+    """'0-3,8,10-11' -> [0, 1, 2, 3, 8, 10, 11]"""
+    out = []
+    for part in text.strip().split(","):
+        if not part:
+            continue
+        a, _, b = part.partition("-")
+        out += list(range(int(a), int(b or a) + 1))
+    return out
+
+
+def _ranges(cpus) -> str:
+    cpus = sorted(cpus)
+    out, i = [], 0
+    while i < len(cpus):
+        j = i
+        while j + 1 < len(cpus) and cpus[j + 1] == cpus[j] + 1:
+            j += 1
+        out.append(str(cpus[i]) if i == j else f"{cpus[i]}-{cpus[j]}")
+        i = j + 1
+    return ",".join(out)
+
+
+def numa_nodes() -> dict:
+    """CPU list of every NUMA node that has CPUs ({} where sysfs has no node info)."""
+    nodes = {}
+    base = "/sys/devices/system/node"
+    try:
+        names = os.listdir(base)
+    except OSError:
+        return nodes
+    for n in names:
+        if n.startswith("node") and n[4:].isdigit():
+            try:
+                cpus = _cpulist(open(os.path.join(base, n, "cpulist")).read())
+            except OSError:
+                continue
+            if cpus:
+                nodes[int(n[4:])] = cpus
+    return nodes
+
+
+def gpu_numa_node(device_index: int):
+    """The NUMA node sysfs gives the GPU's PCI function (None if unknown or -1)."""
+    import torch
+    p = torch.cuda.get_device_properties(device_index)
+    try:
+        bdf = f"{p.pci_domain_id:04x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+        node = int(open(f"/sys/bus/pci/devices/{bdf}/numa_node").read())
+    except (AttributeError, OSError, ValueError):
+        return None
+    return node if node >= 0 else None
+
+
+def pages_by_node(ptr: int) -> dict:
+    """Resident pages per NUMA node of the mapping that holds address ptr, from
+    /proc/self/numa_maps ({} if unknown)."""
+    try:
+        lines = open("/proc/self/numa_maps").read().splitlines()
+    except OSError:
+        return {}
+    best, best_start = None, -1
+    for line in lines:
+        start = int(line.split()[0], 16)
+        if best_start < start <= ptr:
+            best, best_start = line, start
+    if best is None:
+        return {}
+    out = {}
+    for f in best.split()[2:]:
+        if f.startswith("N") and "=" in f and f[1:f.index("=")].isdigit():
+            out[int(f[1:f.index("=")])] = int(f.split("=")[1])
+    return out
+
+
+_SYS_SET_MEMPOLICY = {"aarch64": 237, "x86_64": 238}
+
+
+def prefer_node(node) -> bool:
+    """Ask the kernel to place this thread's new pages on `node` (MPOL_PREFERRED), or
+    back to the default policy for None.  False where the call is unavailable."""
+    import ctypes
+    import platform
+    nr = _SYS_SET_MEMPOLICY.get(platform.machine())
+    if nr is None:
+        return False
+    libc = ctypes.CDLL(None, use_errno=True)
+    if node is None:
+        return libc.syscall(nr, 0, None, 0) == 0
+    if not 0 <= node < 64:
+        return False
+    mask = ctypes.c_ulong(1 << node)
+    return libc.syscall(nr, 1, ctypes.byref(mask), 65) == 0
+
+
+def link_ceilings(host, devbuf, dev, reps: int = 3) -> dict:
+    """Pinned host <-> device copy rates of the same buffers in this run (GB/s, best of
+    reps): host->device, device->host, and both at once (the first half of the buffer
+    up while the second half comes down, on two streams; GB/s counts both directions)."""
+    import torch
+    n = host.numel()
+    half = n // 2
+    nbytes = n * host.element_size()
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def best(fn, moved):
+        ts = []
+        for _ in range(reps):
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
+            fn()
+            torch.cuda.synchronize(dev)
+            ts.append(time.perf_counter() - t0)
+        return round(moved / min(ts) / 1e9, 1)
+
+    def both():
+        with torch.cuda.stream(s1):
+            devbuf[:half].copy_(host[:half], non_blocking=True)
+        with torch.cuda.stream(s2):
+            host[half:].copy_(devbuf[half:], non_blocking=True)
+
+    h2d = best(lambda: devbuf.copy_(host, non_blocking=True), nbytes)
+    d2h = best(lambda: host.copy_(devbuf, non_blocking=True), nbytes)
+    bidir = best(both, nbytes)
+    return {"h2d_gbs": h2d, "d2h_gbs": d2h, "both_gbs": bidir, "bytes": nbytes,
+            "how": "pinned q buffer <-> device q, best of 3 each; 'both': first half up while "
+                   "the second half comes down on another stream"}
+
+
 def e2e_run(batch: DeviceBatch, lib, steps: int, chunks: int = 16):
     """Same metric through the C ABI with host buffers: per step, token chunks of q, kv,
     positions and slots go host->device from pinned memory, the kernel runs on each chunk,
@@ -477,13 +606,28 @@ def e2e_run(batch: DeviceBatch, lib, steps: int, chunks: int = 16):
     import torch
     wl = batch.wl
     dev = batch.dev
-    q_h = torch.empty((wl.T, wl.H, 512), dtype=torch.bfloat16, pin_memory=True)
-    kv_h = torch.empty((wl.T, 512), dtype=torch.bfloat16, pin_memory=True)
-    pos_h = torch.from_numpy(batch.positions_np).pin_memory()
-    sl_h = torch.from_numpy(batch.slots_np).pin_memory()
-    cache_h = torch.empty(batch.cache.numel(), dtype=torch.uint8, pin_memory=True)
+    # pinned buffers on the GPU's own NUMA node where sysfs names one (the host link
+    # runs through that node's memory); the placement found is reported either way
+    gnode = gpu_numa_node(dev.index if dev.index is not None else 0)
+    nodes = numa_nodes()
+    preferred = gnode in nodes and prefer_node(gnode)
+    try:
+        q_h = torch.empty((wl.T, wl.H, 512), dtype=torch.bfloat16, pin_memory=True)
+        kv_h = torch.empty((wl.T, 512), dtype=torch.bfloat16, pin_memory=True)
+        pos_h = torch.from_numpy(batch.positions_np).pin_memory()
+        sl_h = torch.from_numpy(batch.slots_np).pin_memory()
+        cache_h = torch.empty(batch.cache.numel(), dtype=torch.uint8, pin_memory=True)
+    finally:
+        if preferred:
+            prefer_node(None)
     q_h.copy_(batch.q)
     kv_h.copy_(batch.kv)
+    allowed = sorted(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else []
+    placement = {"gpu_numa_node": gnode, "preferred_node_for_pinned": bool(preferred),
+                 "pinned_q_pages_by_node": pages_by_node(q_h.data_ptr()),
+                 "process_cpus": _ranges(allowed),
+                 "cpu_nodes": {n: _ranges(c) for n, c in sorted(nodes.items())}}
+    ceilings = link_ceilings(q_h.view(-1), batch.q.view(-1), dev)
     fn = entry(lib, wl.store)
     s_in, s_k, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     bounds = np.linspace(0, wl.T, chunks + 1).astype(np.int64)
@@ -533,7 +677,7 @@ def e2e_run(batch: DeviceBatch, lib, steps: int, chunks: int = 16):
         step()
     torch.cuda.synchronize(dev)
     dt = (time.perf_counter() - t0) / steps
-    return batch.bytes / dt / 1e9, h2d, d2h, dt
+    return batch.bytes / dt / 1e9, h2d, d2h, dt, ceilings, placement
 
 
 # ------------------------------------------------------------------ CPU oracle timing
@@ -712,13 +856,19 @@ def run_ours(args):
 
     e2e = None
     if not args.no_e2e and args.op == "fused":
-        e2e_gbs, h2d, d2h, e2e_dt = e2e_run(batch, lib, args.e2e_steps)
+        e2e_gbs, h2d, d2h, e2e_dt, ceil, placement = e2e_run(batch, lib, args.e2e_steps)
         e2e_dt = max_over_ranks(e2e_dt, world, dev)
+        link_gbs = (h2d + d2h) / e2e_dt / 1e9
         e2e = {"value": round(total_bytes / e2e_dt / 1e9, 2), "unit": "GB/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "tokens_per_s": round(total_tokens / e2e_dt, 1),
                "chunks": 16, "ms_per_step": round(e2e_dt * 1e3, 3),
-               "link": "pinned host memory; H2D and D2H overlap across chunks and steps"}
+               "link": "pinned host memory; H2D and D2H overlap across chunks and steps",
+               "link_gbs": round(link_gbs, 1),
+               "link_ceilings": ceil,
+               "frac_of_both_ways_ceiling": round(link_gbs / ceil["both_gbs"], 4)
+               if ceil["both_gbs"] else None,
+               "placement": placement}
     graph_us = graph_device_us(batch, lib, dev, flush) if flush is not None else None
     warm_us = graph_warm_us(batch, lib, dev) if flush is not None else None
     kac_after = known_answer_check() if rank == 0 else "skipped"
@@ -744,8 +894,8 @@ def run_ours(args):
                    "io": IO_OF_OP[args.op],
                    **({"hidden": args.hidden} if args.op == "mxfp8" else {}),
                    "variant": (args.variant if args.variant != "auto" else
-                               {k.VARIANT_STREAM: "stream", k.VARIANT_SMALL: "small", k.VARIANT_HALF: "half",
-                                k.VARIANT_BULK: "bulk"}[plan.variant])
+                               {k.VARIANT_STREAM: "stream", k.VARIANT_SMALL: "small",
+                                k.VARIANT_HALF: "half"}[plan.variant])
                    if args.op in ("fused", "prenorm", "kv_only") else "n/a",
                    "parallelism": f"dp{world}" if world > 1 else "single"},
         "tokens_per_s": round(total_tokens / t_step, 1),

@@ -75,3 +75,28 @@ def test_self_check_flags_rates_above_the_copy_ceiling():
 
 def test_cpu_model_is_a_nonempty_name():
     assert isinstance(bench.cpu_model(), str) and bench.cpu_model()
+
+
+def test_cpulist_round_trip():
+    assert bench._cpulist("0-3,8,10-11\n") == [0, 1, 2, 3, 8, 10, 11]
+    assert bench._ranges([11, 0, 1, 2, 3, 8, 10]) == "0-3,8,10-11"
+    assert bench._cpulist("") == [] and bench._ranges([]) == ""
+
+
+def test_pages_by_node_finds_the_mapping_of_an_address(tmp_path, monkeypatch):
+    maps = ("00400000 default file=/bin/x mapped=3 N0=3\n"
+            "7f0000000000 default anon=10 dirty=10 N0=4 N1=6 kernelpagesize_kB=64\n"
+            "7f0000100000 default anon=2 N1=2\n")
+    real_open = open
+
+    def fake_open(path, *a, **kw):
+        if path == "/proc/self/numa_maps":
+            p = tmp_path / "numa_maps"
+            p.write_text(maps)
+            return real_open(p, *a, **kw)
+        return real_open(path, *a, **kw)
+
+    monkeypatch.setattr("builtins.open", fake_open)
+    assert bench.pages_by_node(0x7f0000000040) == {0: 4, 1: 6}
+    assert bench.pages_by_node(0x7f0000100000) == {1: 2}
+    assert bench.pages_by_node(0x100) == {}
