@@ -562,15 +562,17 @@ def prefer_node(node) -> bool:
     return libc.syscall(nr, 1, ctypes.byref(mask), 65) == 0
 
 
-def link_ceilings(host, devbuf, dev, reps: int = 3) -> dict:
+def link_ceilings(host, devbuf, dev, reps: int = 3, chunks: int = 8) -> dict:
     """Pinned host <-> device copy rates of the same buffers in this run (GB/s, best of
-    reps): host->device, device->host, and both at once (the first half of the buffer
-    up while the second half comes down, on two streams; GB/s counts both directions)."""
+    reps): host->device, device->host, and both at once (chunk c of the first half goes
+    up on one stream while chunk c of the second half comes down on another, as the
+    e2e step interleaves its copies; GB/s counts both directions)."""
     import torch
     n = host.numel()
     half = n // 2
     nbytes = n * host.element_size()
     s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    cut = np.linspace(0, half, chunks + 1).astype(np.int64)
 
     def best(fn, moved):
         ts = []
@@ -583,17 +585,20 @@ def link_ceilings(host, devbuf, dev, reps: int = 3) -> dict:
         return round(moved / min(ts) / 1e9, 1)
 
     def both():
-        with torch.cuda.stream(s1):
-            devbuf[:half].copy_(host[:half], non_blocking=True)
-        with torch.cuda.stream(s2):
-            host[half:].copy_(devbuf[half:], non_blocking=True)
+        for c in range(chunks):
+            a, b = int(cut[c]), int(cut[c + 1])
+            with torch.cuda.stream(s1):
+                devbuf[a:b].copy_(host[a:b], non_blocking=True)
+            with torch.cuda.stream(s2):
+                host[half + a:half + b].copy_(devbuf[half + a:half + b], non_blocking=True)
 
     h2d = best(lambda: devbuf.copy_(host, non_blocking=True), nbytes)
     d2h = best(lambda: host.copy_(devbuf, non_blocking=True), nbytes)
     bidir = best(both, nbytes)
     return {"h2d_gbs": h2d, "d2h_gbs": d2h, "both_gbs": bidir, "bytes": nbytes,
-            "how": "pinned q buffer <-> device q, best of 3 each; 'both': first half up while "
-                   "the second half comes down on another stream"}
+            "how": f"pinned q buffer <-> device q, best of {reps} each; 'both': {chunks} chunks "
+                   f"of the first half up on one stream while the second half's come down on "
+                   f"another"}
 
 
 def e2e_run(batch: DeviceBatch, lib, steps: int, chunks: int = 16):

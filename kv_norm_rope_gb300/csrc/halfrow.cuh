@@ -41,6 +41,36 @@ __device__ __forceinline__ float half_sum(float v)
     return v;
 }
 
+// The row's sum of squares in the whole-warp order: lane h's vectors (0, 2)
+// are whole-warp lane h's, its vectors (1, 3) whole-warp lane h + 16's; their
+// sum is the butterfly's xor-16 level, then xor 8, 4, 2, 1 inside the half.
+__device__ __forceinline__ float half_sumsq(const float (*v)[8])
+{
+    float sa = 0.0f, sb = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        sa = __fmaf_rn(v[0][k], v[0][k], sa);
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        sa = __fmaf_rn(v[2][k], v[2][k], sa);
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        sb = __fmaf_rn(v[1][k], v[1][k], sb);
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        sb = __fmaf_rn(v[3][k], v[3][k], sb);
+    return half_sum(__fadd_rn(sa, sb));
+}
+
+__device__ __forceinline__ void half_scale(float (*v)[8])
+{
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            v[j][k] = __fmul_rn(v[j][k], 0x1p64f);
+}
+
 // cos and sin of the 4 pairs held by a rope lane (h >= 8) at row pos; zeros
 // elsewhere and for rows that are not written
 __device__ __forceinline__ void half_load_cs(const KParams &p, int h, bool active, int64_t pos,
@@ -74,21 +104,7 @@ __device__ __forceinline__ void half_row_values(const KParams &p, int h, const u
         }
         return;
     }
-    // the whole-warp order: lane h's vectors (0, 2), lane h + 16's (1, 3)
-    float sa = 0.0f, sb = 0.0f;
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-        sa = __fmaf_rn(v[0][k], v[0][k], sa);
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-        sa = __fmaf_rn(v[2][k], v[2][k], sa);
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-        sb = __fmaf_rn(v[1][k], v[1][k], sb);
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-        sb = __fmaf_rn(v[3][k], v[3][k], sb);
-    const float r = inv_rms(half_sum(__fadd_rn(sa, sb)), p.eps);
+    const float r = row_inv_rms(p.eps, [&] { return half_sumsq(v); }, [&] { half_scale(v); });
 #pragma unroll
     for (int j = 0; j < 3; ++j) {
         const float4 wa = w_smem[w_index(j, 0, h)], wb = w_smem[w_index(j, 1, h)];
@@ -294,21 +310,7 @@ __device__ __forceinline__ void q_half_row(const KParams &p, int h, const uint4 
 #pragma unroll
     for (int j = 0; j < 4; ++j)
         widen8(x[j], y[j]);
-    // the whole-warp order: lane h's vectors (0, 2), lane h + 16's (1, 3)
-    float sa = 0.0f, sb = 0.0f;
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-        sa = __fmaf_rn(y[0][k], y[0][k], sa);
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-        sa = __fmaf_rn(y[2][k], y[2][k], sa);
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-        sb = __fmaf_rn(y[1][k], y[1][k], sb);
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-        sb = __fmaf_rn(y[3][k], y[3][k], sb);
-    const float r = inv_rms(half_sum(__fadd_rn(sa, sb)), p.eps);
+    const float r = row_inv_rms(p.eps, [&] { return half_sumsq(y); }, [&] { half_scale(y); });
 #pragma unroll
     for (int j = 0; j < 3; ++j) {
 #pragma unroll

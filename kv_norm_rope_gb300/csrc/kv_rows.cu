@@ -71,6 +71,26 @@ __device__ __forceinline__ float quarter_sum(float v)
     return v;
 }
 
+// The row's sum of squares in the whole-warp order: the partials of whole-warp
+// lanes 8u + g (their vectors u and u + 4), the xor-16 and xor-8 levels as
+// (p0 + p2) + (p1 + p3), then xor 4, 2, 1 inside the quarter.
+__device__ __forceinline__ float quarter_sumsq(const float (*v)[8])
+{
+    float ps[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        float s = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            s = __fmaf_rn(v[u][k], v[u][k], s);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            s = __fmaf_rn(v[u + 4][k], v[u + 4][k], s);
+        ps[u] = s;
+    }
+    return quarter_sum(__fadd_rn(__fadd_rn(ps[0], ps[2]), __fadd_rn(ps[1], ps[3])));
+}
+
 // v = x * r * w (or x) for the lane's 64 dims of its row, rope dims rotated
 template <bool kKvNorm>
 __device__ __forceinline__ void quarter_values(const KParams &p, int g, const uint4 *x, float4 cv,
@@ -86,21 +106,13 @@ __device__ __forceinline__ void quarter_values(const KParams &p, int g, const ui
             t[k] = v[7][k];
         rope8_scaled(t, cv, sv, 1.0f, v[7]);
     } else {
-        // partials of whole-warp lanes 8u + g (their vectors u and u + 4)
-        float ps[4];
+        const float r = row_inv_rms(p.eps, [&] { return quarter_sumsq(v); }, [&] {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            float s = 0.0f;
+            for (int u = 0; u < 8; ++u)
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-                s = __fmaf_rn(v[u][k], v[u][k], s);
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                s = __fmaf_rn(v[u + 4][k], v[u + 4][k], s);
-            ps[u] = s;
-        }
-        const float r =
-            inv_rms(quarter_sum(__fadd_rn(__fadd_rn(ps[0], ps[2]), __fadd_rn(ps[1], ps[3]))), p.eps);
+                for (int k = 0; k < 8; ++k)
+                    v[u][k] = __fmul_rn(v[u][k], 0x1p64f);
+        });
 #pragma unroll
         for (int u = 0; u < 7; ++u) {
             const float4 wa = w_smem[wq_index(u, 0, g)], wb = w_smem[wq_index(u, 1, g)];
