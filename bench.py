@@ -682,6 +682,11 @@ def e2e_run(batch: DeviceBatch, lib, steps: int, chunks: int = 16):
         step()
     torch.cuda.synchronize(dev)
     dt = (time.perf_counter() - t0) / steps
+    # the link ceilings again, right after: the host link is shared with the
+    # node's other GPUs and CPU jobs, so both measurements bracket the e2e run
+    after = link_ceilings(q_h.view(-1), batch.q.view(-1), dev)
+    ceilings = {"before": ceilings, "after": after,
+                "both_gbs": max(ceilings["both_gbs"], after["both_gbs"])}
     return batch.bytes / dt / 1e9, h2d, d2h, dt, ceilings, placement
 
 

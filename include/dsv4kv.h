@@ -80,9 +80,12 @@ enum {
 enum {
     DSV4_DEVERR_SLOT_RANGE = 1, /* slot_mapping[t] >= num_blocks*block_size: cache row not written */
     DSV4_DEVERR_POS_RANGE = 2,  /* positions[t] < 0 or >= max_position: token not written at all */
-    DSV4_DEVERR_TIMEOUT = 4     /* the KV-row kernel (num_heads 0, STREAM): a bounded wait on a
+    DSV4_DEVERR_TIMEOUT = 4,    /* the KV-row kernel (num_heads 0, STREAM): a bounded wait on a
                                    bulk copy inside the kernel ran out (never expected); the
                                    outputs of that launch are undefined */
+    DSV4_DEVERR_BOUNDS = 8      /* the checked build only (libdsv4kv_checked.so, compiled with
+                                   DSV4_CHECK_BOUNDS): an access would have touched bytes outside
+                                   the buffer it belongs to; it was skipped (never expected) */
 };
 
 /* store modes and launch variants of dsv4_qnorm_rope_kv_insert_variant */
@@ -345,6 +348,23 @@ size_t dsv4_indexer_cache_bytes(int64_t num_blocks, int32_t block_size);
  * max_cycles < 0, DSV4_ERR_CUDA if the launch fails, else DSV4_OK.
  */
 int dsv4_check_bounded_wait(int64_t max_cycles, int32_t *device_error, void *stream);
+
+/*
+ * Debug aid of the checked build.  libdsv4kv_checked.so is the same library
+ * compiled with DSV4_CHECK_BOUNDS: before every global load or store, each kernel
+ * tests that the bytes it touches lie inside the buffer the access belongs to
+ * (q, kv, weight, positions, slots, cos/sin, cache, outputs; extents from the
+ * call's sizes).  An access that would leave its buffer is skipped and
+ * DSV4_DEVERR_BOUNDS is OR-ed into *device_error (where the entry point has one)
+ * and into a flag of the library.  This returns that flag, synchronising the
+ * current device first, and clears it when `reset` is nonzero: 0 if no access was
+ * skipped since the last reset, DSV4_DEVERR_BOUNDS if one was, DSV4_ERR_CUDA
+ * negated (-5) if reading it failed.  The release library (libdsv4kv.so) records
+ * nothing and returns -1.  The pages record two address faults of this operator
+ * on other hardware (FlagGems-vllm PR #684, "Performance against a baseline": a
+ * 32-bit index past 2^31 q elements, a KV store into the rope region).
+ */
+int dsv4_debug_bounds_flags(int reset);
 
 /* Static string naming a dsv4_status value ("unknown status" otherwise). */
 const char *dsv4_status_string(int status);

@@ -9,6 +9,7 @@ PyTorch supplies device memory and the current stream.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import subprocess
@@ -20,6 +21,8 @@ _ROOT = os.path.dirname(_HERE)
 _CSRC = os.path.join(_HERE, "csrc")
 _INCLUDE = os.path.join(_ROOT, "include")
 LIB_PATH = os.path.join(_HERE, "libdsv4kv.so")
+# the same sources with every global access tested against its buffer (DSV4_CHECK_BOUNDS)
+CHECKED_LIB_PATH = os.path.join(_HERE, "libdsv4kv_checked.so")
 _SOURCES = ["qnorm_rope_kv_insert.cu", "dequant_gather.cu",
             "gemma_rmsnorm_mxfp8.cu", "indexer_k.cu", "kv_rows.cu", "qnorm_rope_kv_insert_half.cu",
             "wait_check.cu",
@@ -27,12 +30,12 @@ _SOURCES = ["qnorm_rope_kv_insert.cu", "dequant_gather.cu",
 _HEADERS = [os.path.join(_INCLUDE, "dsv4kv.h")] + [
     os.path.join(_CSRC, h)
     for h in ("launch.h", "ops.h", "fastdiv.h", "convert.cuh", "launch_status.h", "rowmath.cuh",
-              "halfrow.cuh", "bulkcopy.cuh")]
+              "halfrow.cuh", "bulkcopy.cuh", "bounds.cuh", "bounds_range.h")]
 NVCC_ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 # status codes and constants (mirrors include/dsv4kv.h)
 OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_VALUE, ERR_CUDA = range(6)
-DEVERR_SLOT_RANGE, DEVERR_POS_RANGE, DEVERR_TIMEOUT = 1, 2, 4
+DEVERR_SLOT_RANGE, DEVERR_POS_RANGE, DEVERR_TIMEOUT, DEVERR_BOUNDS = 1, 2, 4, 8
 STORE_FP8, STORE_BF16 = 0, 1
 VARIANT_AUTO, VARIANT_SMALL, VARIANT_STREAM, VARIANT_HALF = 0, 1, 2, 4
 FP8_SLOT_BYTES, BF16_SLOT_BYTES = 584, 1024
@@ -43,7 +46,7 @@ EXPORTS = ("dsv4_qnorm_rope_kv_quant_insert", "dsv4_qnorm_rope_kv_bf16_insert",
            "dsv4_add_gemma_rmsnorm_mxfp8", "dsv4_mxfp8_scale_bytes", "dsv4_launch_plan",
            "dsv4_fp8_cache_bytes", "dsv4_bf16_cache_bytes", "dsv4_indexer_k_quant_insert",
            "dsv4_indexer_k_gather", "dsv4_indexer_cache_bytes", "dsv4_check_bounded_wait",
-           "dsv4_status_string")
+           "dsv4_debug_bounds_flags", "dsv4_status_string")
 
 
 class Dsv4Error(RuntimeError):
@@ -57,25 +60,18 @@ def _nvcc() -> str:
     return cand if os.path.exists(cand) else "nvcc"
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB_PATH):
+def _stale(path: str) -> bool:
+    if not os.path.exists(path):
         return True
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(path)
     deps = [os.path.join(_CSRC, s) for s in _SOURCES] + _HEADERS
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile csrc/ into libdsv4kv.so (in-tree) for sm_103a with nvcc.
-
-    The translation units are compiled in parallel, then linked with the static
-    CUDA runtime, so the library needs only the driver at run time.
-    """
-    if not force and not _stale():
-        return LIB_PATH
+def _build_one(path: str, extra: list, verbose: bool) -> str:
     bdir = tempfile.mkdtemp(prefix="dsv4kv_build_", dir=_HERE)
     flags = NVCC_ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
-                         "-I", _INCLUDE, "-I", _CSRC]
+                         "-I", _INCLUDE, "-I", _CSRC] + extra
     if verbose:
         flags += ["-Xptxas", "-v"]
 
@@ -86,66 +82,110 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with ThreadPoolExecutor(len(_SOURCES)) as ex:
         objs = list(ex.map(compile_one, _SOURCES))
-    tmp = os.path.join(bdir, "libdsv4kv.so")
+    tmp = os.path.join(bdir, os.path.basename(path))
     subprocess.run([_nvcc()] + NVCC_ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs,
                    check=True)
-    os.replace(tmp, LIB_PATH)
+    os.replace(tmp, path)
     for f in objs:
         os.remove(f)
     os.rmdir(bdir)
-    return LIB_PATH
+    return path
+
+
+def build(force: bool = False, verbose: bool = False, checked: bool | None = None) -> str:
+    """Compile csrc/ for sm_103a with nvcc into libdsv4kv.so and its checked twin
+    libdsv4kv_checked.so (DSV4_CHECK_BOUNDS: every global access tested against its
+    buffer), both in-tree.  checked=False builds the release library only, True the
+    checked one only.  Translation units compile in parallel and link the static CUDA
+    runtime, so the libraries need only the driver at run time.  Returns the path of
+    the release library (of the checked one for checked=True)."""
+    jobs = []
+    if checked is not True and (force or _stale(LIB_PATH)):
+        jobs.append((LIB_PATH, []))
+    if checked is not False and (force or _stale(CHECKED_LIB_PATH)):
+        jobs.append((CHECKED_LIB_PATH, ["-DDSV4_CHECK_BOUNDS"]))
+    with ThreadPoolExecutor(max(1, len(jobs))) as ex:
+        list(ex.map(lambda j: _build_one(j[0], j[1], verbose), jobs))
+    return CHECKED_LIB_PATH if checked else LIB_PATH
 
 
 _lib = None
 
 
 def lib():
-    """The loaded libdsv4kv (built first if missing or older than its sources)."""
+    """The loaded libdsv4kv (built first if missing or older than its sources).  With
+    DSV4KV_CHECKED=1 in the environment this is the checked build instead."""
     global _lib
     if _lib is None:
-        path = build()
-        L = ctypes.CDLL(path)
-        vp, i64, i32, f32, c_int = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32,
-                                    ctypes.c_float, ctypes.c_int)
-        common = [vp, vp, vp, vp, vp, i64, vp, vp, i64, i32, i64, i32, f32, vp, vp]
-        L.dsv4_qnorm_rope_kv_quant_insert.argtypes = common
-        L.dsv4_qnorm_rope_kv_quant_insert.restype = c_int
-        L.dsv4_qnorm_rope_kv_bf16_insert.argtypes = common
-        L.dsv4_qnorm_rope_kv_bf16_insert.restype = c_int
-        L.dsv4_qnorm_rope_kv_insert_variant.argtypes = [c_int, c_int] + common
-        L.dsv4_qnorm_rope_kv_insert_variant.restype = c_int
-        L.dsv4_insert_ex.argtypes = [c_int, c_int, c_int] + common
-        L.dsv4_insert_ex.restype = c_int
-        L.dsv4_qnorm_rope_kv_rope_quant_insert.argtypes = [vp, vp, vp, vp, i64, vp, vp, i64, i32,
-                                                           i64, i32, f32, vp, vp]
-        L.dsv4_qnorm_rope_kv_rope_quant_insert.restype = c_int
-        L.dsv4_kv_norm_rope_insert.argtypes = [c_int, vp, vp, vp, vp, i64, vp, vp, i64, i32, i64,
-                                               f32, vp, vp]
-        L.dsv4_kv_norm_rope_insert.restype = c_int
-        L.dsv4_dequant_gather.argtypes = [vp, i64, i32, vp, i64, vp, vp, vp]
-        L.dsv4_dequant_gather.restype = c_int
-        L.dsv4_add_gemma_rmsnorm_mxfp8.argtypes = [vp, vp, vp, i64, i32, f32, vp, vp, vp, vp]
-        L.dsv4_add_gemma_rmsnorm_mxfp8.restype = c_int
-        L.dsv4_mxfp8_scale_bytes.argtypes = [i64, i32]
-        L.dsv4_mxfp8_scale_bytes.restype = ctypes.c_size_t
-        L.dsv4_launch_plan.argtypes = [i64, i32, i32, i32, i32, ctypes.POINTER(Plan)]
-        L.dsv4_launch_plan.restype = c_int
-        L.dsv4_fp8_cache_bytes.argtypes = [i64, i32]
-        L.dsv4_fp8_cache_bytes.restype = ctypes.c_size_t
-        L.dsv4_bf16_cache_bytes.argtypes = [i64, i32]
-        L.dsv4_bf16_cache_bytes.restype = ctypes.c_size_t
-        L.dsv4_indexer_k_quant_insert.argtypes = [vp, vp, vp, i64, i32, i64, vp, vp]
-        L.dsv4_indexer_k_quant_insert.restype = c_int
-        L.dsv4_indexer_k_gather.argtypes = [vp, i64, i32, vp, i64, vp, vp, vp, vp]
-        L.dsv4_indexer_k_gather.restype = c_int
-        L.dsv4_indexer_cache_bytes.argtypes = [i64, i32]
-        L.dsv4_indexer_cache_bytes.restype = ctypes.c_size_t
-        L.dsv4_check_bounded_wait.argtypes = [i64, vp, vp]
-        L.dsv4_check_bounded_wait.restype = c_int
-        L.dsv4_status_string.argtypes = [c_int]
-        L.dsv4_status_string.restype = ctypes.c_char_p
-        _lib = L
+        checked = os.environ.get("DSV4KV_CHECKED", "") == "1"
+        _lib = _load(build(checked=checked))
     return _lib
+
+
+@contextlib.contextmanager
+def checked_build():
+    """Route every call made in the block through libdsv4kv_checked.so, whose kernels
+    test each global access against its buffer (see dsv4_debug_bounds_flags)."""
+    global _lib
+    saved = lib()
+    _lib = _load(build(checked=True))
+    try:
+        yield _lib
+    finally:
+        _lib = saved
+
+
+def debug_bounds_flags(reset: bool = True) -> int:
+    """dsv4_debug_bounds_flags of the loaded library: 0 or DEVERR_BOUNDS (checked
+    build), -1 (release build)."""
+    return int(lib().dsv4_debug_bounds_flags(1 if reset else 0))
+
+
+def _load(path: str):
+    """Open a built library and declare its entry points' argument types."""
+    L = ctypes.CDLL(path)
+    vp, i64, i32, f32, c_int = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32,
+                                ctypes.c_float, ctypes.c_int)
+    common = [vp, vp, vp, vp, vp, i64, vp, vp, i64, i32, i64, i32, f32, vp, vp]
+    L.dsv4_qnorm_rope_kv_quant_insert.argtypes = common
+    L.dsv4_qnorm_rope_kv_quant_insert.restype = c_int
+    L.dsv4_qnorm_rope_kv_bf16_insert.argtypes = common
+    L.dsv4_qnorm_rope_kv_bf16_insert.restype = c_int
+    L.dsv4_qnorm_rope_kv_insert_variant.argtypes = [c_int, c_int] + common
+    L.dsv4_qnorm_rope_kv_insert_variant.restype = c_int
+    L.dsv4_insert_ex.argtypes = [c_int, c_int, c_int] + common
+    L.dsv4_insert_ex.restype = c_int
+    L.dsv4_qnorm_rope_kv_rope_quant_insert.argtypes = [vp, vp, vp, vp, i64, vp, vp, i64, i32,
+                                                       i64, i32, f32, vp, vp]
+    L.dsv4_qnorm_rope_kv_rope_quant_insert.restype = c_int
+    L.dsv4_kv_norm_rope_insert.argtypes = [c_int, vp, vp, vp, vp, i64, vp, vp, i64, i32, i64,
+                                           f32, vp, vp]
+    L.dsv4_kv_norm_rope_insert.restype = c_int
+    L.dsv4_dequant_gather.argtypes = [vp, i64, i32, vp, i64, vp, vp, vp]
+    L.dsv4_dequant_gather.restype = c_int
+    L.dsv4_add_gemma_rmsnorm_mxfp8.argtypes = [vp, vp, vp, i64, i32, f32, vp, vp, vp, vp]
+    L.dsv4_add_gemma_rmsnorm_mxfp8.restype = c_int
+    L.dsv4_mxfp8_scale_bytes.argtypes = [i64, i32]
+    L.dsv4_mxfp8_scale_bytes.restype = ctypes.c_size_t
+    L.dsv4_launch_plan.argtypes = [i64, i32, i32, i32, i32, ctypes.POINTER(Plan)]
+    L.dsv4_launch_plan.restype = c_int
+    L.dsv4_fp8_cache_bytes.argtypes = [i64, i32]
+    L.dsv4_fp8_cache_bytes.restype = ctypes.c_size_t
+    L.dsv4_bf16_cache_bytes.argtypes = [i64, i32]
+    L.dsv4_bf16_cache_bytes.restype = ctypes.c_size_t
+    L.dsv4_indexer_k_quant_insert.argtypes = [vp, vp, vp, i64, i32, i64, vp, vp]
+    L.dsv4_indexer_k_quant_insert.restype = c_int
+    L.dsv4_indexer_k_gather.argtypes = [vp, i64, i32, vp, i64, vp, vp, vp, vp]
+    L.dsv4_indexer_k_gather.restype = c_int
+    L.dsv4_indexer_cache_bytes.argtypes = [i64, i32]
+    L.dsv4_indexer_cache_bytes.restype = ctypes.c_size_t
+    L.dsv4_check_bounded_wait.argtypes = [i64, vp, vp]
+    L.dsv4_check_bounded_wait.restype = c_int
+    L.dsv4_debug_bounds_flags.argtypes = [c_int]
+    L.dsv4_debug_bounds_flags.restype = c_int
+    L.dsv4_status_string.argtypes = [c_int]
+    L.dsv4_status_string.restype = ctypes.c_char_p
+    return L
 
 
 class Plan(ctypes.Structure):

@@ -457,6 +457,21 @@ int dsv4_check_bounded_wait(int64_t max_cycles, int32_t *device_error, void *str
     return dsv4::launch_wait_check(max_cycles, device_error, static_cast<cudaStream_t>(stream));
 }
 
+int dsv4_debug_bounds_flags(int reset)
+{
+    int (*const readers[])(int) = {dsv4::bounds_flag_fused, dsv4::bounds_flag_half,
+                                   dsv4::bounds_flag_kv_rows, dsv4::bounds_flag_gather,
+                                   dsv4::bounds_flag_indexer, dsv4::bounds_flag_mxfp8};
+    int flags = 0;
+    for (auto read : readers) {
+        const int v = read(reset);
+        if (v < 0)
+            return v;  // -1: the release build, which records nothing; else a CUDA failure
+        flags |= v;
+    }
+    return flags;
+}
+
 const char *dsv4_status_string(int status)
 {
     switch (status) {

@@ -20,6 +20,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "bounds.cuh"
 #include "convert.cuh"
 #include "fastdiv.h"
 #include "launch.h"
@@ -96,9 +97,18 @@ __device__ __forceinline__ uint4 dequant8(uint2 codes, uint32_t e)
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-__device__ __forceinline__ uint2 ld8(const uint8_t *p)
+// the buffers of a launch, for the checked build's bounds tests (bounds.cuh)
+__device__ __forceinline__ Span cache_span(const GParams &p)
 {
-    return __ldcs(reinterpret_cast<const uint2 *>(p));
+    return Span{p.cache, uint64_t(p.num_slots) * DSV4_FP8_SLOT_BYTES};
+}
+__device__ __forceinline__ Span slots_span(const GParams &p)
+{
+    return Span{p.slots, uint64_t(p.rows) * 8u};
+}
+__device__ __forceinline__ Span out_span(const GParams &p)
+{
+    return Span{p.out, uint64_t(p.rows) * DSV4_HEAD_DIM * 2u};
 }
 
 // one group of rows as loaded by one lane
@@ -113,7 +123,7 @@ __device__ __forceinline__ void load_slots(const GParams &p, int64_t g, int64_t 
 #pragma unroll
     for (int j = 0; j < kGatherRows; ++j) {
         const int64_t r = g * kGatherRows + j;
-        slot[j] = r < p.rows ? __ldg(p.slots + r) : -1;
+        slot[j] = r < p.rows ? ldg_i64_in(p.slots + r, slots_span(p), p.err) : -1;
     }
 }
 
@@ -130,15 +140,17 @@ __device__ __forceinline__ void load_rows(const GParams &p, int lane, Group &q)
             const int64_t off = slot - blk * p.block_size;
             const uint8_t *base = p.cache + blk * int64_t(p.block_size) * DSV4_FP8_SLOT_BYTES;
             const uint8_t *data = base + off * DSV4_FP8_DATA_BYTES;
-            q.lo[j] = ld8(data + 8 * lane);
+            const Span cs = cache_span(p);
+            q.lo[j] = ld_stream8_in(data + 8 * lane, cs, p.err);
             if (!rope_lane) {
-                q.hi0[j] = ld8(data + 256 + 8 * lane);
+                q.hi0[j] = ld_stream8_in(data + 256 + 8 * lane, cs, p.err);
             } else {
-                q.hi0[j] = ld8(data + DSV4_NOPE_DIM + 16 * (lane - 24));
-                q.hi1[j] = ld8(data + DSV4_NOPE_DIM + 16 * (lane - 24) + 8);
+                q.hi0[j] = ld_stream8_in(data + DSV4_NOPE_DIM + 16 * (lane - 24), cs, p.err);
+                q.hi1[j] = ld_stream8_in(data + DSV4_NOPE_DIM + 16 * (lane - 24) + 8, cs, p.err);
             }
-            q.sc[j] = __ldg(reinterpret_cast<const uint2 *>(
-                base + int64_t(p.block_size) * DSV4_FP8_DATA_BYTES + off * DSV4_FP8_SCALE_BYTES));
+            q.sc[j] = ldg8_in(
+                base + int64_t(p.block_size) * DSV4_FP8_DATA_BYTES + off * DSV4_FP8_SCALE_BYTES, cs,
+                p.err);
         }
     }
 }
@@ -166,8 +178,8 @@ __device__ __forceinline__ void emit_rows(const GParams &p, int lane, int64_t g,
             b = rope_lane ? make_uint4(q.hi0[j].x, q.hi0[j].y, q.hi1[j].x, q.hi1[j].y)
                           : dequant8(q.hi0[j], e1);
         }
-        __stcs(reinterpret_cast<uint4 *>(row + 8 * lane), a);
-        __stcs(reinterpret_cast<uint4 *>(row + 256 + 8 * lane), b);
+        st_stream16_in(row + 8 * lane, a, out_span(p), p.err);
+        st_stream16_in(row + 256 + 8 * lane, b, out_span(p), p.err);
     }
 }
 
@@ -229,3 +241,5 @@ int gather_rows_per_warp()
 }
 
 }  // namespace dsv4
+
+DSV4_BOUNDS_FLAG_READER(bounds_flag_gather)

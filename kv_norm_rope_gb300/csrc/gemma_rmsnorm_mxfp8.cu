@@ -19,6 +19,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "bounds.cuh"
 #include "convert.cuh"
 #include "launch_status.h"
 #include "ops.h"
@@ -40,6 +41,17 @@ struct MParams {
     int32_t padded_cols;
     float eps;
 };
+
+// the buffers of a launch, for the checked build's bounds tests (bounds.cuh);
+// this entry point has no error word, so only the library's flag records a hit
+__device__ __forceinline__ Span rows_span(const void *a, const MParams &p, uint32_t elem)
+{
+    return Span{a, uint64_t(p.m) * uint64_t(p.n) * elem};
+}
+__device__ __forceinline__ Span scales_span(const MParams &p)
+{
+    return Span{p.scales, uint64_t((p.m + 127) / 128) * 128u * uint64_t(p.padded_cols)};
+}
 
 __device__ __forceinline__ float bf16_round(float v)
 {
@@ -85,7 +97,7 @@ __global__ void __launch_bounds__(kThreads) gemma_rmsnorm_mxfp8_kernel(const MPa
     if (row >= p.m) {
         // padding row of the last 128-row scale tile: zero scales
         for (int c = tid; c < cols; c += kThreads)
-            p.scales[swizzled(row, c, p.padded_cols)] = 0;
+            st_byte_in(p.scales + swizzled(row, c, p.padded_cols), 0, scales_span(p), nullptr);
         return;
     }
     const uint16_t *xr = p.x + row * p.n;
@@ -97,14 +109,18 @@ __global__ void __launch_bounds__(kThreads) gemma_rmsnorm_mxfp8_kernel(const MPa
         const int f = tid + k * kThreads;
         if (f < fragments) {
             float a[8], b[8];
-            widen8(__ldcs(reinterpret_cast<const uint4 *>(xr) + f), a);
-            widen8(__ldcs(reinterpret_cast<const uint4 *>(rr) + f), b);
+            widen8(ld_stream16_in(reinterpret_cast<const uint4 *>(xr) + f, rows_span(p.x, p, 2), nullptr),
+                   a);
+            widen8(ld_stream16_in(reinterpret_cast<const uint4 *>(rr) + f,
+                                  rows_span(p.residual, p, 2), nullptr),
+                   b);
             uint32_t o[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i)
                 o[i] = bf16x2_rn(__fadd_rn(a[2 * i], b[2 * i]), __fadd_rn(a[2 * i + 1], b[2 * i + 1]));
             pre[k] = make_uint4(o[0], o[1], o[2], o[3]);
-            __stcs(reinterpret_cast<uint4 *>(p.residual_out + row * p.n) + f, pre[k]);
+            st_stream16_in(reinterpret_cast<uint4 *>(p.residual_out + row * p.n) + f, pre[k],
+                           rows_span(p.residual_out, p, 2), nullptr);
             float w[8];
             widen8(pre[k], w);
 #pragma unroll
@@ -134,7 +150,9 @@ __global__ void __launch_bounds__(kThreads) gemma_rmsnorm_mxfp8_kernel(const MPa
         const bool valid = f < fragments;  // 4-lane groups are all valid or all not
         float g[8] = {0, 0, 0, 0, 0, 0, 0, 0};
         if (valid)
-            widen8(__ldg(reinterpret_cast<const uint4 *>(p.gamma) + f), g);
+            widen8(ldg16_in(reinterpret_cast<const uint4 *>(p.gamma) + f,
+                            Span{p.gamma, uint64_t(p.n) * 2u}, nullptr),
+                   g);
         float v[8];
         widen8(pre[k], v);
         float amax = 0.0f;
@@ -148,13 +166,15 @@ __global__ void __launch_bounds__(kThreads) gemma_rmsnorm_mxfp8_kernel(const MPa
         const uint32_t e = ue8m0_round_up(__fmul_rn(amax, inv448));
         const float inv = ue8m0_inverse(e);
         if (valid) {
-            __stcs(reinterpret_cast<uint2 *>(p.codes + row * p.n) + f,
-                   make_uint2(e4m3x4_rn(__fmul_rn(v[0], inv), __fmul_rn(v[1], inv),
-                                        __fmul_rn(v[2], inv), __fmul_rn(v[3], inv)),
-                              e4m3x4_rn(__fmul_rn(v[4], inv), __fmul_rn(v[5], inv),
-                                        __fmul_rn(v[6], inv), __fmul_rn(v[7], inv))));
+            st_stream8_in(reinterpret_cast<uint2 *>(p.codes + row * p.n) + f,
+                          make_uint2(e4m3x4_rn(__fmul_rn(v[0], inv), __fmul_rn(v[1], inv),
+                                               __fmul_rn(v[2], inv), __fmul_rn(v[3], inv)),
+                                     e4m3x4_rn(__fmul_rn(v[4], inv), __fmul_rn(v[5], inv),
+                                               __fmul_rn(v[6], inv), __fmul_rn(v[7], inv))),
+                          rows_span(p.codes, p, 1), nullptr);
             if ((lane & 3) == 0)
-                p.scales[swizzled(row, f / 4, p.padded_cols)] = uint8_t(e);
+                st_byte_in(p.scales + swizzled(row, f / 4, p.padded_cols), uint8_t(e),
+                           scales_span(p), nullptr);
         }
     }
 }
@@ -202,3 +222,5 @@ int launch_gemma_rmsnorm_mxfp8(const uint16_t *x, const uint16_t *residual, cons
 }
 
 }  // namespace dsv4
+
+DSV4_BOUNDS_FLAG_READER(bounds_flag_mxfp8)

@@ -80,8 +80,8 @@ __device__ __forceinline__ void half_load_cs(const KParams &p, int h, bool activ
     sv = cv;
     if (active && h >= 8) {
         const float *cs = p.cs + pos * DSV4_ROPE_DIM + 4 * (h - 8);
-        cv = __ldg(reinterpret_cast<const float4 *>(cs));
-        sv = __ldg(reinterpret_cast<const float4 *>(cs + DSV4_ROPE_DIM / 2));
+        cv = ldg_f4_in(cs, cs_span(p), p.err);
+        sv = ldg_f4_in(cs + DSV4_ROPE_DIM / 2, cs_span(p), p.err);
     }
 }
 
@@ -218,24 +218,28 @@ __device__ __forceinline__ void half_row_fp8(const KParams &p, int h, bool activ
     const int64_t off = slot - blk * p.block_size;
     uint8_t *base = p.cache + blk * int64_t(p.block_size) * DSV4_FP8_SLOT_BYTES;
     uint8_t *data = base + off * DSV4_FP8_DATA_BYTES;
+    const Span cspan = cache_span<DSV4_STORE_FP8>(p);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         if (j == 3 && rope_lane)
             break;
         const float kj = pow2_neg(g[j].s);
-        st_stream8(data + 128 * j + 8 * h,
-                   make_uint2(e4m3x4_rn(v[j][0] * kj, v[j][1] * kj, v[j][2] * kj, v[j][3] * kj),
-                              e4m3x4_rn(v[j][4] * kj, v[j][5] * kj, v[j][6] * kj, v[j][7] * kj)));
+        st_stream8_in(data + 128 * j + 8 * h,
+                      make_uint2(e4m3x4_rn(v[j][0] * kj, v[j][1] * kj, v[j][2] * kj, v[j][3] * kj),
+                                 e4m3x4_rn(v[j][4] * kj, v[j][5] * kj, v[j][6] * kj, v[j][7] * kj)),
+                      cspan, p.err);
     }
     if (rope_lane) {
         // rope dims stay bf16; 8-byte stores keep any block_size legal
         uint8_t *tail = data + DSV4_NOPE_DIM + 16 * (h - 8);
-        st_stream8(tail, make_uint2(bf16x2_rn(v[3][0], v[3][1]), bf16x2_rn(v[3][2], v[3][3])));
-        st_stream8(tail + 8, make_uint2(bf16x2_rn(v[3][4], v[3][5]), bf16x2_rn(v[3][6], v[3][7])));
+        st_stream8_in(tail, make_uint2(bf16x2_rn(v[3][0], v[3][1]), bf16x2_rn(v[3][2], v[3][3])),
+                      cspan, p.err);
+        st_stream8_in(tail + 8, make_uint2(bf16x2_rn(v[3][4], v[3][5]), bf16x2_rn(v[3][6], v[3][7])),
+                      cspan, p.err);
     }
     if (h == 0)
-        st_stream8(base + int64_t(p.block_size) * DSV4_FP8_DATA_BYTES + off * DSV4_FP8_SCALE_BYTES,
-                   make_uint2(lo, hi));
+        st_stream8_in(base + int64_t(p.block_size) * DSV4_FP8_DATA_BYTES + off * DSV4_FP8_SCALE_BYTES,
+                      make_uint2(lo, hi), cspan, p.err);
 }
 
 // One row per half-warp.  active: this half's row is written (valid token,
@@ -255,7 +259,7 @@ __device__ __forceinline__ void half_row(const KParams &p, int h, bool active, i
             uint16_t *row = reinterpret_cast<uint16_t *>(p.cache) + slot * kHead;
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-                st_stream16(row + 128 * j + 8 * h, bf16x8_rn(v[j]));
+                st_stream16_in(row + 128 * j + 8 * h, bf16x8_rn(v[j]), cache_span<kStore>(p), p.err);
         }
     } else {
         half_row_fp8<kKvNorm>(p, h, active, t, slot, v);
@@ -263,10 +267,10 @@ __device__ __forceinline__ void half_row(const KParams &p, int h, bool active, i
 }
 
 // thread i < 64 widens the 8 weights of dims [8i, 8i + 8): j = i / 16, h = i % 16
-__device__ __forceinline__ void stage_weight(const uint16_t *w, int i, float4 *w_smem)
+__device__ __forceinline__ void stage_weight(const KParams &p, int i, float4 *w_smem)
 {
     float f[8];
-    widen8(__ldg(reinterpret_cast<const uint4 *>(w) + i), f);
+    widen8(ldg16_in(reinterpret_cast<const uint4 *>(p.w) + i, w_span(p), p.err), f);
     const int j = i >> 4, h = i & 15;
     w_smem[w_index(j, 0, h)] = make_float4(f[0], f[1], f[2], f[3]);
     w_smem[w_index(j, 1, h)] = make_float4(f[4], f[5], f[6], f[7]);
@@ -282,12 +286,13 @@ __device__ __forceinline__ void kv_pair_item(const KParams &p, int h, int64_t t,
                                              const float4 *w_smem)
 {
     const bool live = t < p.num_tokens;
-    const int64_t pos = live ? __ldg(p.pos + t) : 0;
-    const int64_t slot = live ? __ldg(p.slot + t) : -1;
+    const int64_t pos = live ? ldg_i64_in(p.pos + t, pos_span(p), p.err) : 0;
+    const int64_t slot = live ? ldg_i64_in(p.slot + t, slot_span(p), p.err) : -1;
     uint4 x[4];
 #pragma unroll
     for (int v = 0; v < 4; ++v)
-        x[v] = live ? ld_stream16(p.kv + t * kHead + 128 * v + 8 * h) : make_uint4(0u, 0u, 0u, 0u);
+        x[v] = live ? ld_stream16_in(p.kv + t * kHead + 128 * v + 8 * h, kv_span(p), p.err)
+                    : make_uint4(0u, 0u, 0u, 0u);
     const bool pos_ok = pos >= 0 && pos < p.max_pos;
     if (live && h == 0) {
         if (!pos_ok)

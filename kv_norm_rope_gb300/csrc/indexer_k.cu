@@ -28,6 +28,7 @@
 #include <stdint.h>
 
 #include "convert.cuh"
+#include "bounds.cuh"
 #include "fastdiv.h"
 #include "launch_status.h"
 #include "ops.h"
@@ -55,6 +56,28 @@ struct IParams {
     uint64_t slot_div;  // fastdiv_magic(block_size)
 };
 
+// the buffers of a launch, for the checked build's bounds tests (bounds.cuh)
+__device__ __forceinline__ Span k_span(const IParams &p)
+{
+    return Span{p.k, uint64_t(p.rows) * kDim * 2u};
+}
+__device__ __forceinline__ Span slots_span(const IParams &p)
+{
+    return Span{p.slots, uint64_t(p.rows) * 8u};
+}
+__device__ __forceinline__ Span icache_span(const void *cache, const IParams &p)
+{
+    return Span{cache, uint64_t(p.num_slots) * kSlotBytes};
+}
+__device__ __forceinline__ Span kout_span(const IParams &p)
+{
+    return Span{p.k_out, uint64_t(p.rows) * kDim};
+}
+__device__ __forceinline__ Span sout_span(const IParams &p)
+{
+    return Span{p.scale_out, uint64_t(p.rows) * 4u};
+}
+
 // the 8 codes of one lane: E4M3(x * inv) for the 8 bf16 of v
 __device__ __forceinline__ uint2 encode8(uint4 v, float inv)
 {
@@ -75,8 +98,10 @@ __device__ __forceinline__ int row_exponent(uint32_t amax_bits)
 }
 
 template <bool kWide>
-__device__ __forceinline__ void store_codes(uint8_t *p, uint2 c)
+__device__ __forceinline__ void store_codes(uint8_t *p, uint2 c, Span s, int32_t *err)
 {
+    if (!in_span(p, 8, s, err))
+        return;
     if (kWide) {
         __stcs(reinterpret_cast<uint2 *>(p), c);
     } else {
@@ -86,8 +111,10 @@ __device__ __forceinline__ void store_codes(uint8_t *p, uint2 c)
 }
 
 template <bool kWide>
-__device__ __forceinline__ uint2 load_codes(const uint8_t *p)
+__device__ __forceinline__ uint2 load_codes(const uint8_t *p, Span s, int32_t *err)
 {
+    if (!in_span(p, 8, s, err))
+        return make_uint2(0u, 0u);
     if (kWide)
         return __ldcs(reinterpret_cast<const uint2 *>(p));
     return make_uint2(__ldcs(reinterpret_cast<const unsigned *>(p)),
@@ -103,8 +130,9 @@ __device__ __forceinline__ void insert_load(const IParams &p, int64_t g, int hal
 #pragma unroll
     for (int j = 0; j < kPairs; ++j) {
         const int64_t t = g * 2 * kPairs + half + 2 * j;
-        slot[j] = t < p.rows ? __ldg(p.slots + t) : -1;
-        x[j] = t < p.rows ? __ldcs(reinterpret_cast<const uint4 *>(p.k + t * kDim) + h)
+        slot[j] = t < p.rows ? ldg_i64_in(p.slots + t, slots_span(p), p.err) : -1;
+        x[j] = t < p.rows ? ld_stream16_in(reinterpret_cast<const uint4 *>(p.k + t * kDim) + h,
+                                           k_span(p), p.err)
                           : make_uint4(0u, 0u, 0u, 0u);
     }
 }
@@ -135,10 +163,12 @@ __device__ __forceinline__ void insert_store(const IParams &p, int h, const int6
         const int64_t blk = fastdiv(static_cast<uint32_t>(slot[j]), p.slot_div);
         const int64_t off = slot[j] - blk * p.block_size;
         uint8_t *base = p.cache + blk * int64_t(p.block_size) * kSlotBytes;
-        store_codes<kWide>(base + off * kDim + 8 * h, encode8(x[j], inv));
+        store_codes<kWide>(base + off * kDim + 8 * h, encode8(x[j], inv), icache_span(p.cache, p),
+                           p.err);
         if (h == 0)
-            __stcs(reinterpret_cast<unsigned *>(base + int64_t(p.block_size) * kDim + off * 4),
-                   s > -127 ? uint32_t(s + 127) << 23 : 0x00400000u);
+            st_stream4_in(base + int64_t(p.block_size) * kDim + off * 4,
+                          s > -127 ? uint32_t(s + 127) << 23 : 0x00400000u, icache_span(p.cache, p),
+                          p.err);
     }
 }
 
@@ -178,7 +208,7 @@ __device__ __forceinline__ void gather_slots(const IParams &p, int64_t g, int ha
 #pragma unroll
     for (int j = 0; j < kGatherPairs; ++j) {
         const int64_t n = g * 2 * kGatherPairs + half + 2 * j;
-        slot[j] = n < p.rows ? __ldg(p.slots + n) : -1;
+        slot[j] = n < p.rows ? ldg_i64_in(p.slots + n, slots_span(p), p.err) : -1;
     }
 }
 
@@ -194,10 +224,10 @@ __device__ __forceinline__ void gather_load(const IParams &p, int h, const int64
             const int64_t blk = fastdiv(static_cast<uint32_t>(slot[j]), p.slot_div);
             const int64_t off = slot[j] - blk * p.block_size;
             const uint8_t *base = p.src + blk * int64_t(p.block_size) * kSlotBytes;
-            c[j] = load_codes<kWide>(base + off * kDim + 8 * h);
-            if (h == 0)
-                sc[j] = __ldcs(reinterpret_cast<const unsigned *>(
-                    base + int64_t(p.block_size) * kDim + off * 4));
+            c[j] = load_codes<kWide>(base + off * kDim + 8 * h, icache_span(p.src, p), p.err);
+            const uint8_t *sp = base + int64_t(p.block_size) * kDim + off * 4;
+            if (h == 0 && in_span(sp, 4, icache_span(p.src, p), p.err))
+                sc[j] = __ldcs(reinterpret_cast<const unsigned *>(sp));
         }
     }
 }
@@ -212,9 +242,9 @@ __device__ __forceinline__ void gather_store(const IParams &p, int h, int half, 
             continue;
         if (slot[j] >= p.num_slots && h == 0 && p.err != nullptr)
             atomicOr(p.err, DSV4_DEVERR_SLOT_RANGE);
-        __stcs(reinterpret_cast<uint2 *>(p.k_out + n * kDim) + h, c[j]);
+        st_stream8_in(reinterpret_cast<uint2 *>(p.k_out + n * kDim) + h, c[j], kout_span(p), p.err);
         if (h == 0)
-            __stcs(reinterpret_cast<unsigned *>(p.scale_out) + n, sc[j]);
+            st_stream4_in(reinterpret_cast<unsigned *>(p.scale_out) + n, sc[j], sout_span(p), p.err);
     }
 }
 
@@ -316,3 +346,5 @@ int launch_indexer_gather(const uint8_t *cache, int64_t num_blocks, int32_t bloc
 }
 
 }  // namespace dsv4
+
+DSV4_BOUNDS_FLAG_READER(bounds_flag_indexer)

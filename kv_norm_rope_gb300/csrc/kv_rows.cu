@@ -54,10 +54,10 @@ __device__ __forceinline__ int wq_index(int u, int part, int g)
 }
 
 // thread i < 64 widens the 8 weights of dims [8i, 8i + 8): u = i / 8, g = i % 8
-__device__ __forceinline__ void stage_weight_q(const uint16_t *w, int i, float4 *w_smem)
+__device__ __forceinline__ void stage_weight_q(const KParams &p, int i, float4 *w_smem)
 {
     float f[8];
-    widen8(__ldg(reinterpret_cast<const uint4 *>(w) + i), f);
+    widen8(ldg16_in(reinterpret_cast<const uint4 *>(p.w) + i, w_span(p), p.err), f);
     const int u = i >> 3, g = i & 7;
     w_smem[wq_index(u, 0, g)] = make_float4(f[0], f[1], f[2], f[3]);
     w_smem[wq_index(u, 1, g)] = make_float4(f[4], f[5], f[6], f[7]);
@@ -223,25 +223,29 @@ __device__ __forceinline__ void quarter_row_fp8(const KParams &p, int lane, bool
     const int64_t off = slot - blk * p.block_size;
     uint8_t *cbase = p.cache + blk * int64_t(p.block_size) * DSV4_FP8_SLOT_BYTES;
     uint8_t *data = cbase + off * DSV4_FP8_DATA_BYTES;
+    const Span cspan = cache_span<DSV4_STORE_FP8>(p);
 #pragma unroll
     for (int u = 0; u < 7; ++u) {
         const float ku = pow2_neg(s[u]);
-        st_stream8(data + 64 * u + 8 * g,
-                   make_uint2(e4m3x4_rn(v[u][0] * ku, v[u][1] * ku, v[u][2] * ku, v[u][3] * ku),
-                              e4m3x4_rn(v[u][4] * ku, v[u][5] * ku, v[u][6] * ku, v[u][7] * ku)));
+        st_stream8_in(data + 64 * u + 8 * g,
+                      make_uint2(e4m3x4_rn(v[u][0] * ku, v[u][1] * ku, v[u][2] * ku, v[u][3] * ku),
+                                 e4m3x4_rn(v[u][4] * ku, v[u][5] * ku, v[u][6] * ku, v[u][7] * ku)),
+                      cspan, p.err);
     }
     // rope dims stay bf16; 8-byte stores keep any block_size legal
     uint8_t *tail = data + DSV4_NOPE_DIM + 16 * g;
-    st_stream8(tail, make_uint2(bf16x2_rn(v[7][0], v[7][1]), bf16x2_rn(v[7][2], v[7][3])));
-    st_stream8(tail + 8, make_uint2(bf16x2_rn(v[7][4], v[7][5]), bf16x2_rn(v[7][6], v[7][7])));
+    st_stream8_in(tail, make_uint2(bf16x2_rn(v[7][0], v[7][1]), bf16x2_rn(v[7][2], v[7][3])), cspan,
+                  p.err);
+    st_stream8_in(tail + 8, make_uint2(bf16x2_rn(v[7][4], v[7][5]), bf16x2_rn(v[7][6], v[7][7])),
+                  cspan, p.err);
     if (g == 0) {
         // byte b of the scale word is block b's exponent; byte 7 stays 0
         const uint32_t lo = uint32_t(s[0] + 127) | (uint32_t(s[1] + 127) << 8) |
                             (uint32_t(s[2] + 127) << 16) | (uint32_t(s[3] + 127) << 24);
         const uint32_t hi =
             uint32_t(s[4] + 127) | (uint32_t(s[5] + 127) << 8) | (uint32_t(s[6] + 127) << 16);
-        st_stream8(cbase + int64_t(p.block_size) * DSV4_FP8_DATA_BYTES + off * DSV4_FP8_SCALE_BYTES,
-                   make_uint2(lo, hi));
+        st_stream8_in(cbase + int64_t(p.block_size) * DSV4_FP8_DATA_BYTES + off * DSV4_FP8_SCALE_BYTES,
+                      make_uint2(lo, hi), cspan, p.err);
     }
 }
 
@@ -269,8 +273,8 @@ __device__ __forceinline__ void kv_quad_row(const KParams &p, int lane, int64_t 
     float4 cv = make_float4(0.f, 0.f, 0.f, 0.f), sv = cv;
     if (active) {
         const float *cs = p.cs + pos * DSV4_ROPE_DIM + 4 * g;
-        cv = __ldg(reinterpret_cast<const float4 *>(cs));
-        sv = __ldg(reinterpret_cast<const float4 *>(cs + DSV4_ROPE_DIM / 2));
+        cv = ldg_f4_in(cs, cs_span(p), p.err);
+        sv = ldg_f4_in(cs + DSV4_ROPE_DIM / 2, cs_span(p), p.err);
     }
     float v[8][8];
     quarter_values<kKvNorm>(p, g, x, cv, sv, w_smem, v);
@@ -279,7 +283,7 @@ __device__ __forceinline__ void kv_quad_row(const KParams &p, int lane, int64_t 
             uint16_t *row = reinterpret_cast<uint16_t *>(p.cache) + slot * kHead;
 #pragma unroll
             for (int u = 0; u < 8; ++u)
-                st_stream16(row + 64 * u + 8 * g, bf16x8_rn(v[u]));
+                st_stream16_in(row + 64 * u + 8 * g, bf16x8_rn(v[u]), cache_span<kStore>(p), p.err);
         }
     } else {
         quarter_row_fp8<kKvNorm>(p, lane, active, t, slot, v);
@@ -327,8 +331,12 @@ __global__ void __launch_bounds__(kKvThreads, kKvCtasPerSm) kv_rows_kernel(const
         const int64_t t0 = 4 * (first + j * total);
         const uint32_t bytes = uint32_t(T - t0 < 4 ? T - t0 : 4) * (DSV4_HEAD_DIM * 2);
         uint64_t *bar = &bars[j % kKvStages];
-        mbar_arrive_expect_tx(bar, bytes);
-        bulk_load(stages + (j % kKvStages) * kItemBytes, p.kv + t0 * kHead, bytes, bar);
+        if (in_span(p.kv + t0 * kHead, bytes, kv_span(p), p.err)) {
+            mbar_arrive_expect_tx(bar, bytes);
+            bulk_load(stages + (j % kKvStages) * kItemBytes, p.kv + t0 * kHead, bytes, bar);
+        } else {
+            mbar_arrive(bar);  // checked build: the copy is skipped, its phase completes empty
+        }
     };
     int64_t issued = mine < kKvStages ? mine : kKvStages;
     if (lane == 0)
@@ -336,21 +344,21 @@ __global__ void __launch_bounds__(kKvThreads, kKvCtasPerSm) kv_rows_kernel(const
             issue(j);
 
     int64_t t = 4 * first + c;
-    int64_t pos = t < T ? __ldg(p.pos + t) : 0;
-    int64_t slot = t < T ? __ldg(p.slot + t) : -1;
+    int64_t pos = t < T ? ldg_i64_in(p.pos + t, pos_span(p), p.err) : 0;
+    int64_t slot = t < T ? ldg_i64_in(p.slot + t, slot_span(p), p.err) : -1;
     // the first copies and metadata are in flight while the CTA stages the
     // weight; the barriers' other lanes and the weight wait for the CTA barrier
     if (kKvNorm) {
         for (int i = threadIdx.x; i < 64; i += kKvThreads)
-            stage_weight_q(p.w, i, w_smem);
+            stage_weight_q(p, i, w_smem);
     }
     __syncthreads();
     for (int64_t j = 0; j < mine; ++j) {
         // the next item's metadata, one item ahead
         const int64_t tn = t + 4 * total;
         const bool next_live = j + 1 < mine && tn < T;
-        const int64_t pos_n = next_live ? __ldg(p.pos + tn) : 0;
-        const int64_t slot_n = next_live ? __ldg(p.slot + tn) : -1;
+        const int64_t pos_n = next_live ? ldg_i64_in(p.pos + tn, pos_span(p), p.err) : 0;
+        const int64_t slot_n = next_live ? ldg_i64_in(p.slot + tn, slot_span(p), p.err) : -1;
 
         const int s = int(j % kKvStages);
         if (!mbar_wait(&bars[s], uint32_t(j / kKvStages) & 1)) {
@@ -459,3 +467,5 @@ int launch_kv_rows(int store_mode, const LaunchArgs &a, int64_t max_ctas, cudaSt
 }
 
 }  // namespace dsv4
+
+DSV4_BOUNDS_FLAG_READER(bounds_flag_kv_rows)

@@ -43,4 +43,13 @@ int launch_indexer_gather(const uint8_t *cache, int64_t num_blocks, int32_t bloc
 // cycles (clamped to the kernels' own limit), then flags DSV4_DEVERR_TIMEOUT.
 int launch_wait_check(int64_t max_cycles, int32_t *err, cudaStream_t stream);
 
+// The checked build's record of skipped accesses, one reader per kernel file
+// (DSV4_BOUNDS_FLAG_READER of bounds.cuh); -1 in the release build.
+int bounds_flag_fused(int reset);
+int bounds_flag_half(int reset);
+int bounds_flag_kv_rows(int reset);
+int bounds_flag_gather(int reset);
+int bounds_flag_indexer(int reset);
+int bounds_flag_mxfp8(int reset);
+
 }  // namespace dsv4

@@ -66,7 +66,7 @@ __global__ void __launch_bounds__(256, 3) qnorm_rope_kv_insert_kernel(const KPar
     const int warps_per_cta = blockDim.x >> 5;
     if (kSmemW && kKvNorm) {
         for (int i = threadIdx.x; i < 64; i += blockDim.x)
-            w_smem[i] = __ldg(reinterpret_cast<const uint4 *>(p.w) + i);
+            w_smem[i] = ldg16_in(reinterpret_cast<const uint4 *>(p.w) + i, w_span(p), p.err);
         __syncthreads();
     }
     const int64_t H = p.num_heads;
@@ -87,11 +87,11 @@ __global__ void __launch_bounds__(256, 3) qnorm_rope_kv_insert_kernel(const KPar
         const int64_t o = it - period * P;
         if (period < T && o == 0) {
             const int64_t t = period;
-            const int64_t pos = __ldg(p.pos + t);
-            const int64_t slot = __ldg(p.slot + t);
+            const int64_t pos = ldg_i64_in(p.pos + t, pos_span(p), p.err);
+            const int64_t slot = ldg_i64_in(p.slot + t, slot_span(p), p.err);
             const uint16_t *src = p.kv + t * kHead;
-            const uint4 xa = ld_stream16(src + 8 * lane);
-            const uint4 xb = ld_stream16(src + 256 + 8 * lane);
+            const uint4 xa = ld_stream16_in(src + 8 * lane, kv_span(p), p.err);
+            const uint4 xb = ld_stream16_in(src + 256 + 8 * lane, kv_span(p), p.err);
             kv_row<kStore, kSmemW, kKvNorm>(p, lane, t, pos, slot, xa, xb, w_smem);
             continue;
         }
@@ -111,15 +111,15 @@ __global__ void __launch_bounds__(256, 3) qnorm_rope_kv_insert_kernel(const KPar
         }
 #pragma unroll
         for (int j = 0; j < kRows; ++j)
-            pos[j] = r0 + j < q_rows ? __ldg(p.pos + t[j]) : 0;
+            pos[j] = r0 + j < q_rows ? ldg_i64_in(p.pos + t[j], pos_span(p), p.err) : 0;
         // all row loads back to back: no dependency between them
         uint4 a[kRows], b[kRows];
 #pragma unroll
         for (int j = 0; j < kRows; ++j) {
             if (r0 + j < q_rows) {
                 const uint16_t *src = p.q + (r0 + j) * kHead;
-                a[j] = ld_stream16(src + 8 * lane);
-                b[j] = ld_stream16(src + 256 + 8 * lane);
+                a[j] = ld_stream16_in(src + 8 * lane, q_span(p), p.err);
+                b[j] = ld_stream16_in(src + 256 + 8 * lane, q_span(p), p.err);
             } else {
                 a[j] = make_uint4(0u, 0u, 0u, 0u);
                 b[j] = a[j];
@@ -136,8 +136,8 @@ __global__ void __launch_bounds__(256, 3) qnorm_rope_kv_insert_kernel(const KPar
             uint4 out_a, out_b;
             q_row(p, lane, a[j], b[j], cv, sv, out_a, out_b);
             uint16_t *dst = p.q + (r0 + j) * kHead;
-            st_stream16(dst + 8 * lane, out_a);
-            st_stream16(dst + 256 + 8 * lane, out_b);
+            st_stream16_in(dst + 8 * lane, out_a, q_span(p), p.err);
+            st_stream16_in(dst + 256 + 8 * lane, out_b, q_span(p), p.err);
         }
     }
 }
@@ -200,3 +200,5 @@ int launch(int store_mode, const dsv4_plan &plan, const LaunchArgs &a, cudaStrea
 }
 
 }  // namespace dsv4
+
+DSV4_BOUNDS_FLAG_READER(bounds_flag_fused)

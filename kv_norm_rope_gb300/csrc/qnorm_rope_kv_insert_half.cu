@@ -34,7 +34,7 @@ __global__ void __launch_bounds__(kHalfThreads, 3) qnorm_rope_kv_insert_half_ker
     __shared__ float4 w_smem[128];
     if (kKvNorm) {
         for (int i = threadIdx.x; i < 64; i += kHalfThreads)
-            stage_weight(p.w, i, w_smem);
+            stage_weight(p, i, w_smem);
         __syncthreads();
     }
     const int lane = threadIdx.x & 31, h = lane & 15, half = lane >> 4;
@@ -65,7 +65,7 @@ __global__ void __launch_bounds__(kHalfThreads, 3) qnorm_rope_kv_insert_half_ker
                 ++tok;
             }
             live[j] = r0 + 2 * j + half < q_rows;
-            pos[j] = live[j] ? __ldg(p.pos + tok) : 0;
+            pos[j] = live[j] ? ldg_i64_in(p.pos + tok, pos_span(p), p.err) : 0;
         }
         // all row loads back to back: no dependency between them
         uint4 x[kQPairs][4];
@@ -74,7 +74,8 @@ __global__ void __launch_bounds__(kHalfThreads, 3) qnorm_rope_kv_insert_half_ker
             const uint16_t *src = p.q + (r0 + 2 * j + half) * kHead + 8 * h;
 #pragma unroll
             for (int v = 0; v < 4; ++v)
-                x[j][v] = live[j] ? ld_stream16(src + 128 * v) : make_uint4(0u, 0u, 0u, 0u);
+                x[j][v] = live[j] ? ld_stream16_in(src + 128 * v, q_span(p), p.err)
+                                  : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
         for (int j = 0; j < kQPairs; ++j) {
@@ -91,7 +92,7 @@ __global__ void __launch_bounds__(kHalfThreads, 3) qnorm_rope_kv_insert_half_ker
                 uint16_t *dst = p.q + (r0 + 2 * j + half) * kHead + 8 * h;
 #pragma unroll
                 for (int v = 0; v < 4; ++v)
-                    st_stream16(dst + 128 * v, out[v]);
+                    st_stream16_in(dst + 128 * v, out[v], q_span(p), p.err);
             }
         }
     }
@@ -146,3 +147,5 @@ int launch_half(int store_mode, const LaunchArgs &a, int64_t ctas, cudaStream_t 
 }
 
 }  // namespace dsv4
+
+DSV4_BOUNDS_FLAG_READER(bounds_flag_half)

@@ -11,11 +11,44 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "bounds.cuh"
 #include "convert.cuh"
 #include "launch.h"
 
 namespace dsv4 {
 namespace {
+
+// The buffers of a launch, for the checked build's bounds tests (bounds.cuh).
+__device__ __forceinline__ Span q_span(const KParams &p)
+{
+    return Span{p.q, uint64_t(p.num_tokens) * uint64_t(p.num_heads) * 1024u};
+}
+__device__ __forceinline__ Span kv_span(const KParams &p)
+{
+    return Span{p.kv, uint64_t(p.num_tokens) * 1024u};
+}
+__device__ __forceinline__ Span w_span(const KParams &p)
+{
+    return Span{p.w, 1024u};
+}
+__device__ __forceinline__ Span pos_span(const KParams &p)
+{
+    return Span{p.pos, uint64_t(p.num_tokens) * 8u};
+}
+__device__ __forceinline__ Span slot_span(const KParams &p)
+{
+    return Span{p.slot, uint64_t(p.num_tokens) * 8u};
+}
+__device__ __forceinline__ Span cs_span(const KParams &p)
+{
+    return Span{p.cs, uint64_t(p.max_pos) * 256u};
+}
+template <int kStore>
+__device__ __forceinline__ Span cache_span(const KParams &p)
+{
+    return Span{p.cache, uint64_t(p.num_slots) *
+                             (kStore == DSV4_STORE_BF16 ? DSV4_BF16_SLOT_BYTES : DSV4_FP8_SLOT_BYTES)};
+}
 
 
 constexpr int kHead = DSV4_HEAD_DIM;
@@ -296,8 +329,10 @@ __device__ __noinline__ int exact_scale_bumps_fp64(const KParams &p, int lane, i
 {
     const uint4 *row = reinterpret_cast<const uint4 *>(p.kv + t * kHead);
     const uint4 *wv = reinterpret_cast<const uint4 *>(p.w);
-    const uint4 xa = __ldg(row + lane), xb = __ldg(row + 32 + lane);
-    const uint4 wa = __ldg(wv + lane), wb = __ldg(wv + 32 + lane);
+    const uint4 xa = ldg16_in(row + lane, kv_span(p), p.err);
+    const uint4 xb = ldg16_in(row + 32 + lane, kv_span(p), p.err);
+    const uint4 wa = ldg16_in(wv + lane, w_span(p), p.err);
+    const uint4 wb = ldg16_in(wv + 32 + lane, w_span(p), p.err);
     // rolled loops: this path is rare, its registers are not
     double ss = 0.0;
 #pragma unroll 1
@@ -341,8 +376,10 @@ __device__ __noinline__ int exact_scale_bumps(const KParams &p, int lane, int64_
 {
     const uint4 *row = reinterpret_cast<const uint4 *>(p.kv + t * kHead);
     const uint4 *wv = reinterpret_cast<const uint4 *>(p.w);
-    const uint4 xa = __ldg(row + lane), xb = __ldg(row + 32 + lane);
-    const uint4 wa = __ldg(wv + lane), wb = __ldg(wv + 32 + lane);
+    const uint4 xa = ldg16_in(row + lane, kv_span(p), p.err);
+    const uint4 xb = ldg16_in(row + 32 + lane, kv_span(p), p.err);
+    const uint4 wa = ldg16_in(wv + lane, w_span(p), p.err);
+    const uint4 wb = ldg16_in(wv + 32 + lane, w_span(p), p.err);
     float x[16];
     widen8(xa, x);
     widen8(xb, x + 8);
@@ -428,9 +465,11 @@ __device__ __forceinline__ void kv_values(const KParams &p, int lane, uint4 xa, 
         return;
     }
     const float r = row_inv_rms(p.eps, [&] { return warp_sumsq16(v); }, [&] { scale_16(v); });
-    const uint4 wa = kSmemW ? w_smem[lane] : __ldg(reinterpret_cast<const uint4 *>(p.w) + lane);
+    const uint4 wa = kSmemW ? w_smem[lane]
+                            : ldg16_in(reinterpret_cast<const uint4 *>(p.w) + lane, w_span(p), p.err);
     const uint4 wb =
-        kSmemW ? w_smem[32 + lane] : __ldg(reinterpret_cast<const uint4 *>(p.w) + 32 + lane);
+        kSmemW ? w_smem[32 + lane]
+               : ldg16_in(reinterpret_cast<const uint4 *>(p.w) + 32 + lane, w_span(p), p.err);
     float w[16];
     widen8(wa, w);
     widen8(wb, w + 8);
@@ -476,16 +515,16 @@ __device__ __forceinline__ void kv_row(const KParams &p, int lane, int64_t t, in
     float4 cv = make_float4(0.f, 0.f, 0.f, 0.f), sv = cv;
     if (rope_lane) {
         const float *cs = p.cs + pos * DSV4_ROPE_DIM + 4 * (lane - 24);
-        cv = __ldg(reinterpret_cast<const float4 *>(cs));
-        sv = __ldg(reinterpret_cast<const float4 *>(cs + DSV4_ROPE_DIM / 2));
+        cv = ldg_f4_in(cs, cs_span(p), p.err);
+        sv = ldg_f4_in(cs + DSV4_ROPE_DIM / 2, cs_span(p), p.err);
     }
     float v[16];
     kv_values<kSmemW, kKvNorm>(p, lane, xa, xb, cv, sv, w_smem, v);
 
     if (kStore == DSV4_STORE_BF16) {
         uint16_t *row = reinterpret_cast<uint16_t *>(p.cache) + slot * kHead;
-        st_stream16(row + 8 * lane, bf16x8_rn(v));
-        st_stream16(row + 256 + 8 * lane, bf16x8_rn(v + 8));
+        st_stream16_in(row + 8 * lane, bf16x8_rn(v), cache_span<kStore>(p), p.err);
+        st_stream16_in(row + 256 + 8 * lane, bf16x8_rn(v + 8), cache_span<kStore>(p), p.err);
         return;
     }
 
@@ -509,9 +548,10 @@ __device__ __forceinline__ void kv_row(const KParams &p, int lane, int64_t t, in
         if (g1.near)
             g1.s = clamp_s(g1.e - 8 + ((bumps >> 1) & 1));
         // recompute v (same bits) instead of keeping it live across the call
-        kv_values<kSmemW, kKvNorm>(p, lane, __ldg(reinterpret_cast<const uint4 *>(src) + lane),
-                          __ldg(reinterpret_cast<const uint4 *>(src) + 32 + lane), cv, sv,
-                          w_smem, v);
+        kv_values<kSmemW, kKvNorm>(
+            p, lane, ldg16_in(reinterpret_cast<const uint4 *>(src) + lane, kv_span(p), p.err),
+            ldg16_in(reinterpret_cast<const uint4 *>(src) + 32 + lane, kv_span(p), p.err), cv, sv,
+            w_smem, v);
     }
 
     // 0 <= slot < num_slots <= 2^32 here, so the quotient is a 32-bit one
@@ -520,20 +560,24 @@ __device__ __forceinline__ void kv_row(const KParams &p, int lane, int64_t t, in
     uint8_t *base = p.cache + blk * int64_t(p.block_size) * DSV4_FP8_SLOT_BYTES;
     uint8_t *data = base + off * DSV4_FP8_DATA_BYTES;
 
+    const Span cspan = cache_span<kStore>(p);
     const float k0 = pow2_neg(g0.s);
-    st_stream8(data + 8 * lane,
-               make_uint2(e4m3x4_rn(v[0] * k0, v[1] * k0, v[2] * k0, v[3] * k0),
-                          e4m3x4_rn(v[4] * k0, v[5] * k0, v[6] * k0, v[7] * k0)));
+    st_stream8_in(data + 8 * lane,
+                  make_uint2(e4m3x4_rn(v[0] * k0, v[1] * k0, v[2] * k0, v[3] * k0),
+                             e4m3x4_rn(v[4] * k0, v[5] * k0, v[6] * k0, v[7] * k0)),
+                  cspan, p.err);
     if (!rope_lane) {
         const float k1 = pow2_neg(g1.s);
-        st_stream8(data + 256 + 8 * lane,
-                   make_uint2(e4m3x4_rn(v[8] * k1, v[9] * k1, v[10] * k1, v[11] * k1),
-                              e4m3x4_rn(v[12] * k1, v[13] * k1, v[14] * k1, v[15] * k1)));
+        st_stream8_in(data + 256 + 8 * lane,
+                      make_uint2(e4m3x4_rn(v[8] * k1, v[9] * k1, v[10] * k1, v[11] * k1),
+                                 e4m3x4_rn(v[12] * k1, v[13] * k1, v[14] * k1, v[15] * k1)),
+                      cspan, p.err);
     } else {
         // rope dims stay bf16; 8-byte stores keep any block_size legal
         uint8_t *tail = data + DSV4_NOPE_DIM + 16 * (lane - 24);
-        st_stream8(tail, make_uint2(bf16x2_rn(v[8], v[9]), bf16x2_rn(v[10], v[11])));
-        st_stream8(tail + 8, make_uint2(bf16x2_rn(v[12], v[13]), bf16x2_rn(v[14], v[15])));
+        st_stream8_in(tail, make_uint2(bf16x2_rn(v[8], v[9]), bf16x2_rn(v[10], v[11])), cspan, p.err);
+        st_stream8_in(tail + 8, make_uint2(bf16x2_rn(v[12], v[13]), bf16x2_rn(v[14], v[15])), cspan,
+                      p.err);
     }
 
     // scale word: byte b is the exponent of block b, held by lane 8*(b%4) of
@@ -544,8 +588,8 @@ __device__ __forceinline__ void kv_row(const KParams &p, int lane, int64_t t, in
     const uint32_t hi =
         __reduce_or_sync(kFull, leader && !rope_lane ? uint32_t(g1.s + 127) << shift : 0u);
     if (lane == 0)
-        st_stream8(base + int64_t(p.block_size) * DSV4_FP8_DATA_BYTES + off * DSV4_FP8_SCALE_BYTES,
-                   make_uint2(lo, hi));
+        st_stream8_in(base + int64_t(p.block_size) * DSV4_FP8_DATA_BYTES + off * DSV4_FP8_SCALE_BYTES,
+                      make_uint2(lo, hi), cspan, p.err);
 }
 
 
@@ -584,8 +628,8 @@ __device__ __forceinline__ void load_cs(const KParams &p, int lane, int64_t pos,
     sv = cv;
     if (lane >= 24) {
         const float *cs = p.cs + pos * DSV4_ROPE_DIM + 4 * (lane - 24);
-        cv = __ldg(reinterpret_cast<const float4 *>(cs));
-        sv = __ldg(reinterpret_cast<const float4 *>(cs + DSV4_ROPE_DIM / 2));
+        cv = ldg_f4_in(cs, cs_span(p), p.err);
+        sv = ldg_f4_in(cs + DSV4_ROPE_DIM / 2, cs_span(p), p.err);
     }
 }
 

@@ -38,6 +38,7 @@ class Report:
     q_ulp1: int = 0
     fp8_elems: int = 0
     fp8_step1: int = 0
+    q_rows: int = 0  # q head rows compared (set by the caller that compares q)
 
     def fail(self, msg: str):
         self.ok = False

@@ -141,6 +141,7 @@ def compare_q(inp: Inputs, q_tokens: np.ndarray, gpu_q: np.ndarray, ref_q: np.nd
         if not np.array_equal(gpu_q[~valid_pos], inp.q[q_tokens][~valid_pos]):
             rep.fail("q rows of tokens with out-of-range positions changed")
     compare.compare_bf16(gpu_q[valid_pos], ref_q[valid_pos], "q", rep)
+    rep.q_rows += int(gpu_q.shape[0]) * int(gpu_q.shape[1])
     return rep
 
 
