@@ -35,9 +35,12 @@
  *  - Preconditions that are not checked: non-negative slots are distinct (if
  *    two tokens share a slot, which one's row lands is unspecified); q does
  *    not overlap kv, the cache or the metadata arrays; inputs are finite and
- *    sum(x^2) of a row stays below 3.4e38.  With eps = 0 a row of zeros has
- *    no norm: 1/sqrt(0) is infinite and its outputs are NaN, as the definition
- *    gives them.
+ *    sum(x^2) of a row stays below 3.4e38; each kv_norm_weight element is 0 or
+ *    has magnitude in [2^-9, 2^64), so that every product x * w of a KV element
+ *    and its weight is exact in fp32 (the kernels form v = (x * w) * r).  With
+ *    eps = 0 a row of zeros has no norm: 1/sqrt(0) is infinite and its outputs
+ *    are NaN, as the definition gives them; rows of tiny elements (down to
+ *    bf16 subnormals) are normalised like any other row.
  *  - Every paged cache holds at most 2^32 slots (num_blocks * block_size <=
  *    2^32; larger returns DSV4_ERR_SHAPE).  At 132 bytes or more per slot such
  *    a cache exceeds one GPU's memory, and the bound lets the kernels split a

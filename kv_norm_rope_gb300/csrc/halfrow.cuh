@@ -25,14 +25,6 @@
 namespace dsv4 {
 namespace {
 
-// The weight in shared memory as fp32 (exact), laid out so that the 16 lanes
-// of a half-warp read 16 consecutive float4: lane h's 8 weights of vector j
-// are float4s (2j) * 16 + h and (2j + 1) * 16 + h.
-__device__ __forceinline__ int w_index(int j, int part, int h)
-{
-    return (2 * j + part) * 16 + h;
-}
-
 __device__ __forceinline__ float half_sum(float v)
 {
 #pragma unroll
@@ -44,31 +36,16 @@ __device__ __forceinline__ float half_sum(float v)
 // The row's sum of squares in the whole-warp order: lane h's vectors (0, 2)
 // are whole-warp lane h's, its vectors (1, 3) whole-warp lane h + 16's; their
 // sum is the butterfly's xor-16 level, then xor 8, 4, 2, 1 inside the half.
-__device__ __forceinline__ float half_sumsq(const float (*v)[8])
+__device__ __forceinline__ float half_sumsq(const uint4 *x)
 {
-    float sa = 0.0f, sb = 0.0f;
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-        sa = __fmaf_rn(v[0][k], v[0][k], sa);
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-        sa = __fmaf_rn(v[2][k], v[2][k], sa);
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-        sb = __fmaf_rn(v[1][k], v[1][k], sb);
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-        sb = __fmaf_rn(v[3][k], v[3][k], sb);
-    return half_sum(__fadd_rn(sa, sb));
+    return half_sum(__fadd_rn(lane_sumsq(x[0], x[2]), lane_sumsq(x[1], x[3])));
 }
 
-__device__ __forceinline__ void half_scale(float (*v)[8])
+__device__ __forceinline__ void half_scale(uint4 *x)
 {
 #pragma unroll
     for (int j = 0; j < 4; ++j)
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            v[j][k] = __fmul_rn(v[j][k], 0x1p64f);
+        x[j] = scale8_2p64(x[j]);
 }
 
 // cos and sin of the 4 pairs held by a rope lane (h >= 8) at row pos; zeros
@@ -85,48 +62,41 @@ __device__ __forceinline__ void half_load_cs(const KParams &p, int h, bool activ
     }
 }
 
-// v = x * r * w (or x) for the lane's 32 dims of its row, rope dims rotated
+// The lane's products for its row in the half-warp layout (vector j: dims
+// [128j + 8h, 128j + 8h + 8)), their maxima t[j] = max |xw[j]| (0 for the rope
+// vector of rope lanes) and the row's r: xw = x * w, except that rope lanes
+// (h >= 8) get their dims 448.. final in xw[3] (x * w rotated, then scaled by
+// r).  r comes first and the products after it, so x and the products are not
+// held together (a tiny row rescales x in place first).  With no norm, xw = x
+// and r = 1.  w_smem: the weight as packed bf16 in dim order.  The steps of
+// kv_products, so the same bits.
 template <bool kKvNorm>
-__device__ __forceinline__ void half_row_values(const KParams &p, int h, const uint4 *x, float4 cv,
-                                                float4 sv, const float4 *w_smem, float (*v)[8])
+__device__ __forceinline__ float half_products(const KParams &p, int h, uint4 *x, float4 cv,
+                                               float4 sv, const uint4 *w_smem, float (*xw)[8],
+                                               float *t)
 {
+    const bool rope_lane = h >= 8;
+    float r = 1.0f;
+    if (kKvNorm)
+        r = row_inv_rms(p.eps, [&] { return half_sumsq(x); }, [&] { half_scale(x); });
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        if (kKvNorm)
+            prod8(x[j], w_smem[16 * j + h], xw[j]);
+        else
+            widen8(x[j], xw[j]);
+    }
 #pragma unroll
     for (int j = 0; j < 4; ++j)
-        widen8(x[j], v[j]);
-    const bool rope_lane = h >= 8;
-    if (!kKvNorm) {
-        if (rope_lane) {
-            float u[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                u[k] = v[3][k];
-            rope8_scaled(u, cv, sv, 1.0f, v[3]);
-        }
-        return;
-    }
-    const float r = row_inv_rms(p.eps, [&] { return half_sumsq(v); }, [&] { half_scale(v); });
-#pragma unroll
-    for (int j = 0; j < 3; ++j) {
-        const float4 wa = w_smem[w_index(j, 0, h)], wb = w_smem[w_index(j, 1, h)];
-        const float w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            v[j][k] = __fmul_rn(__fmul_rn(v[j][k], r), w[k]);
-    }
-    const float4 wa = w_smem[w_index(3, 0, h)], wb = w_smem[w_index(3, 1, h)];
-    const float w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
-    if (!rope_lane) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            v[3][k] = __fmul_rn(__fmul_rn(v[3][k], r), w[k]);
-    } else {
-        // x*w is exact in fp32; rotate, then scale
+        t[j] = (j < 3 || !rope_lane) ? absmax8(xw[j]) : 0.0f;
+    if (rope_lane) {
         float u[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-            u[k] = __fmul_rn(v[3][k], w[k]);
-        rope8_scaled(u, cv, sv, r, v[3]);
+            u[k] = xw[3][k];
+        rope8_scaled(u, cv, sv, r, xw[3]);
     }
+    return r;
 }
 
 // The exact decision for blocks too close to a boundary in fp32 (rare), for
@@ -173,23 +143,18 @@ __device__ __noinline__ int half_exact_bumps(const KParams &p, int lane, int64_t
 }
 
 // The FP8 store of a half-warp row: block scales, E4M3 payload, bf16 rope
-// tail and the scale word.
+// tail and the scale word.  xw, r: from half_products.
 template <bool kKvNorm>
 __device__ __forceinline__ void half_row_fp8(const KParams &p, int h, bool active, int64_t t,
-                                             int64_t slot, float (*v)[8])
+                                             int64_t slot, const float (*xw)[8], const float *tmax,
+                                             float r)
 {
     const bool rope_lane = h >= 8;
 
     ScaleGuess g[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        float am = 0.0f;
-        if (j < 3 || !rope_lane) {
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                am = fmaxf(am, fabsf(v[j][k]));
-        }
-        g[j] = ue8m0_guess(group8_max(am));  // rope lanes: amax 0, never near
+        g[j] = ue8m0_guess(__fmul_rn(group8_max(tmax[j]), r));  // rope lanes: amax 0, never near
         g[j].near = g[j].near && active;
     }
     if (kKvNorm && __any_sync(kFull, g[0].near || g[1].near || g[2].near || g[3].near)) {
@@ -211,6 +176,13 @@ __device__ __forceinline__ void half_row_fp8(const KParams &p, int h, bool activ
     const uint32_t hi_part = h == 0 ? (b2 | (b3 << 16)) : (b2 << 8);
     const uint32_t lo = lo_part | __shfl_xor_sync(kFull, lo_part, 8);
     const uint32_t hi = hi_part | __shfl_xor_sync(kFull, hi_part, 8);
+    // a block below kTwoStepBelow anywhere in the warp: the two-step payload form
+    // (voted by every lane before the inactive ones leave)
+    bool slow = false;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        slow = slow || ((j < 3 || !rope_lane) && g[j].s < kTwoStepBelow);
+    slow = __any_sync(kFull, active && slow);
 
     if (!active)
         return;
@@ -219,22 +191,29 @@ __device__ __forceinline__ void half_row_fp8(const KParams &p, int h, bool activ
     uint8_t *base = p.cache + blk * int64_t(p.block_size) * DSV4_FP8_SLOT_BYTES;
     uint8_t *data = base + off * DSV4_FP8_DATA_BYTES;
     const Span cspan = cache_span<DSV4_STORE_FP8>(p);
+    if (slow) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        if (j == 3 && rope_lane)
-            break;
-        const float kj = pow2_neg(g[j].s);
-        st_stream8_in(data + 128 * j + 8 * h,
-                      make_uint2(e4m3x4_rn(v[j][0] * kj, v[j][1] * kj, v[j][2] * kj, v[j][3] * kj),
-                                 e4m3x4_rn(v[j][4] * kj, v[j][5] * kj, v[j][6] * kj, v[j][7] * kj)),
-                      cspan, p.err);
+        for (int j = 0; j < 4; ++j) {
+            if (j == 3 && rope_lane)
+                break;
+            st_stream8_in(data + 128 * j + 8 * h, e4m3x8_block(xw[j], r, g[j].s), cspan, p.err);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (j == 3 && rope_lane)
+                break;
+            st_stream8_in(data + 128 * j + 8 * h, e4m3x8_of(xw[j], __fmul_rn(r, pow2_neg(g[j].s))),
+                          cspan, p.err);
+        }
     }
     if (rope_lane) {
         // rope dims stay bf16; 8-byte stores keep any block_size legal
         uint8_t *tail = data + DSV4_NOPE_DIM + 16 * (h - 8);
-        st_stream8_in(tail, make_uint2(bf16x2_rn(v[3][0], v[3][1]), bf16x2_rn(v[3][2], v[3][3])),
+        st_stream8_in(tail, make_uint2(bf16x2_rn(xw[3][0], xw[3][1]), bf16x2_rn(xw[3][2], xw[3][3])),
                       cspan, p.err);
-        st_stream8_in(tail + 8, make_uint2(bf16x2_rn(v[3][4], v[3][5]), bf16x2_rn(v[3][6], v[3][7])),
+        st_stream8_in(tail + 8,
+                      make_uint2(bf16x2_rn(xw[3][4], xw[3][5]), bf16x2_rn(xw[3][6], xw[3][7])),
                       cspan, p.err);
     }
     if (h == 0)
@@ -246,34 +225,32 @@ __device__ __forceinline__ void half_row_fp8(const KParams &p, int h, bool activ
 // position and slot); inactive halves still take part in every shuffle.
 template <int kStore, bool kKvNorm>
 __device__ __forceinline__ void half_row(const KParams &p, int h, bool active, int64_t t,
-                                         int64_t pos, int64_t slot, const uint4 *x,
-                                         const float4 *w_smem)
+                                         int64_t pos, int64_t slot, uint4 *x, const uint4 *w_smem)
 {
     float4 cv, sv;
     half_load_cs(p, h, active, pos, cv, sv);
-    float v[4][8];
-    half_row_values<kKvNorm>(p, h, x, cv, sv, w_smem, v);
+    float xw[4][8], tmax[4];
+    const float r = half_products<kKvNorm>(p, h, x, cv, sv, w_smem, xw, tmax);
 
     if constexpr (kStore == DSV4_STORE_BF16) {
         if (active) {
             uint16_t *row = reinterpret_cast<uint16_t *>(p.cache) + slot * kHead;
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-                st_stream16_in(row + 128 * j + 8 * h, bf16x8_rn(v[j]), cache_span<kStore>(p), p.err);
+                st_stream16_in(row + 128 * j + 8 * h,
+                               (j == 3 && h >= 8) ? bf16x8_rn(xw[3]) : bf16x8_scaled(xw[j], r),
+                               cache_span<kStore>(p), p.err);
         }
     } else {
-        half_row_fp8<kKvNorm>(p, h, active, t, slot, v);
+        half_row_fp8<kKvNorm>(p, h, active, t, slot, xw, tmax, r);
     }
 }
 
-// thread i < 64 widens the 8 weights of dims [8i, 8i + 8): j = i / 16, h = i % 16
-__device__ __forceinline__ void stage_weight(const KParams &p, int i, float4 *w_smem)
+// The weight as packed bf16 in dim order (thread i < 64 copies dims [8i, 8i + 8)):
+// lane h of a half reads vector j at 16j + h, 16 consecutive 16-byte words
+__device__ __forceinline__ void stage_weight(const KParams &p, int i, uint4 *w_smem)
 {
-    float f[8];
-    widen8(ldg16_in(reinterpret_cast<const uint4 *>(p.w) + i, w_span(p), p.err), f);
-    const int j = i >> 4, h = i & 15;
-    w_smem[w_index(j, 0, h)] = make_float4(f[0], f[1], f[2], f[3]);
-    w_smem[w_index(j, 1, h)] = make_float4(f[4], f[5], f[6], f[7]);
+    w_smem[i] = ldg16_in(reinterpret_cast<const uint4 *>(p.w) + i, w_span(p), p.err);
 }
 
 
@@ -283,7 +260,7 @@ __device__ __forceinline__ void stage_weight(const KParams &p, int i, float4 *w_
 // shuffle; a pair with no row to write skips the arithmetic (warp-uniform).
 template <int kStore, bool kKvNorm>
 __device__ __forceinline__ void kv_pair_item(const KParams &p, int h, int64_t t,
-                                             const float4 *w_smem)
+                                             const uint4 *w_smem)
 {
     const bool live = t < p.num_tokens;
     const int64_t pos = live ? ldg_i64_in(p.pos + t, pos_span(p), p.err) : 0;
@@ -305,17 +282,41 @@ __device__ __forceinline__ void kv_pair_item(const KParams &p, int h, int64_t t,
         half_row<kStore, kKvNorm>(p, h, active, t, pos, slot, x, w_smem);
 }
 
-// One q head row: y = x * r with the rope dims rotated first (compensated)
-// and then scaled, the operations of q_row on the same values; returns the
-// lane's four output vectors (bf16, round to nearest).
-__device__ __forceinline__ void q_half_row(const KParams &p, int h, const uint4 *x, float4 cv,
-                                           float4 sv, uint4 *out)
+// r of the kPairs q rows of this half (x[j]: the lane's vectors of row j), one
+// tiny-row vote for the group as in q_rows_inv_rms.
+template <int kPairs>
+__device__ __forceinline__ void q_half_rows_inv_rms(float eps, uint4 (*x)[4], float *r)
+{
+    float m[kPairs];
+    bool tiny = false;
+#pragma unroll
+    for (int j = 0; j < kPairs; ++j) {
+        m[j] = mean_sq(half_sumsq(x[j]), eps);
+        tiny = tiny || m[j] < kTinyMeanSq;
+    }
+    if (__any_sync(kFull, tiny)) {
+#pragma unroll
+        for (int j = 0; j < kPairs; ++j) {
+            if (__any_sync(kFull, m[j] < kTinyMeanSq))
+                m[j] = rescale_tiny(
+                    eps, m[j], [&] { return half_sumsq(x[j]); }, [&] { half_scale(x[j]); });
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < kPairs; ++j)
+        r[j] = __frsqrt_rn(m[j]);
+}
+
+// One q head row with its r: y = x * r with the rope dims rotated first
+// (compensated) and then scaled, the operations of q_row_out on the same
+// values; returns the lane's four output vectors (bf16, round to nearest).
+__device__ __forceinline__ void q_half_out(int h, const uint4 *x, float r, float4 cv, float4 sv,
+                                           uint4 *out)
 {
     float y[4][8];
 #pragma unroll
     for (int j = 0; j < 4; ++j)
         widen8(x[j], y[j]);
-    const float r = row_inv_rms(p.eps, [&] { return half_sumsq(y); }, [&] { half_scale(y); });
 #pragma unroll
     for (int j = 0; j < 3; ++j) {
 #pragma unroll

@@ -43,24 +43,14 @@ namespace dsv4 {
 namespace {
 
 constexpr int kKvThreads = 256;
-constexpr int kKvCtasPerSm = 2;  // 64 fp32 values per lane: up to 128 registers
+constexpr int kKvCtasPerSm = 2;
 
-// The weight in shared memory as fp32 (exact): lane g's 8 weights of vector u
-// are float4s (2u) * 8 + g and (2u + 1) * 8 + g, so the 8 lanes of a quarter
-// read 8 consecutive float4s (the four quarters read the same ones).
-__device__ __forceinline__ int wq_index(int u, int part, int g)
+// The weight as packed bf16 in dim order (thread i < 64 copies dims
+// [8i, 8i + 8)): lane g of a quarter reads vector u at 8u + g, 8 consecutive
+// 16-byte words (the four quarters read the same ones).
+__device__ __forceinline__ void stage_weight_q(const KParams &p, int i, uint4 *w_smem)
 {
-    return (2 * u + part) * 8 + g;
-}
-
-// thread i < 64 widens the 8 weights of dims [8i, 8i + 8): u = i / 8, g = i % 8
-__device__ __forceinline__ void stage_weight_q(const KParams &p, int i, float4 *w_smem)
-{
-    float f[8];
-    widen8(ldg16_in(reinterpret_cast<const uint4 *>(p.w) + i, w_span(p), p.err), f);
-    const int u = i >> 3, g = i & 7;
-    w_smem[wq_index(u, 0, g)] = make_float4(f[0], f[1], f[2], f[3]);
-    w_smem[wq_index(u, 1, g)] = make_float4(f[4], f[5], f[6], f[7]);
+    w_smem[i] = ldg16_in(reinterpret_cast<const uint4 *>(p.w) + i, w_span(p), p.err);
 }
 
 __device__ __forceinline__ float quarter_sum(float v)
@@ -74,62 +64,71 @@ __device__ __forceinline__ float quarter_sum(float v)
 // The row's sum of squares in the whole-warp order: the partials of whole-warp
 // lanes 8u + g (their vectors u and u + 4), the xor-16 and xor-8 levels as
 // (p0 + p2) + (p1 + p3), then xor 4, 2, 1 inside the quarter.
-__device__ __forceinline__ float quarter_sumsq(const float (*v)[8])
+__device__ __forceinline__ float quarter_sumsq(const uint4 *x)
 {
     float ps[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        float s = 0.0f;
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            s = __fmaf_rn(v[u][k], v[u][k], s);
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            s = __fmaf_rn(v[u + 4][k], v[u + 4][k], s);
-        ps[u] = s;
-    }
+    for (int u = 0; u < 4; ++u)
+        ps[u] = lane_sumsq(x[u], x[u + 4]);
     return quarter_sum(__fadd_rn(__fadd_rn(ps[0], ps[2]), __fadd_rn(ps[1], ps[3])));
 }
 
-// v = x * r * w (or x) for the lane's 64 dims of its row, rope dims rotated
-template <bool kKvNorm>
-__device__ __forceinline__ void quarter_values(const KParams &p, int g, const uint4 *x, float4 cv,
-                                               float4 sv, const float4 *w_smem, float (*v)[8])
+// max |x_k * w_k| over one 16-byte vector (the products are exact and then
+// dropped: the second pass forms them again where they are quantised)
+__device__ __forceinline__ float absmax_prod8(uint4 x, uint4 w)
 {
-#pragma unroll
-    for (int u = 0; u < 8; ++u)
-        widen8(x[u], v[u]);
+    float xw[8];
+    prod8(x, w, xw);
+    return absmax8(xw);
+}
+
+// Pass 1 of a quarter-warp row (vector u of lane g: dims [64u + 8g, 64u + 8g + 8)):
+// the block maxima t[u] = max |x * w| over the lane's dims of block u (u < 7;
+// t[7] = 0, the rope dims are not quantised) and the row's r.  Only the packed
+// row x is held: the products are formed again by the second pass, which keeps
+// the registers of a row to x plus one vector at a time.  A tiny row rescales x
+// (in place) and t with it.  With no norm, t[u] = max |x| and r = 1.  The values
+// are those of kv_products (exact products and maxima, the same sum order).
+template <bool kKvNorm>
+__device__ __forceinline__ float quarter_pass1(const KParams &p, int g, uint4 *x,
+                                               const uint4 *w_smem, float *t)
+{
+    t[7] = 0.0f;
     if constexpr (!kKvNorm) {
-        float t[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            t[k] = v[7][k];
-        rope8_scaled(t, cv, sv, 1.0f, v[7]);
-    } else {
-        const float r = row_inv_rms(p.eps, [&] { return quarter_sumsq(v); }, [&] {
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-#pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    v[u][k] = __fmul_rn(v[u][k], 0x1p64f);
-        });
 #pragma unroll
         for (int u = 0; u < 7; ++u) {
-            const float4 wa = w_smem[wq_index(u, 0, g)], wb = w_smem[wq_index(u, 1, g)];
-            const float w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                v[u][k] = __fmul_rn(__fmul_rn(v[u][k], r), w[k]);
+            float f[8];
+            widen8(x[u], f);
+            t[u] = absmax8(f);
         }
-        // rope dims: x*w is exact in fp32; rotate, then scale
-        const float4 wa = w_smem[wq_index(7, 0, g)], wb = w_smem[wq_index(7, 1, g)];
-        const float w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
-        float t[8];
+        return 1.0f;
+    } else {
+        const float sum = quarter_sumsq(x);
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-            t[k] = __fmul_rn(v[7][k], w[k]);
-        rope8_scaled(t, cv, sv, r, v[7]);
+        for (int u = 0; u < 7; ++u)
+            t[u] = absmax_prod8(x[u], w_smem[8 * u + g]);
+        float m = mean_sq(sum, p.eps);
+        if (__any_sync(kFull, m < kTinyMeanSq))
+            m = rescale_tiny(p.eps, m, [&] { return quarter_sumsq(x); }, [&] {
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    x[u] = scale8_2p64(x[u]);
+                    t[u] = __fmul_rn(t[u], 0x1p64f);
+                }
+            });
+        return __frsqrt_rn(m);
     }
+}
+
+// Pass 2, vector u: xw = x * w (or x with no norm), formed again
+template <bool kKvNorm>
+__device__ __forceinline__ void quarter_vec(const uint4 *x, const uint4 *w_smem, int g, int u,
+                                            float *xw)
+{
+    if (kKvNorm)
+        prod8(x[u], w_smem[8 * u + g], xw);
+    else
+        widen8(x[u], xw);
 }
 
 // Max of each of 8 values over the 8 lanes of a quarter, scattered: lane g
@@ -188,23 +187,16 @@ __device__ __noinline__ bool quarter_exact_bump(const KParams &p, int lane, int6
 }
 
 // The FP8 store of a quarter-warp row: block scales, E4M3 payload, bf16 rope
-// tail and the scale word.
+// tail and the scale word.  x: the row (as scaled by pass 1), tmax and r: from
+// pass 1, rope: the lane's rope dims, final.
 template <bool kKvNorm>
 __device__ __forceinline__ void quarter_row_fp8(const KParams &p, int lane, bool active, int64_t t,
-                                                int64_t slot, float (*v)[8])
+                                                int64_t slot, const uint4 *x, const uint4 *w_smem,
+                                                const float *tmax, float r, const float *rope)
 {
     const int g = lane & 7, base = lane & ~7;
-    float am[8];
-#pragma unroll
-    for (int u = 0; u < 7; ++u) {
-        float a = 0.0f;
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            a = fmaxf(a, fabsf(v[u][k]));
-        am[u] = a;
-    }
-    am[7] = 0.0f;  // the rope dims are not quantised: lane 7 leads no block
-    ScaleGuess sg = ue8m0_guess(quarter_max_scatter(am, g));
+    // tmax[7] = 0: the rope dims are not quantised, lane 7 leads no block
+    ScaleGuess sg = ue8m0_guess(__fmul_rn(quarter_max_scatter(tmax, g), r));
     sg.near = sg.near && active;
     // with no norm, v = x exactly and the guess is already exact
     if (kKvNorm && __any_sync(kFull, sg.near)) {
@@ -216,6 +208,13 @@ __device__ __forceinline__ void quarter_row_fp8(const KParams &p, int lane, bool
 #pragma unroll
     for (int u = 0; u < 7; ++u)
         s[u] = __shfl_sync(kFull, sg.s, base + u);
+    // a block below kTwoStepBelow anywhere in the warp: the two-step payload form
+    // (voted by every lane before the inactive ones leave)
+    bool slow = false;
+#pragma unroll
+    for (int u = 0; u < 7; ++u)
+        slow = slow || s[u] < kTwoStepBelow;
+    slow = __any_sync(kFull, active && slow);
     if (!active)
         return;
 
@@ -224,19 +223,27 @@ __device__ __forceinline__ void quarter_row_fp8(const KParams &p, int lane, bool
     uint8_t *cbase = p.cache + blk * int64_t(p.block_size) * DSV4_FP8_SLOT_BYTES;
     uint8_t *data = cbase + off * DSV4_FP8_DATA_BYTES;
     const Span cspan = cache_span<DSV4_STORE_FP8>(p);
+    if (slow) {
 #pragma unroll
-    for (int u = 0; u < 7; ++u) {
-        const float ku = pow2_neg(s[u]);
-        st_stream8_in(data + 64 * u + 8 * g,
-                      make_uint2(e4m3x4_rn(v[u][0] * ku, v[u][1] * ku, v[u][2] * ku, v[u][3] * ku),
-                                 e4m3x4_rn(v[u][4] * ku, v[u][5] * ku, v[u][6] * ku, v[u][7] * ku)),
-                      cspan, p.err);
+        for (int u = 0; u < 7; ++u) {
+            float xw[8];
+            quarter_vec<kKvNorm>(x, w_smem, g, u, xw);
+            st_stream8_in(data + 64 * u + 8 * g, e4m3x8_block(xw, r, s[u]), cspan, p.err);
+        }
+    } else {
+#pragma unroll
+        for (int u = 0; u < 7; ++u) {
+            float xw[8];
+            quarter_vec<kKvNorm>(x, w_smem, g, u, xw);
+            st_stream8_in(data + 64 * u + 8 * g, e4m3x8_of(xw, __fmul_rn(r, pow2_neg(s[u]))), cspan,
+                          p.err);
+        }
     }
     // rope dims stay bf16; 8-byte stores keep any block_size legal
     uint8_t *tail = data + DSV4_NOPE_DIM + 16 * g;
-    st_stream8_in(tail, make_uint2(bf16x2_rn(v[7][0], v[7][1]), bf16x2_rn(v[7][2], v[7][3])), cspan,
+    st_stream8_in(tail, make_uint2(bf16x2_rn(rope[0], rope[1]), bf16x2_rn(rope[2], rope[3])), cspan,
                   p.err);
-    st_stream8_in(tail + 8, make_uint2(bf16x2_rn(v[7][4], v[7][5]), bf16x2_rn(v[7][6], v[7][7])),
+    st_stream8_in(tail + 8, make_uint2(bf16x2_rn(rope[4], rope[5]), bf16x2_rn(rope[6], rope[7])),
                   cspan, p.err);
     if (g == 0) {
         // byte b of the scale word is block b's exponent; byte 7 stays 0
@@ -256,7 +263,7 @@ __device__ __forceinline__ void quarter_row_fp8(const KParams &p, int lane, bool
 // arithmetic.
 template <int kStore, bool kKvNorm>
 __device__ __forceinline__ void kv_quad_row(const KParams &p, int lane, int64_t t, int64_t pos,
-                                            int64_t slot, const uint4 *x, const float4 *w_smem)
+                                            int64_t slot, uint4 *x, const uint4 *w_smem)
 {
     const int g = lane & 7;
     const bool live = t < p.num_tokens;
@@ -276,27 +283,39 @@ __device__ __forceinline__ void kv_quad_row(const KParams &p, int lane, int64_t 
         cv = ldg_f4_in(cs, cs_span(p), p.err);
         sv = ldg_f4_in(cs + DSV4_ROPE_DIM / 2, cs_span(p), p.err);
     }
-    float v[8][8];
-    quarter_values<kKvNorm>(p, g, x, cv, sv, w_smem, v);
+    float tmax[8];
+    const float r = quarter_pass1<kKvNorm>(p, g, x, w_smem, tmax);
+    // the rope dims (vector 7 on every lane): x * w rotated, then scaled by r
+    float rope[8];
+    {
+        float u7[8];
+        quarter_vec<kKvNorm>(x, w_smem, g, 7, u7);
+        rope8_scaled(u7, cv, sv, r, rope);
+    }
     if constexpr (kStore == DSV4_STORE_BF16) {
         if (active) {
             uint16_t *row = reinterpret_cast<uint16_t *>(p.cache) + slot * kHead;
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-                st_stream16_in(row + 64 * u + 8 * g, bf16x8_rn(v[u]), cache_span<kStore>(p), p.err);
+            for (int u = 0; u < 7; ++u) {
+                float xw[8];
+                quarter_vec<kKvNorm>(x, w_smem, g, u, xw);
+                st_stream16_in(row + 64 * u + 8 * g, bf16x8_scaled(xw, r), cache_span<kStore>(p),
+                               p.err);
+            }
+            st_stream16_in(row + 64 * 7 + 8 * g, bf16x8_rn(rope), cache_span<kStore>(p), p.err);
         }
     } else {
-        quarter_row_fp8<kKvNorm>(p, lane, active, t, slot, v);
+        quarter_row_fp8<kKvNorm>(p, lane, active, t, slot, x, w_smem, tmax, r, rope);
     }
 }
 
-// Shared memory: per warp kKvStages mbarriers, the weight as fp32, then per
+// Shared memory: per warp kKvStages mbarriers, the weight (packed bf16), then per
 // warp kKvStages stages of one item (4 rows, 4 KB) each.
 constexpr int kKvWarps = kKvThreads / 32;
 constexpr int kKvStages = 2;
 constexpr uint32_t kItemBytes = 4 * DSV4_HEAD_DIM * 2;
 constexpr int kKvWeightOffset = 256;
-constexpr int kKvStageOffset = kKvWeightOffset + 2048;
+constexpr int kKvStageOffset = kKvWeightOffset + 1024;
 constexpr size_t kKvSmemBytes = size_t(kKvStageOffset) + size_t(kKvWarps) * kKvStages * kItemBytes;
 static_assert(kKvWarps * kKvStages * 8 <= kKvWeightOffset, "barriers overlap the weight");
 static_assert(kKvStageOffset % 128 == 0, "stages must be 16-byte aligned");
@@ -313,7 +332,7 @@ __global__ void __launch_bounds__(kKvThreads, kKvCtasPerSm) kv_rows_kernel(const
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, c = lane >> 3, g = lane & 7;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem) + warp * kKvStages;
-    float4 *w_smem = reinterpret_cast<float4 *>(smem + kKvWeightOffset);
+    uint4 *w_smem = reinterpret_cast<uint4 *>(smem + kKvWeightOffset);
     uint8_t *stages = smem + kKvStageOffset + size_t(warp) * kKvStages * kItemBytes;
     if (lane == 0) {
         for (int s = 0; s < kKvStages; ++s)

@@ -125,6 +125,10 @@ __global__ void __launch_bounds__(256, 3) qnorm_rope_kv_insert_kernel(const KPar
                 b[j] = a[j];
             }
         }
+        // every row's r at once (rows past the end or with a position outside the
+        // table are computed too and not stored)
+        float r[kRows];
+        q_rows_inv_rms<kRows>(p.eps, a, b, r);
 #pragma unroll
         for (int j = 0; j < kRows; ++j) {
             if (r0 + j >= q_rows)
@@ -134,7 +138,7 @@ __global__ void __launch_bounds__(256, 3) qnorm_rope_kv_insert_kernel(const KPar
             float4 cv, sv;
             load_cs(p, lane, pos[j], cv, sv);
             uint4 out_a, out_b;
-            q_row(p, lane, a[j], b[j], cv, sv, out_a, out_b);
+            q_row_out(lane, a[j], b[j], r[j], cv, sv, out_a, out_b);
             uint16_t *dst = p.q + (r0 + j) * kHead;
             st_stream16_in(dst + 8 * lane, out_a, q_span(p), p.err);
             st_stream16_in(dst + 256 + 8 * lane, out_b, q_span(p), p.err);

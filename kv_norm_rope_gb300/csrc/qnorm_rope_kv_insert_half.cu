@@ -31,7 +31,7 @@ constexpr int kQPairs = 2;  // q row pairs per warp item (4 rows)
 template <int kStore, bool kKvNorm>
 __global__ void __launch_bounds__(kHalfThreads, 3) qnorm_rope_kv_insert_half_kernel(const KParams p)
 {
-    __shared__ float4 w_smem[128];
+    __shared__ uint4 w_smem[64];
     if (kKvNorm) {
         for (int i = threadIdx.x; i < 64; i += kHalfThreads)
             stage_weight(p, i, w_smem);
@@ -77,6 +77,9 @@ __global__ void __launch_bounds__(kHalfThreads, 3) qnorm_rope_kv_insert_half_ker
                 x[j][v] = live[j] ? ld_stream16_in(src + 128 * v, q_span(p), p.err)
                                   : make_uint4(0u, 0u, 0u, 0u);
         }
+        // every row's r at once (rows that are not written are computed too)
+        float r[kQPairs];
+        q_half_rows_inv_rms<kQPairs>(p.eps, x, r);
 #pragma unroll
         for (int j = 0; j < kQPairs; ++j) {
             // rows past the end or with a position outside the table are not
@@ -87,7 +90,7 @@ __global__ void __launch_bounds__(kHalfThreads, 3) qnorm_rope_kv_insert_half_ker
             float4 cv, sv;
             half_load_cs(p, h, active, pos[j], cv, sv);
             uint4 out[4];
-            q_half_row(p, h, x[j], cv, sv, out);
+            q_half_out(h, x[j], r[j], cv, sv, out);
             if (active) {
                 uint16_t *dst = p.q + (r0 + 2 * j + half) * kHead + 8 * h;
 #pragma unroll

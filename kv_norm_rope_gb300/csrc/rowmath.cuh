@@ -152,31 +152,39 @@ constexpr float kTinyMeanSq = 0x1p-100f;
 // r = 1 / sqrt(sum(x^2)/512 + eps) of the row held in part by this lane.
 // sum() returns the row's sum of squares in the layout's fixed order (the same
 // bits on every lane of the row; every lane of the warp calls it together, so
-// it may shuffle); scale() multiplies this lane's elements of the row by 2^64.
-// On return the lane's elements may have been scaled by 2^64 or 2^128, and r by
-// the inverse, so that (element * r) is unchanged.  Rows of normal size take
-// one compare and one vote more than inv_rms.
+// it may shuffle); scale() multiplies this lane's elements of the row (and
+// anything derived from them linearly) by 2^64.  On return those may have been
+// scaled by 2^64 or 2^128, and r by the inverse, so that (element * r) is
+// unchanged.  Rows of normal size take one compare and one vote more than
+// inv_rms.  rescale_tiny is the rare part: given m = mean_sq of the row, it
+// rescales the rows whose m is below kTinyMeanSq and returns their new m.
+template <typename Sum, typename Scale>
+__device__ __forceinline__ float rescale_tiny(float eps, float m, Sum sum, Scale scale)
+{
+    bool tiny = m < kTinyMeanSq;
+    float e = eps;
+#pragma unroll 1
+    for (int i = 0; i < 2; ++i) {
+        if (tiny) {
+            scale();
+            e = __fmul_rn(__fmul_rn(e, 0x1p64f), 0x1p64f);
+        }
+        const float s = sum();
+        if (tiny)
+            m = mean_sq(s, e);
+        tiny = tiny && m < kTinyMeanSq;
+        if (!__any_sync(kFull, tiny))
+            break;
+    }
+    return m;
+}
+
 template <typename Sum, typename Scale>
 __device__ __forceinline__ float row_inv_rms(float eps, Sum sum, Scale scale)
 {
     float m = mean_sq(sum(), eps);
-    bool tiny = m < kTinyMeanSq;
-    if (__any_sync(kFull, tiny)) {
-        float e = eps;
-#pragma unroll 1
-        for (int i = 0; i < 2; ++i) {
-            if (tiny) {
-                scale();
-                e = __fmul_rn(__fmul_rn(e, 0x1p64f), 0x1p64f);
-            }
-            const float s = sum();
-            if (tiny)
-                m = mean_sq(s, e);
-            tiny = tiny && m < kTinyMeanSq;
-            if (!__any_sync(kFull, tiny))
-                break;
-        }
-    }
+    if (__any_sync(kFull, m < kTinyMeanSq))
+        m = rescale_tiny(eps, m, sum, scale);
     return __frsqrt_rn(m);
 }
 
@@ -426,71 +434,199 @@ __device__ __forceinline__ void flag_error(int32_t *err, int bit)
         atomicOr(err, bit);
 }
 
-// the whole-warp layout's sum of squares: 16 sequential fmas per lane, then
-// the xor butterfly
-__device__ __forceinline__ float warp_sumsq16(const float *y)
+// ---- KV row values, shared by every layout
+//
+// For a normalised KV row the kernels form, per element,
+//   xw = x * w                        exact: the product of two bf16 values fits fp32
+//                                     (for weights 0 or 2^-9 <= |w| < 2^64)
+//   v  = fp32(xw * r)                 one rounding of x * w * r
+// and for the FP8 store, per 64-dim block b with t_b = max |xw| (exact),
+//   amax_b    = fp32(t_b * r)         = max |v| over the block (rounding is monotone)
+//   payload   = E4M3(fp32(xw * k_b)), k_b = r * 2^-s_b (exact)
+// which is E4M3(v * 2^-s_b): scaling by a power of two commutes with the
+// rounding.  When s_b < -64, r * 2^-s_b could overflow, and the two steps
+// E4M3(fp32(xw * r) * 2^-s_b) are taken instead (blocks whose amax is below
+// 2^-55: all-zero blocks, or blocks far below the rest of their row).  The
+// products x * w and x * x read the bf16 inputs directly (fma.rn.f32.bf16), so
+// no element is widened first.  Every layout evaluates exactly these steps, so
+// a row's bytes do not depend on the kernel that wrote them.
+
+constexpr int kTwoStepBelow = -64;
+
+// x * y + c for bf16 half kHalf (0: low, 1: high) of two packed words: one
+// rounding (x * y is exact in fp32)
+template <int kHalf>
+__device__ __forceinline__ float fma_bf16(uint32_t x, uint32_t y, float c)
 {
-    float ss = 0.0f;
-#pragma unroll
-    for (int k = 0; k < 16; ++k)
-        ss = __fmaf_rn(y[k], y[k], ss);
-    return warp_sum(ss);
+    float d;
+    if (kHalf == 0)
+        asm("{\n\t.reg .b16 xl, xh, yl, yh;\n\tmov.b32 {xl, xh}, %1;\n\tmov.b32 {yl, yh}, %2;\n\t"
+            "fma.rn.f32.bf16 %0, xl, yl, %3;\n\t}"
+            : "=f"(d)
+            : "r"(x), "r"(y), "f"(c));
+    else
+        asm("{\n\t.reg .b16 xl, xh, yl, yh;\n\tmov.b32 {xl, xh}, %1;\n\tmov.b32 {yl, yh}, %2;\n\t"
+            "fma.rn.f32.bf16 %0, xh, yh, %3;\n\t}"
+            : "=f"(d)
+            : "r"(x), "r"(y), "f"(c));
+    return d;
 }
 
-__device__ __forceinline__ void scale_16(float *y)
+// x_0^2 + ... + x_7^2 of one 16-byte vector, accumulated in element order
+__device__ __forceinline__ float sumsq8(uint4 x)
 {
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    float acc = 0.0f;
 #pragma unroll
-    for (int k = 0; k < 16; ++k)
-        y[k] = __fmul_rn(y[k], 0x1p64f);
-}
-
-// v = x * r * w for the lane's 16 dims of the KV row, then the rotation of
-// the rope dims (lanes 24..31).  Deterministic: calling it twice on the same
-// data gives the same bits.
-template <bool kSmemW, bool kKvNorm>
-__device__ __forceinline__ void kv_values(const KParams &p, int lane, uint4 xa, uint4 xb,
-                                          float4 cv, float4 sv, const uint4 *w_smem, float *v)
-{
-    widen8(xa, v);
-    widen8(xb, v + 8);
-    if (!kKvNorm) {
-        // the row arrives normalised: v = x (exact), only the rope dims turn
-        if (lane >= 24) {
-            float u[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                u[k] = v[8 + k];
-            rope8_scaled(u, cv, sv, 1.0f, v + 8);
-        }
-        return;
+    for (int i = 0; i < 4; ++i) {
+        acc = fma_bf16<0>(w[i], w[i], acc);
+        acc = fma_bf16<1>(w[i], w[i], acc);
     }
-    const float r = row_inv_rms(p.eps, [&] { return warp_sumsq16(v); }, [&] { scale_16(v); });
-    const uint4 wa = kSmemW ? w_smem[lane]
-                            : ldg16_in(reinterpret_cast<const uint4 *>(p.w) + lane, w_span(p), p.err);
-    const uint4 wb =
-        kSmemW ? w_smem[32 + lane]
-               : ldg16_in(reinterpret_cast<const uint4 *>(p.w) + 32 + lane, w_span(p), p.err);
-    float w[16];
-    widen8(wa, w);
-    widen8(wb, w + 8);
+    return acc;
+}
+
+// The fixed order of every row's sum of squares, in every layout: whole-warp
+// lane l's partial is (its first vector's sum) + (its second vector's sum),
+// each vector summed in element order; the 32 partials are then added by the
+// xor butterfly (16, 8, 4, 2, 1).  Two chains of 8 per partial keep the
+// dependency chains short.
+__device__ __forceinline__ float lane_sumsq(uint4 first, uint4 second)
+{
+    return __fadd_rn(sumsq8(first), sumsq8(second));
+}
+
+// out[k] = x_k * w_k, exact
+__device__ __forceinline__ void prod8(uint4 x, uint4 w, float *out)
+{
+    const uint32_t a[4] = {x.x, x.y, x.z, x.w}, b[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        out[2 * i] = fma_bf16<0>(a[i], b[i], -0.0f);
+        out[2 * i + 1] = fma_bf16<1>(a[i], b[i], -0.0f);
+    }
+}
+
+// 8 bf16 times 2^64, exact (the tiny-row rescaling of row_inv_rms)
+__device__ __forceinline__ uint4 scale8_2p64(uint4 x)
+{
+    const uint32_t k = 0x5F805F80u;  // bf16x2 (2^64, 2^64)
+    uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(w[i]) : "r"(w[i]), "r"(k));
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// E4M3 of the payload of 8 values of one block: xw * k in one rounding, or for
+// two_step (s < kTwoStepBelow) fp32(xw * r) * k2 with k2 = 2^-s
+__device__ __forceinline__ uint2 e4m3x8_of(const float *xw, float k)
+{
+    return make_uint2(e4m3x4_rn(__fmul_rn(xw[0], k), __fmul_rn(xw[1], k), __fmul_rn(xw[2], k),
+                                __fmul_rn(xw[3], k)),
+                      e4m3x4_rn(__fmul_rn(xw[4], k), __fmul_rn(xw[5], k), __fmul_rn(xw[6], k),
+                                __fmul_rn(xw[7], k)));
+}
+
+__device__ __forceinline__ uint2 e4m3x8_two_step(const float *xw, float r, float k2)
+{
+    float v[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k)
-        v[k] = __fmul_rn(__fmul_rn(v[k], r), w[k]);
-    if (lane < 24) {
+        v[k] = __fmul_rn(__fmul_rn(xw[k], r), k2);
+    return make_uint2(e4m3x4_rn(v[0], v[1], v[2], v[3]), e4m3x4_rn(v[4], v[5], v[6], v[7]));
+}
+
+// the payload of a block, either form (callers take this path only when some
+// lane of the warp has a block below kTwoStepBelow; the others use e4m3x8_of
+// with r * 2^-s directly, so the common path carries no select)
+__device__ __forceinline__ uint2 e4m3x8_block(const float *xw, float r, int s)
+{
+    return s < kTwoStepBelow ? e4m3x8_two_step(xw, r, pow2_neg(s))
+                             : e4m3x8_of(xw, __fmul_rn(r, pow2_neg(s)));
+}
+
+// bf16 of fp32(xw * r) for 8 values
+__device__ __forceinline__ uint4 bf16x8_scaled(const float *xw, float r)
+{
+    float v[8];
 #pragma unroll
-        for (int k = 8; k < 16; ++k)
-            v[k] = __fmul_rn(__fmul_rn(v[k], r), w[k]);
+    for (int k = 0; k < 8; ++k)
+        v[k] = __fmul_rn(xw[k], r);
+    return bf16x8_rn(v);
+}
+
+// max |xw| of 8 values
+__device__ __forceinline__ float absmax8(const float *xw)
+{
+    float t = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        t = fmaxf(t, fabsf(xw[k]));
+    return t;
+}
+
+// The lane's products for the KV row of token tok in the whole-warp layout
+// (lane l: dims [8l, 8l+8) in xw[0..7], [256+8l, 256+8l+8) in xw[8..15]), their
+// lane-local maxima t[0] = max |xw[0..7]|, t[1] = max |xw[8..15]| (0 on rope
+// lanes), and the row's r.  Rope lanes (24..31) get their dims 448.. final in
+// xw[8..15]: x * w rotated (compensated), then scaled by r.  The partial sums,
+// products and maxima do not depend on r and come first, so they overlap the
+// reduction and x dies early; a tiny row (rare) reloads x from p.kv and scales
+// the products and maxima with it.  With no norm, xw = x and r = 1.
+template <bool kSmemW, bool kKvNorm>
+__device__ __forceinline__ float kv_products(const KParams &p, int lane, int64_t tok, uint4 xa,
+                                             uint4 xb, float4 cv, float4 sv, const uint4 *w_smem,
+                                             float *xw, float *t)
+{
+    const bool rope_lane = lane >= 24;
+    float r = 1.0f;
+    float part = 0.0f;
+    if (!kKvNorm) {
+        // the row arrives normalised: v = x (exact), only the rope dims turn
+        widen8(xa, xw);
+        widen8(xb, xw + 8);
     } else {
-        // rope dims: x*w is exact in fp32 (two 8-bit significands), rotate, then scale
+        const uint4 wa = kSmemW
+                             ? w_smem[lane]
+                             : ldg16_in(reinterpret_cast<const uint4 *>(p.w) + lane, w_span(p), p.err);
+        const uint4 wb =
+            kSmemW ? w_smem[32 + lane]
+                   : ldg16_in(reinterpret_cast<const uint4 *>(p.w) + 32 + lane, w_span(p), p.err);
+        part = lane_sumsq(xa, xb);
+        prod8(xa, wa, xw);
+        prod8(xb, wb, xw + 8);
+    }
+    t[0] = absmax8(xw);
+    t[1] = rope_lane ? 0.0f : absmax8(xw + 8);
+    if (kKvNorm) {
+        float m = mean_sq(warp_sum(part), p.eps);
+        if (__any_sync(kFull, m < kTinyMeanSq)) {
+            const uint4 *row = reinterpret_cast<const uint4 *>(p.kv + tok * kHead);
+            uint4 ya = ldg16_in(row + lane, kv_span(p), p.err);
+            uint4 yb = ldg16_in(row + 32 + lane, kv_span(p), p.err);
+            m = rescale_tiny(p.eps, m, [&] { return warp_sum(lane_sumsq(ya, yb)); }, [&] {
+                ya = scale8_2p64(ya);
+                yb = scale8_2p64(yb);
+#pragma unroll
+                for (int k = 0; k < 16; ++k)
+                    xw[k] = __fmul_rn(xw[k], 0x1p64f);
+                t[0] = __fmul_rn(t[0], 0x1p64f);
+                t[1] = __fmul_rn(t[1], 0x1p64f);
+            });
+        }
+        r = __frsqrt_rn(m);
+    }
+    if (rope_lane) {
         float u[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-            u[k] = __fmul_rn(v[8 + k], w[8 + k]);
-        rope8_scaled(u, cv, sv, r, v + 8);
+            u[k] = xw[8 + k];
+        rope8_scaled(u, cv, sv, r, xw + 8);
     }
+    return r;
 }
 
-// The KV row of token t: v = x*r*w (or v = x when the row arrives normalised),
+// The KV row of token t: v = x*w*r (or v = x when the row arrives normalised),
 // rotate, store into the paged cache.  xa, xb: the row's two 16-byte vectors of
 // this lane (from global memory or a shared-memory stage); pos, slot: the
 // token's metadata.  The rare exact-scale path reloads the row from p.kv.
@@ -518,28 +654,20 @@ __device__ __forceinline__ void kv_row(const KParams &p, int lane, int64_t t, in
         cv = ldg_f4_in(cs, cs_span(p), p.err);
         sv = ldg_f4_in(cs + DSV4_ROPE_DIM / 2, cs_span(p), p.err);
     }
-    float v[16];
-    kv_values<kSmemW, kKvNorm>(p, lane, xa, xb, cv, sv, w_smem, v);
+    float xw[16], tmax[2];
+    float r = kv_products<kSmemW, kKvNorm>(p, lane, t, xa, xb, cv, sv, w_smem, xw, tmax);
 
     if (kStore == DSV4_STORE_BF16) {
         uint16_t *row = reinterpret_cast<uint16_t *>(p.cache) + slot * kHead;
-        st_stream16_in(row + 8 * lane, bf16x8_rn(v), cache_span<kStore>(p), p.err);
-        st_stream16_in(row + 256 + 8 * lane, bf16x8_rn(v + 8), cache_span<kStore>(p), p.err);
+        st_stream16_in(row + 8 * lane, bf16x8_scaled(xw, r), cache_span<kStore>(p), p.err);
+        st_stream16_in(row + 256 + 8 * lane, rope_lane ? bf16x8_rn(xw + 8) : bf16x8_scaled(xw + 8, r),
+                       cache_span<kStore>(p), p.err);
         return;
     }
 
     // block amax: half 0 -> blocks 0..3 (lane / 8), half 1 -> blocks 4..6 (lanes 0..23)
-    float am0 = 0.0f, am1 = 0.0f;
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-        am0 = fmaxf(am0, fabsf(v[k]));
-    if (!rope_lane) {
-#pragma unroll
-        for (int k = 8; k < 16; ++k)
-            am1 = fmaxf(am1, fabsf(v[k]));
-    }
-    ScaleGuess g0 = ue8m0_guess(group8_max(am0));
-    ScaleGuess g1 = ue8m0_guess(group8_max(am1));  // lanes 24..31: amax 0, never near
+    ScaleGuess g0 = ue8m0_guess(__fmul_rn(group8_max(tmax[0]), r));
+    ScaleGuess g1 = ue8m0_guess(__fmul_rn(group8_max(tmax[1]), r));  // lanes 24..31: never near
     // with no norm, v = x exactly and the guess is already exact
     if (kKvNorm && __any_sync(kFull, g0.near || g1.near)) {
         const int bumps = exact_scale_bumps(p, lane, t, g0.e, g0.near, g1.e, g1.near);
@@ -547,11 +675,11 @@ __device__ __forceinline__ void kv_row(const KParams &p, int lane, int64_t t, in
             g0.s = clamp_s(g0.e - 8 + (bumps & 1));
         if (g1.near)
             g1.s = clamp_s(g1.e - 8 + ((bumps >> 1) & 1));
-        // recompute v (same bits) instead of keeping it live across the call
-        kv_values<kSmemW, kKvNorm>(
-            p, lane, ldg16_in(reinterpret_cast<const uint4 *>(src) + lane, kv_span(p), p.err),
+        // recompute the products (same bits) instead of keeping them live across the call
+        r = kv_products<kSmemW, kKvNorm>(
+            p, lane, t, ldg16_in(reinterpret_cast<const uint4 *>(src) + lane, kv_span(p), p.err),
             ldg16_in(reinterpret_cast<const uint4 *>(src) + 32 + lane, kv_span(p), p.err), cv, sv,
-            w_smem, v);
+            w_smem, xw, tmax);
     }
 
     // 0 <= slot < num_slots <= 2^32 here, so the quotient is a 32-bit one
@@ -561,23 +689,23 @@ __device__ __forceinline__ void kv_row(const KParams &p, int lane, int64_t t, in
     uint8_t *data = base + off * DSV4_FP8_DATA_BYTES;
 
     const Span cspan = cache_span<kStore>(p);
-    const float k0 = pow2_neg(g0.s);
-    st_stream8_in(data + 8 * lane,
-                  make_uint2(e4m3x4_rn(v[0] * k0, v[1] * k0, v[2] * k0, v[3] * k0),
-                             e4m3x4_rn(v[4] * k0, v[5] * k0, v[6] * k0, v[7] * k0)),
-                  cspan, p.err);
-    if (!rope_lane) {
-        const float k1 = pow2_neg(g1.s);
-        st_stream8_in(data + 256 + 8 * lane,
-                      make_uint2(e4m3x4_rn(v[8] * k1, v[9] * k1, v[10] * k1, v[11] * k1),
-                                 e4m3x4_rn(v[12] * k1, v[13] * k1, v[14] * k1, v[15] * k1)),
-                      cspan, p.err);
+    if (__any_sync(kFull, g0.s < kTwoStepBelow || (!rope_lane && g1.s < kTwoStepBelow))) {
+        st_stream8_in(data + 8 * lane, e4m3x8_block(xw, r, g0.s), cspan, p.err);
+        if (!rope_lane)
+            st_stream8_in(data + 256 + 8 * lane, e4m3x8_block(xw + 8, r, g1.s), cspan, p.err);
     } else {
+        st_stream8_in(data + 8 * lane, e4m3x8_of(xw, __fmul_rn(r, pow2_neg(g0.s))), cspan, p.err);
+        if (!rope_lane)
+            st_stream8_in(data + 256 + 8 * lane, e4m3x8_of(xw + 8, __fmul_rn(r, pow2_neg(g1.s))),
+                          cspan, p.err);
+    }
+    if (rope_lane) {
         // rope dims stay bf16; 8-byte stores keep any block_size legal
         uint8_t *tail = data + DSV4_NOPE_DIM + 16 * (lane - 24);
-        st_stream8_in(tail, make_uint2(bf16x2_rn(v[8], v[9]), bf16x2_rn(v[10], v[11])), cspan, p.err);
-        st_stream8_in(tail + 8, make_uint2(bf16x2_rn(v[12], v[13]), bf16x2_rn(v[14], v[15])), cspan,
+        st_stream8_in(tail, make_uint2(bf16x2_rn(xw[8], xw[9]), bf16x2_rn(xw[10], xw[11])), cspan,
                       p.err);
+        st_stream8_in(tail + 8, make_uint2(bf16x2_rn(xw[12], xw[13]), bf16x2_rn(xw[14], xw[15])),
+                      cspan, p.err);
     }
 
     // scale word: byte b is the exponent of block b, held by lane 8*(b%4) of
@@ -593,15 +721,46 @@ __device__ __forceinline__ void kv_row(const KParams &p, int lane, int64_t t, in
 }
 
 
-// One q head row: y = x * r with the rope dims rotated first (compensated) and
-// then scaled; returns the lane's two output vectors (bf16, round to nearest).
-__device__ __forceinline__ void q_row(const KParams &p, int lane, uint4 a, uint4 b, float4 cv,
-                                      float4 sv, uint4 &out_a, uint4 &out_b)
+// r of kRows q head rows held in the whole-warp layout (a[j], b[j]: lane l's
+// two vectors of row j), with one tiny-row vote for the whole group, so the
+// rows' arithmetic stays straight-line and interleaved; a row that needs the
+// rare rescaling gets it as in row_inv_rms (a[j], b[j] scaled with it).
+template <int kRows>
+__device__ __forceinline__ void q_rows_inv_rms(float eps, uint4 *a, uint4 *b, float *r)
+{
+    float m[kRows];
+    bool tiny = false;
+#pragma unroll
+    for (int j = 0; j < kRows; ++j) {
+        m[j] = mean_sq(warp_sum(lane_sumsq(a[j], b[j])), eps);
+        tiny = tiny || m[j] < kTinyMeanSq;
+    }
+    if (__any_sync(kFull, tiny)) {
+#pragma unroll
+        for (int j = 0; j < kRows; ++j) {
+            if (__any_sync(kFull, m[j] < kTinyMeanSq))
+                m[j] = rescale_tiny(
+                    eps, m[j], [&] { return warp_sum(lane_sumsq(a[j], b[j])); },
+                    [&] {
+                        a[j] = scale8_2p64(a[j]);
+                        b[j] = scale8_2p64(b[j]);
+                    });
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < kRows; ++j)
+        r[j] = __frsqrt_rn(m[j]);
+}
+
+// One q head row with its r: y = x * r with the rope dims rotated first
+// (compensated) and then scaled; returns the lane's two output vectors (bf16,
+// round to nearest).
+__device__ __forceinline__ void q_row_out(int lane, uint4 a, uint4 b, float r, float4 cv,
+                                          float4 sv, uint4 &out_a, uint4 &out_b)
 {
     float y[16];
     widen8(a, y);
     widen8(b, y + 8);
-    const float r = row_inv_rms(p.eps, [&] { return warp_sumsq16(y); }, [&] { scale_16(y); });
 #pragma unroll
     for (int k = 0; k < 8; ++k)
         y[k] = __fmul_rn(y[k], r);

@@ -46,7 +46,11 @@ def _same_step(a: harness.GpuResult, b: harness.GpuResult):
 
 
 def test_library_kinds():
-    assert k.debug_bounds_flags() == -1  # the release build records nothing
+    """The release build records nothing (-1); the checked one starts clean (0).  Under
+    DSV4KV_CHECKED=1 the default library is the checked one."""
+    import os
+    default = 0 if os.environ.get("DSV4KV_CHECKED") == "1" else -1
+    assert k.debug_bounds_flags() == default
     with k.checked_build():
         assert k.debug_bounds_flags() == 0
 
