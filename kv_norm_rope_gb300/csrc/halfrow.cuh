@@ -68,12 +68,11 @@ __device__ __forceinline__ void half_load_cs(const KParams &p, int h, bool activ
 // (h >= 8) get their dims 448.. final in xw[3] (x * w rotated, then scaled by
 // r).  r comes first and the products after it, so x and the products are not
 // held together (a tiny row rescales x in place first).  With no norm, xw = x
-// and r = 1.  w_smem: the weight as packed bf16 in dim order.  The steps of
-// kv_products, so the same bits.
+// and r = 1.  w: the weight (global, packed bf16 in dim order; lane h reads
+// vector j at 16j + h).  The steps of kv_products, so the same bits.
 template <bool kKvNorm>
 __device__ __forceinline__ float half_products(const KParams &p, int h, uint4 *x, float4 cv,
-                                               float4 sv, const uint4 *w_smem, float (*xw)[8],
-                                               float *t)
+                                               float4 sv, const uint4 *w, float (*xw)[8], float *t)
 {
     const bool rope_lane = h >= 8;
     float r = 1.0f;
@@ -82,7 +81,7 @@ __device__ __forceinline__ float half_products(const KParams &p, int h, uint4 *x
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         if (kKvNorm)
-            prod8(x[j], w_smem[16 * j + h], xw[j]);
+            prod8(x[j], ldg16_in(w + 16 * j + h, w_span(p), p.err), xw[j]);
         else
             widen8(x[j], xw[j]);
     }
@@ -225,12 +224,12 @@ __device__ __forceinline__ void half_row_fp8(const KParams &p, int h, bool activ
 // position and slot); inactive halves still take part in every shuffle.
 template <int kStore, bool kKvNorm>
 __device__ __forceinline__ void half_row(const KParams &p, int h, bool active, int64_t t,
-                                         int64_t pos, int64_t slot, uint4 *x, const uint4 *w_smem)
+                                         int64_t pos, int64_t slot, uint4 *x, const uint4 *w)
 {
     float4 cv, sv;
     half_load_cs(p, h, active, pos, cv, sv);
     float xw[4][8], tmax[4];
-    const float r = half_products<kKvNorm>(p, h, x, cv, sv, w_smem, xw, tmax);
+    const float r = half_products<kKvNorm>(p, h, x, cv, sv, w, xw, tmax);
 
     if constexpr (kStore == DSV4_STORE_BF16) {
         if (active) {
@@ -246,21 +245,12 @@ __device__ __forceinline__ void half_row(const KParams &p, int h, bool active, i
     }
 }
 
-// The weight as packed bf16 in dim order (thread i < 64 copies dims [8i, 8i + 8)):
-// lane h of a half reads vector j at 16j + h, 16 consecutive 16-byte words
-__device__ __forceinline__ void stage_weight(const KParams &p, int i, uint4 *w_smem)
-{
-    w_smem[i] = ldg16_in(reinterpret_cast<const uint4 *>(p.w) + i, w_span(p), p.err);
-}
-
-
 // One KV row per half-warp: this half takes token t (idle when t >= T).  It
 // loads the token's metadata and row, flags an out-of-range position or slot,
 // and writes the cache row when both are in range.  Both halves reach every
 // shuffle; a pair with no row to write skips the arithmetic (warp-uniform).
 template <int kStore, bool kKvNorm>
-__device__ __forceinline__ void kv_pair_item(const KParams &p, int h, int64_t t,
-                                             const uint4 *w_smem)
+__device__ __forceinline__ void kv_pair_item(const KParams &p, int h, int64_t t, const uint4 *w)
 {
     const bool live = t < p.num_tokens;
     const int64_t pos = live ? ldg_i64_in(p.pos + t, pos_span(p), p.err) : 0;
@@ -279,7 +269,7 @@ __device__ __forceinline__ void kv_pair_item(const KParams &p, int h, int64_t t,
     }
     const bool active = live && pos_ok && slot >= 0 && slot < p.num_slots;
     if (__any_sync(kFull, active))
-        half_row<kStore, kKvNorm>(p, h, active, t, pos, slot, x, w_smem);
+        half_row<kStore, kKvNorm>(p, h, active, t, pos, slot, x, w);
 }
 
 // r of the kPairs q rows of this half (x[j]: the lane's vectors of row j), one

@@ -31,12 +31,9 @@ constexpr int kQPairs = 2;  // q row pairs per warp item (4 rows)
 template <int kStore, bool kKvNorm>
 __global__ void __launch_bounds__(kHalfThreads, 3) qnorm_rope_kv_insert_half_kernel(const KParams p)
 {
-    __shared__ uint4 w_smem[64];
-    if (kKvNorm) {
-        for (int i = threadIdx.x; i < 64; i += kHalfThreads)
-            stage_weight(p, i, w_smem);
-        __syncthreads();
-    }
+    // the weight (1 KB, packed bf16) is read by KV rows through the read-only
+    // cache: no CTA-wide staging barrier in front of the first loads
+    const uint4 *w = reinterpret_cast<const uint4 *>(p.w);
     const int lane = threadIdx.x & 31, h = lane & 15, half = lane >> 4;
     const int64_t H = p.num_heads;
     const int64_t T = p.num_tokens;
@@ -48,7 +45,7 @@ __global__ void __launch_bounds__(kHalfThreads, 3) qnorm_rope_kv_insert_half_ker
     for (int64_t it = int64_t(blockIdx.x) * (kHalfThreads / 32) + (threadIdx.x >> 5); it < items;
          it += stride) {
         if (it < kv_items) {
-            kv_pair_item<kStore, kKvNorm>(p, h, 2 * it + half, w_smem);
+            kv_pair_item<kStore, kKvNorm>(p, h, 2 * it + half, w);
             continue;
         }
         const int64_t r0 = (it - kv_items) * 2 * kQPairs;

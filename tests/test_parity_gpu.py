@@ -341,3 +341,30 @@ def test_positions_at_both_ends_of_the_table(variant):
     assert gpu.err == ref_err == k.DEVERR_POS_RANGE
     rep = harness.compare_results(inp, gpu, ref_q, ref_cache)
     assert rep.ok, str(rep)
+
+
+@pytest.mark.parametrize("store", ["fp8", "bf16"])
+def test_host_resident_buffers(store):
+    """Pinned host memory is addressable by the kernels at the same address (NVLink-C2C
+    on GB300): the step run through the C ABI on host-resident q, kv, positions, slots and
+    cache writes the bytes the device-resident run writes."""
+    wl = configs.generic(3000, 16, store=store, seed=160)
+    inp = harness.make_inputs(wl)
+    ref = harness.run_gpu(inp)
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    q, kv = pin(inp.q.view(np.int16)), pin(inp.kv.view(np.int16))
+    pos, sl, cache = pin(inp.positions), pin(inp.slots), pin(inp.poison)
+    dev = torch.device("cuda:0")
+    w = torch.from_numpy(inp.w.view(np.int16)).to(dev)
+    cs = torch.from_numpy(inp.cos_sin).to(dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    fn = (k.lib().dsv4_qnorm_rope_kv_quant_insert if store == "fp8"
+          else k.lib().dsv4_qnorm_rope_kv_bf16_insert)
+    st = fn(q.data_ptr(), kv.data_ptr(), w.data_ptr(), pos.data_ptr(), cs.data_ptr(),
+            wl.max_position, sl.data_ptr(), cache.data_ptr(), wl.num_blocks, wl.block_size, wl.T,
+            wl.H, wl.eps, err.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert st == k.OK
+    torch.cuda.synchronize()
+    assert int(err.item()) == ref.err
+    assert np.array_equal(q.numpy().view(np.uint16), ref.q)
+    assert np.array_equal(cache.numpy(), ref.cache)
