@@ -53,6 +53,17 @@ __device__ __forceinline__ Span scales_span(const MParams &p)
     return Span{p.scales, uint64_t((p.m + 127) / 128) * 128u * uint64_t(p.padded_cols)};
 }
 
+// 8 bf16 times 2^64, exact (the rescaling of rows with a tiny mean square)
+__device__ __forceinline__ uint4 bf16x8_times_2p64(uint4 x)
+{
+    const uint32_t k = 0x5F805F80u;  // bf16x2 (2^64, 2^64)
+    uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(w[i]) : "r"(w[i]), "r"(k));
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 __device__ __forceinline__ float bf16_round(float v)
 {
     return __uint_as_float(bf16x2_rn(v, 0.0f) << 16);
@@ -141,7 +152,39 @@ __global__ void __launch_bounds__(kThreads) gemma_rmsnorm_mxfp8_kernel(const MPa
 #pragma unroll
     for (int w = 1; w < kThreads / 32; ++w)
         total = __fadd_rn(total, warp_sums[w]);
-    const float r = __frcp_rn(__fsqrt_rn(__fadd_rn(__fdiv_rn(total, float(p.n)), p.eps)));
+    float m = __fadd_rn(__fdiv_rn(total, float(p.n)), p.eps);
+    // A mean square below 2^-100 (only with a tiny eps) may rest on subnormal fp32
+    // squares: the row's prenorm is then scaled by 2^64 (exact, twice at most) and
+    // summed again, which leaves prenorm * r unchanged and r accurate.  Every
+    // thread holds the same total, so the branch and its barriers are block-uniform.
+    float e = p.eps;
+#pragma unroll 1
+    for (int i = 0; i < 2 && m < 0x1p-100f; ++i) {
+        float s2 = 0.0f;
+#pragma unroll
+        for (int k = 0; k < kTrips; ++k) {
+            pre[k] = bf16x8_times_2p64(pre[k]);
+            float w[8];
+            widen8(pre[k], w);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                s2 = __fmaf_rn(w[j], w[j], s2);
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1)
+            s2 = __fadd_rn(s2, __shfl_xor_sync(kFull, s2, o));
+        __syncthreads();  // every thread has read the previous sums
+        if (lane == 0)
+            warp_sums[warp] = s2;
+        __syncthreads();
+        total = warp_sums[0];
+#pragma unroll
+        for (int w = 1; w < kThreads / 32; ++w)
+            total = __fadd_rn(total, warp_sums[w]);
+        e = __fmul_rn(__fmul_rn(e, 0x1p64f), 0x1p64f);
+        m = __fadd_rn(__fdiv_rn(total, float(p.n)), e);
+    }
+    const float r = __frcp_rn(__fsqrt_rn(m));
     const float inv448 = 1.0f / 448.0f;
 
 #pragma unroll

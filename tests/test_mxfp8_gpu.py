@@ -84,3 +84,22 @@ def test_empty_batch_is_a_no_op():
     g = torch.zeros(256, dtype=torch.int16, device=DEV)
     k.add_gemma_rmsnorm_mxfp8(z, z, g, 1e-6, z, torch.zeros(0, dtype=torch.uint8, device=DEV),
                               torch.zeros(0, dtype=torch.uint8, device=DEV))
+
+
+def test_tiny_rows_with_eps_zero():
+    """With eps = 0, rows whose prenorm lies near 2^-70 .. 2^-128 (squares subnormal in
+    fp32) normalise like their unscaled selves: the kernel rescales them by 2^64 before
+    taking r.  Residual, scales and codes against the oracle."""
+    m, n = 8, 1024
+    x, r, g = _inputs(m, n, seed=41)
+    scales = np.array([1.0, 2.0**-50, 2.0**-64, 2.0**-70, 2.0**-100, 2.0**-115, 2.0**-124,
+                       2.0**-128], np.float32)
+
+    def scaled(bits):
+        f = synth.bf16_bits_to_f32(bits).reshape(m, n) * scales[:, None]
+        return torch.from_numpy(np.ascontiguousarray(f)).to(torch.bfloat16).view(torch.int16) \
+            .numpy().view(np.uint16)
+
+    xs, rs = scaled(x), scaled(r)
+    assert np.all((xs & 0x7FFF).max(axis=1) > 0)
+    _check(xs, rs, g, eps=0.0)
