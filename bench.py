@@ -88,7 +88,7 @@ def barrier(world: int):
 
 KERNEL_SOURCES = tuple("kv_norm_rope_gb300/csrc/" + f for f in (
     "qnorm_rope_kv_insert.cu", "rowmath.cuh", "convert.cuh", "fastdiv.h", "launch.h",
-    "launch_status.h"))
+    "launch_status.h", "bounds.cuh", "bounds_range.h"))
 
 
 def kernel_fingerprint() -> str:

@@ -100,3 +100,30 @@ def test_pages_by_node_finds_the_mapping_of_an_address(tmp_path, monkeypatch):
     assert bench.pages_by_node(0x7f0000000040) == {0: 4, 1: 6}
     assert bench.pages_by_node(0x7f0000100000) == {1: 2}
     assert bench.pages_by_node(0x100) == {}
+
+
+def test_counter_captures_run_small_cases():
+    """A committed ncu command that collects more than the launch times (sections, sets
+    or other metrics) must run a case that holds at most a few GB on the device: for
+    the fused step, at most 3 GB of q (stress and bf16_store only with --tokens)."""
+    import re
+    import shlex
+    from synth import configs
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    for name in os.listdir(os.path.join(root, "profiles")):
+        text = open(os.path.join(root, "profiles", name)).read().replace("\\\n", " ")
+        for line in text.splitlines():
+            if "ncu " not in line or "python bench.py" not in line:
+                continue
+            ncu_part, bench_part = line.split("python bench.py", 1)
+            metrics = re.findall(r"--metrics\s+(\S+)", ncu_part)
+            times_only = (not re.search(r"--set|--section", ncu_part)
+                          and all(m == "gpu__time_duration.sum" for m in metrics))
+            if times_only:
+                continue
+            args = shlex.split(bench_part)
+            get = lambda flag, default: args[args.index(flag) + 1] if flag in args else default
+            op, wl = get("--op", "fused"), configs.WORKLOADS[get("--workload", "stress")]
+            tokens = int(get("--tokens", wl.T))
+            if op in ("fused", "prenorm"):
+                assert tokens * wl.H * 1024 <= 3e9, (name, line.strip())
