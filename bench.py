@@ -392,26 +392,25 @@ class DeviceBatch:
                     self.err.data_ptr(), stream_handle)
 
 
-def graph_device_us(batch: DeviceBatch, lib, dev, flush, n: int = 50, reps: int = 7) -> float:
-    """Device time of one launch without the host's launch latency: a CUDA graph of
-    n (L2 flush, launch) pairs replayed and timed with events, minus a graph of the
-    n flushes alone, divided by n (median of `reps` replays)."""
+def graph_flushed_us(op, dev, flush, n: int = 50, reps: int = 7) -> float:
+    """Device time of op(stream) without the host's launch latency: a CUDA graph of
+    n (L2 flush, op) pairs replayed and timed with events, minus a graph of the n
+    flushes alone, divided by n (median of `reps` replays)."""
     import torch
 
-    def timed(with_launch: bool) -> float:
+    def timed(with_op: bool) -> float:
         s = torch.cuda.Stream(dev)
         g = torch.cuda.CUDAGraph()
-        fn, a = batch.call(lib, s.cuda_stream)
         torch.cuda.synchronize(dev)
         with torch.cuda.stream(s):
-            if with_launch:
-                fn(*a)  # warm outside the capture
+            if with_op:
+                op(s)  # warm outside the capture
             torch.cuda.synchronize(dev)
             with torch.cuda.graph(g, stream=s):
                 for i in range(n):
                     flush.fill_(i & 0xFF)
-                    if with_launch:
-                        fn(*a)
+                    if with_op:
+                        op(s)
         torch.cuda.synchronize(dev)
         ts = []
         for _ in range(reps):
@@ -424,6 +423,31 @@ def graph_device_us(batch: DeviceBatch, lib, dev, flush, n: int = 50, reps: int 
         return statistics.median(ts)
 
     return timed(True) - timed(False)
+
+
+def graph_device_us(batch: DeviceBatch, lib, dev, flush, n: int = 50, reps: int = 7) -> float:
+    """Device time of one launch of the batch's step (graph_flushed_us)."""
+    def launch(s):
+        fn, a = batch.call(lib, s.cuda_stream)
+        fn(*a)
+    return graph_flushed_us(launch, dev, flush, n, reps)
+
+
+def graph_copy_us(nbytes: int, dev, flush, n: int = 50, reps: int = 7) -> dict:
+    """The same measurement for moving nbytes / 2 bytes from one device buffer to
+    another (nbytes read and written in total), two ways: a device-to-device memcpy,
+    and an elementwise kernel (bitwise not of int32, one read and one write of each
+    word).  What moving the step's bytes costs at this size, with the same launch,
+    flush and L2 state around it."""
+    import torch
+    words = max(4, (nbytes // 2) // 16 * 4)
+    src = torch.ones(words, dtype=torch.int32, device=dev)
+    dst = torch.empty(words, dtype=torch.int32, device=dev)
+    out = {"memcpy_us": graph_flushed_us(lambda s: dst.copy_(src), dev, flush, n, reps),
+           "elementwise_us": graph_flushed_us(lambda s: torch.bitwise_not(src, out=dst), dev,
+                                              flush, n, reps)}
+    del src, dst
+    return out
 
 
 def graph_warm_us(batch: DeviceBatch, lib, dev, n: int = 50, reps: int = 7) -> float:
@@ -952,6 +976,7 @@ def run_ours(args):
                "placement": placement}
     graph_us = graph_device_us(batch, lib, dev, flush) if flush is not None else None
     warm_us = graph_warm_us(batch, lib, dev) if flush is not None else None
+    copy_us = graph_copy_us(batch.bytes, dev, flush) if flush is not None else None
     kac_after = known_answer_check() if rank == 0 else "skipped"
     if rank != 0:
         return 0
@@ -1000,7 +1025,13 @@ def run_ours(args):
                    "event-timed launch after a flush includes",
             "warm_us_per_launch": round(warm_us, 3),
             "warm_how": "CUDA graph of 50 launches back to back, no flush: inputs that fit stay "
-                        "in L2 and no flush's dirty lines are written back during the launch"},
+                        "in L2 and no flush's dirty lines are written back during the launch",
+            "same_size_copy_us": {k_: round(v_, 3) for k_, v_ in copy_us.items()},
+            "frac_of_same_size_copy": round(min(copy_us.values()) / graph_us, 4),
+            "copy_how": "half the step's bytes moved between two device buffers (the same bytes "
+                        "read plus written) by a memcpy and by an elementwise kernel, timed the "
+                        "same way: what moving them costs at this size; the fraction is against "
+                        "the faster"},
         "gpu_launches": args.steps,
         "ms_per_step_note": "mean launch time (L2 flushed between launches)" if flush is not None
         else "timed region / steps",

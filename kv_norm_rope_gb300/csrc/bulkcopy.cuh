@@ -1,6 +1,6 @@
-// mbarriers and bulk copies (cp.async.bulk) between global and shared memory,
-// shared by the kernels that stage rows through shared memory
-// (qnorm_rope_kv_insert_bulk.cu, kv_rows.cu).
+// mbarriers and bulk copies (cp.async.bulk) from global to shared memory, for
+// the kernel that stages rows through shared memory (kv_rows.cu) and the check
+// of its bounded wait (wait_check.cu).
 //
 // Every wait is bounded: it polls the barrier with try_wait (which blocks
 // for a short, system-defined time per try) and gives up after kWaitCycles SM

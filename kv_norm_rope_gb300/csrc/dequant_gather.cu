@@ -35,7 +35,9 @@ struct GParams {
     const uint8_t *cache;
     int64_t num_slots;
     int32_t block_size;
-    uint64_t slot_div;  // fastdiv_magic(block_size)
+    uint64_t slot_div;     // fastdiv_magic(block_size)
+    uint64_t block_bytes;  // block_size * DSV4_FP8_SLOT_BYTES
+    uint64_t scale_off;    // block_size * DSV4_FP8_DATA_BYTES: the scale words of a block
     const int64_t *slots;
     int64_t rows;
     uint16_t *out;
@@ -52,6 +54,16 @@ __device__ __forceinline__ float scaled(float p, uint32_t e)
     return __fmul_rn(__fmul_rn(p, 0x1p64f), 0x1p64f);  // 2^128: beyond bf16, becomes inf
 }
 
+// Two bytes of w (selector sel) into the low bytes of two 16-bit halves, each
+// half's high byte filled with its byte's sign bit (prmt's sign-replicating
+// selector nibbles, bit 3 set).
+__device__ __forceinline__ uint32_t sext_pair(uint32_t w, uint32_t sel)
+{
+    uint32_t h;
+    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(h) : "r"(w), "r"(sel));
+    return h;
+}
+
 // 8 payload bytes with scale byte e -> 8 bf16 by integer arithmetic, when every
 // code is a normal E4M3 number (exponent field 1..15, not NaN) and 7 <= e <= 246:
 // (1 + m/8) * 2^(E - 7) * 2^(e - 127) is then exactly the bf16 with exponent field
@@ -59,23 +71,25 @@ __device__ __forceinline__ float scaled(float p, uint32_t e)
 // out unset, when any code or the scale is outside that range.
 __device__ __forceinline__ bool dequant8_normal(uint2 codes, uint32_t e, uint4 &out)
 {
-    // a byte with exponent field 0 (zero, subnormal) or equal to 0x7f / 0xff (NaN):
-    // a zero byte of (code & 0x78) or of (code & 0x7f) ^ 0x7f (all bytes < 0x80)
-    const uint32_t xe = codes.x & 0x78787878u, ye = codes.y & 0x78787878u;
-    const uint32_t xn = (codes.x & 0x7f7f7f7fu) ^ 0x7f7f7f7fu;
-    const uint32_t yn = (codes.y & 0x7f7f7f7fu) ^ 0x7f7f7f7fu;
-    const uint32_t special = ((xe - 0x01010101u) & ~xe) | ((ye - 0x01010101u) & ~ye) |
-                             ((xn - 0x01010101u) & ~xn) | ((yn - 0x01010101u) & ~yn);
-    if ((special & 0x80808080u) != 0u || e - 7u > 239u)
+    // per byte, bit 7 of (c & 0x78) + 0x78 is set when the exponent field is not 0,
+    // and bit 7 of (c & 0x7f) + 1 when the low 7 bits are all ones (NaN); neither
+    // sum carries out of its byte
+    const uint32_t xe = (codes.x & 0x78787878u) + 0x78787878u;
+    const uint32_t ye = (codes.y & 0x78787878u) + 0x78787878u;
+    const uint32_t xn = (codes.x & 0x7f7f7f7fu) + 0x01010101u;
+    const uint32_t yn = (codes.y & 0x7f7f7f7fu) + 0x01010101u;
+    if ((xe & ~xn & ye & ~yn & 0x80808080u) != 0x80808080u || e - 7u > 239u)
         return false;
-    const uint32_t off = ((e - 7u) << 7) * 0x00010001u;  // added to both exponent fields
-    // two codes, one per 16-bit half (the first in the low half), to two bf16
+    // a half 0x00cc or 0xffcc shifted left by 4 and masked with 0x87f0 is the sign at
+    // bit 15 and the code's exponent and mantissa at bits 7..10 and 4..6 (the bits
+    // shifted across into the upper half are masked off there); adding e - 7 to the
+    // exponent field cannot carry into the sign (E + e - 7 <= 254)
+    const uint32_t off = ((e - 7u) << 7) * 0x00010001u;
     const auto pair = [off](uint32_t w, uint32_t sel) {
-        const uint32_t h = __byte_perm(w, 0u, sel);
-        return (((h & 0x007f007fu) << 4) + off) | ((h & 0x00800080u) << 8);
+        return ((sext_pair(w, sel) << 4) & 0x87f087f0u) + off;
     };
-    out = make_uint4(pair(codes.x, 0x4140u), pair(codes.x, 0x4342u), pair(codes.y, 0x4140u),
-                     pair(codes.y, 0x4342u));
+    out = make_uint4(pair(codes.x, 0x9180u), pair(codes.x, 0xb3a2u), pair(codes.y, 0x9180u),
+                     pair(codes.y, 0xb3a2u));
     return true;
 }
 
@@ -136,10 +150,12 @@ __device__ __forceinline__ void load_rows(const GParams &p, int lane, Group &q)
         q.lo[j] = q.hi0[j] = q.hi1[j] = q.sc[j] = make_uint2(0u, 0u);
         const int64_t slot = q.slot[j];
         if (slot >= 0 && slot < p.num_slots) {
-            const int64_t blk = fastdiv(static_cast<uint32_t>(slot), p.slot_div);
-            const int64_t off = slot - blk * p.block_size;
-            const uint8_t *base = p.cache + blk * int64_t(p.block_size) * DSV4_FP8_SLOT_BYTES;
-            const uint8_t *data = base + off * DSV4_FP8_DATA_BYTES;
+            // slot < 2^32: block and offset in 32-bit arithmetic
+            const uint32_t s32 = static_cast<uint32_t>(slot);
+            const uint32_t blk = fastdiv(s32, p.slot_div);
+            const uint32_t off = s32 - blk * static_cast<uint32_t>(p.block_size);
+            const uint8_t *base = p.cache + uint64_t(blk) * p.block_bytes;
+            const uint8_t *data = base + uint64_t(off) * DSV4_FP8_DATA_BYTES;
             const Span cs = cache_span(p);
             q.lo[j] = ld_stream8_in(data + 8 * lane, cs, p.err);
             if (!rope_lane) {
@@ -148,9 +164,7 @@ __device__ __forceinline__ void load_rows(const GParams &p, int lane, Group &q)
                 q.hi0[j] = ld_stream8_in(data + DSV4_NOPE_DIM + 16 * (lane - 24), cs, p.err);
                 q.hi1[j] = ld_stream8_in(data + DSV4_NOPE_DIM + 16 * (lane - 24) + 8, cs, p.err);
             }
-            q.sc[j] = ldg8_in(
-                base + int64_t(p.block_size) * DSV4_FP8_DATA_BYTES + off * DSV4_FP8_SCALE_BYTES, cs,
-                p.err);
+            q.sc[j] = ldg8_in(base + p.scale_off + uint64_t(off) * DSV4_FP8_SCALE_BYTES, cs, p.err);
         }
     }
 }
@@ -175,15 +189,19 @@ __device__ __forceinline__ void emit_rows(const GParams &p, int lane, int64_t g,
             const uint32_t e0 = (q.sc[j].x >> (8 * b0)) & 0xFFu;
             const uint32_t e1 = (q.sc[j].y >> (8 * (b1 - 4))) & 0xFFu;
             a = dequant8(q.lo[j], e0);
-            b = rope_lane ? make_uint4(q.hi0[j].x, q.hi0[j].y, q.hi1[j].x, q.hi1[j].y)
-                          : dequant8(q.hi0[j], e1);
+            // the rope lanes' bytes are bf16, not codes: they convert the code of 1.0
+            // (a normal code, so they never send the warp down the slow path) and keep
+            // their bf16
+            const uint4 d = dequant8(rope_lane ? make_uint2(0x38383838u, 0x38383838u) : q.hi0[j],
+                                     rope_lane ? 127u : e1);
+            b = rope_lane ? make_uint4(q.hi0[j].x, q.hi0[j].y, q.hi1[j].x, q.hi1[j].y) : d;
         }
         st_stream16_in(row + 8 * lane, a, out_span(p), p.err);
         st_stream16_in(row + 256 + 8 * lane, b, out_span(p), p.err);
     }
 }
 
-__global__ void __launch_bounds__(256) dequant_gather_kernel(const GParams p)
+__global__ void __launch_bounds__(256, 6) dequant_gather_kernel(const GParams p)
 {
     const int lane = threadIdx.x & 31;
     const int warps_per_cta = blockDim.x >> 5;
@@ -228,6 +246,8 @@ int launch_gather(const uint8_t *cache, int64_t num_blocks, int32_t block_size,
     p.num_slots = num_blocks * int64_t(block_size);
     p.block_size = block_size;
     p.slot_div = fastdiv_magic(static_cast<uint32_t>(block_size));
+    p.block_bytes = uint64_t(block_size) * DSV4_FP8_SLOT_BYTES;
+    p.scale_off = uint64_t(block_size) * DSV4_FP8_DATA_BYTES;
     p.slots = slots;
     p.rows = rows;
     p.out = out;

@@ -20,9 +20,16 @@ inline uint64_t fastdiv_magic(uint32_t d)
 }
 
 #ifdef __CUDACC__
+// The high word of magic * n for n < 2^32, from 32-bit halves: with magic =
+// mh * 2^32 + ml and ml * n = a * 2^32 + b (b < 2^32), magic * n = (mh * n + a) *
+// 2^32 + b, so its high 64 bits are (mh * n + a) >> 32; mh * n + a < 2^64.
 __device__ __forceinline__ uint32_t fastdiv(uint32_t n, uint64_t magic)
 {
-    return magic == 0u ? n : static_cast<uint32_t>(__umul64hi(magic, n));
+    if (magic == 0u)
+        return n;
+    const uint64_t t = uint64_t(static_cast<uint32_t>(magic >> 32)) * n +
+                       __umulhi(static_cast<uint32_t>(magic), n);
+    return static_cast<uint32_t>(t >> 32);
 }
 #endif
 

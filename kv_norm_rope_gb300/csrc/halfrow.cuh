@@ -62,39 +62,44 @@ __device__ __forceinline__ void half_load_cs(const KParams &p, int h, bool activ
     }
 }
 
-// The lane's products for its row in the half-warp layout (vector j: dims
-// [128j + 8h, 128j + 8h + 8)), their maxima t[j] = max |xw[j]| (0 for the rope
-// vector of rope lanes) and the row's r: xw = x * w, except that rope lanes
-// (h >= 8) get their dims 448.. final in xw[3] (x * w rotated, then scaled by
-// r).  r comes first and the products after it, so x and the products are not
-// held together (a tiny row rescales x in place first).  With no norm, xw = x
-// and r = 1.  w: the weight (global, packed bf16 in dim order; lane h reads
-// vector j at 16j + h).  The steps of kv_products, so the same bits.
+// Vector j of the lane's row as xw = x * w (or x with no norm).  w: the weight
+// (global, packed bf16 in dim order; lane h reads vector j at 16j + h).
 template <bool kKvNorm>
-__device__ __forceinline__ float half_products(const KParams &p, int h, uint4 *x, float4 cv,
-                                               float4 sv, const uint4 *w, float (*xw)[8], float *t)
+__device__ __forceinline__ void half_vec(const KParams &p, int h, const uint4 *x, const uint4 *w,
+                                         int j, float *xw)
+{
+    if (kKvNorm)
+        prod8(x[j], ldg16_in(w + 16 * j + h, w_span(p), p.err), xw);
+    else
+        widen8(x[j], xw);
+}
+
+// Pass 1 of a half-warp KV row (vector j: dims [128j + 8h, 128j + 8h + 8)): the
+// row's r, the maxima t[j] = max |xw[j]| (0 for the rope vector of rope lanes,
+// h >= 8) and, on rope lanes, the final rope dims 448.. (x * w rotated, then
+// scaled by r).  The products are dropped once their maxima are taken and formed
+// again where they are stored, so a lane holds x (16 registers) rather than 32
+// products.  A tiny row rescales x in place first.  With no norm, xw = x and
+// r = 1.  The steps of kv_products, so the same bits.
+template <bool kKvNorm>
+__device__ __forceinline__ float half_pass1(const KParams &p, int h, uint4 *x, float4 cv,
+                                            float4 sv, const uint4 *w, float *t, float *rope)
 {
     const bool rope_lane = h >= 8;
     float r = 1.0f;
     if (kKvNorm)
         r = row_inv_rms(p.eps, [&] { return half_sumsq(x); }, [&] { half_scale(x); });
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        if (kKvNorm)
-            prod8(x[j], ldg16_in(w + 16 * j + h, w_span(p), p.err), xw[j]);
-        else
-            widen8(x[j], xw[j]);
+    for (int j = 0; j < 3; ++j) {
+        float xw[8];
+        half_vec<kKvNorm>(p, h, x, w, j, xw);
+        t[j] = absmax8(xw);
     }
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-        t[j] = (j < 3 || !rope_lane) ? absmax8(xw[j]) : 0.0f;
-    if (rope_lane) {
-        float u[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            u[k] = xw[3][k];
-        rope8_scaled(u, cv, sv, r, xw[3]);
-    }
+    float u[8];
+    half_vec<kKvNorm>(p, h, x, w, 3, u);
+    t[3] = rope_lane ? 0.0f : absmax8(u);
+    if (rope_lane)
+        rope8_scaled(u, cv, sv, r, rope);
     return r;
 }
 
@@ -105,7 +110,7 @@ __device__ __forceinline__ float half_products(const KParams &p, int h, uint4 *x
 // and near flag (bit j of near_bits); whole-warp lane l asks for blocks l/8
 // and 4 + l/8.  Returns bit j set when the lane's block of vector j exceeds
 // its boundary.
-__device__ __noinline__ int half_exact_bumps(const KParams &p, int lane, int64_t t, int e0, int e1,
+__device__ __noinline__ int half_exact_bumps(KvSrc p, int lane, int64_t t, int e0, int e1,
                                              int e2, int e3, int near_bits)
 {
     const unsigned halves = __ballot_sync(kFull, near_bits != 0);
@@ -142,11 +147,11 @@ __device__ __noinline__ int half_exact_bumps(const KParams &p, int lane, int64_t
 }
 
 // The FP8 store of a half-warp row: block scales, E4M3 payload, bf16 rope
-// tail and the scale word.  xw, r: from half_products.
+// tail and the scale word.  x, tmax, r, rope: as left by half_pass1.
 template <bool kKvNorm>
 __device__ __forceinline__ void half_row_fp8(const KParams &p, int h, bool active, int64_t t,
-                                             int64_t slot, const float (*xw)[8], const float *tmax,
-                                             float r)
+                                             int64_t slot, const uint4 *x, const uint4 *w,
+                                             const float *tmax, float r, const float *rope)
 {
     const bool rope_lane = h >= 8;
 
@@ -159,7 +164,7 @@ __device__ __forceinline__ void half_row_fp8(const KParams &p, int h, bool activ
     if (kKvNorm && __any_sync(kFull, g[0].near || g[1].near || g[2].near || g[3].near)) {
         const int nb = (g[0].near ? 1 : 0) | (g[1].near ? 2 : 0) | (g[2].near ? 4 : 0) |
                        (g[3].near ? 8 : 0);
-        const int bumps = half_exact_bumps(p, threadIdx.x & 31, active ? t : 0, g[0].e, g[1].e,
+        const int bumps = half_exact_bumps(kv_src(p), threadIdx.x & 31, active ? t : 0, g[0].e, g[1].e,
                                            g[2].e, g[3].e, nb);
 #pragma unroll
         for (int j = 0; j < 4; ++j)
@@ -195,24 +200,27 @@ __device__ __forceinline__ void half_row_fp8(const KParams &p, int h, bool activ
         for (int j = 0; j < 4; ++j) {
             if (j == 3 && rope_lane)
                 break;
-            st_stream8_in(data + 128 * j + 8 * h, e4m3x8_block(xw[j], r, g[j].s), cspan, p.err);
+            float xw[8];
+            half_vec<kKvNorm>(p, h, x, w, j, xw);
+            st_stream8_in(data + 128 * j + 8 * h, e4m3x8_block(xw, r, g[j].s), cspan, p.err);
         }
     } else {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             if (j == 3 && rope_lane)
                 break;
-            st_stream8_in(data + 128 * j + 8 * h, e4m3x8_of(xw[j], __fmul_rn(r, pow2_neg(g[j].s))),
+            float xw[8];
+            half_vec<kKvNorm>(p, h, x, w, j, xw);
+            st_stream8_in(data + 128 * j + 8 * h, e4m3x8_of(xw, __fmul_rn(r, pow2_neg(g[j].s))),
                           cspan, p.err);
         }
     }
     if (rope_lane) {
         // rope dims stay bf16; 8-byte stores keep any block_size legal
         uint8_t *tail = data + DSV4_NOPE_DIM + 16 * (h - 8);
-        st_stream8_in(tail, make_uint2(bf16x2_rn(xw[3][0], xw[3][1]), bf16x2_rn(xw[3][2], xw[3][3])),
+        st_stream8_in(tail, make_uint2(bf16x2_rn(rope[0], rope[1]), bf16x2_rn(rope[2], rope[3])),
                       cspan, p.err);
-        st_stream8_in(tail + 8,
-                      make_uint2(bf16x2_rn(xw[3][4], xw[3][5]), bf16x2_rn(xw[3][6], xw[3][7])),
+        st_stream8_in(tail + 8, make_uint2(bf16x2_rn(rope[4], rope[5]), bf16x2_rn(rope[6], rope[7])),
                       cspan, p.err);
     }
     if (h == 0)
@@ -228,20 +236,23 @@ __device__ __forceinline__ void half_row(const KParams &p, int h, bool active, i
 {
     float4 cv, sv;
     half_load_cs(p, h, active, pos, cv, sv);
-    float xw[4][8], tmax[4];
-    const float r = half_products<kKvNorm>(p, h, x, cv, sv, w, xw, tmax);
+    float tmax[4], rope[8];
+    const float r = half_pass1<kKvNorm>(p, h, x, cv, sv, w, tmax, rope);
 
     if constexpr (kStore == DSV4_STORE_BF16) {
         if (active) {
             uint16_t *row = reinterpret_cast<uint16_t *>(p.cache) + slot * kHead;
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
+            for (int j = 0; j < 4; ++j) {
+                float xw[8];
+                half_vec<kKvNorm>(p, h, x, w, j, xw);
                 st_stream16_in(row + 128 * j + 8 * h,
-                               (j == 3 && h >= 8) ? bf16x8_rn(xw[3]) : bf16x8_scaled(xw[j], r),
+                               (j == 3 && h >= 8) ? bf16x8_rn(rope) : bf16x8_scaled(xw, r),
                                cache_span<kStore>(p), p.err);
+            }
         }
     } else {
-        half_row_fp8<kKvNorm>(p, h, active, t, slot, xw, tmax, r);
+        half_row_fp8<kKvNorm>(p, h, active, t, slot, x, w, tmax, r, rope);
     }
 }
 
@@ -308,15 +319,10 @@ __device__ __forceinline__ void q_half_out(int h, const uint4 *x, float r, float
     for (int j = 0; j < 4; ++j)
         widen8(x[j], y[j]);
 #pragma unroll
-    for (int j = 0; j < 3; ++j) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            y[j][k] = __fmul_rn(y[j][k], r);
-    }
+    for (int j = 0; j < 3; ++j)
+        scale8<false>(y[j], r, y[j]);
     if (h < 8) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            y[3][k] = __fmul_rn(y[3][k], r);
+        scale8<false>(y[3], r, y[3]);
     } else {
         float u[8];
 #pragma unroll

@@ -162,7 +162,7 @@ __device__ __forceinline__ float quarter_max_scatter(const float *a, int g)
 // Lane g of quarter c holds block g's exponent e and near flag; whole-warp
 // lane l asks for blocks l/8 and 4 + l/8.  Returns, to lane g of each
 // quarter, whether block g exceeds its boundary.
-__device__ __noinline__ bool quarter_exact_bump(const KParams &p, int lane, int64_t t, int e,
+__device__ __noinline__ bool quarter_exact_bump(KvSrc p, int lane, int64_t t, int e,
                                                 bool near)
 {
     const unsigned quarters = __ballot_sync(kFull, near);
@@ -200,7 +200,7 @@ __device__ __forceinline__ void quarter_row_fp8(const KParams &p, int lane, bool
     sg.near = sg.near && active;
     // with no norm, v = x exactly and the guess is already exact
     if (kKvNorm && __any_sync(kFull, sg.near)) {
-        const bool up = quarter_exact_bump(p, lane, active ? t : 0, sg.e, sg.near);
+        const bool up = quarter_exact_bump(kv_src(p), lane, active ? t : 0, sg.e, sg.near);
         if (sg.near)
             sg.s = clamp_s(sg.e - 8 + (up ? 1 : 0));
     }

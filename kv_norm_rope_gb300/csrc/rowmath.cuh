@@ -31,6 +31,30 @@ __device__ __forceinline__ Span w_span(const KParams &p)
 {
     return Span{p.w, 1024u};
 }
+
+// What the exact scale decision reads, passed by value to its out-of-line
+// routines: a reference to the launch's KParams there would make every thread
+// copy the whole parameter block to its stack at the start of the kernel (a
+// kernel parameter has no generic address).
+struct KvSrc {
+    const uint16_t *kv;
+    const uint16_t *w;
+    int64_t num_tokens;
+    float eps;
+    int32_t *err;
+};
+__device__ __forceinline__ KvSrc kv_src(const KParams &p)
+{
+    return KvSrc{p.kv, p.w, p.num_tokens, p.eps, p.err};
+}
+__device__ __forceinline__ Span kv_span(const KvSrc &p)
+{
+    return Span{p.kv, uint64_t(p.num_tokens) * 1024u};
+}
+__device__ __forceinline__ Span w_span(const KvSrc &p)
+{
+    return Span{p.w, 1024u};
+}
 __device__ __forceinline__ Span pos_span(const KParams &p)
 {
     return Span{p.pos, uint64_t(p.num_tokens) * 8u};
@@ -332,7 +356,7 @@ __device__ __forceinline__ float boundary_f32(int e)
 // norm recomputed in fp64 in the whole-warp order and each element evaluated
 // in the order of the definition, (x * r) * w, against the boundary 1.75 * 2^e
 // of its block.  Same arguments and result as exact_scale_bumps.
-__device__ __noinline__ int exact_scale_bumps_fp64(const KParams &p, int lane, int64_t t, int e0,
+__device__ __noinline__ int exact_scale_bumps_fp64(KvSrc p, int lane, int64_t t, int e0,
                                               bool near0, int e1, bool near1)
 {
     const uint4 *row = reinterpret_cast<const uint4 *>(p.kv + t * kHead);
@@ -379,7 +403,7 @@ __device__ __noinline__ int exact_scale_bumps_fp64(const KParams &p, int lane, i
 // (above); what that cannot settle goes to the fp64 routine.  Returns bit 0:
 // the lane's half-0 block exceeds its boundary; bit 1: the half-1 block does
 // (the same in the block's 8 lanes).
-__device__ __noinline__ int exact_scale_bumps(const KParams &p, int lane, int64_t t, int e0,
+__device__ __noinline__ int exact_scale_bumps(KvSrc p, int lane, int64_t t, int e0,
                                               bool near0, int e1, bool near1)
 {
     const uint4 *row = reinterpret_cast<const uint4 *>(p.kv + t * kHead);
@@ -517,52 +541,80 @@ __device__ __forceinline__ uint4 scale8_2p64(uint4 x)
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// E4M3 of the payload of 8 values of one block: xw * k in one rounding, or for
-// two_step (s < kTwoStepBelow) fp32(xw * r) * k2 with k2 = 2^-s
-__device__ __forceinline__ uint2 e4m3x8_of(const float *xw, float k)
+// out[k] = in[k] * k for 8 values, two at a time with the packed fp32 multiply
+// (mul.rn.f32x2): each half is the correctly rounded scalar product, so the
+// bits are those of 8 scalar multiplies.  kPacked = false takes 8 scalar
+// multiplies instead, for code at its register limit (a packed operand must sit
+// in an aligned register pair, which can cost copies there).
+template <bool kPacked = true>
+__device__ __forceinline__ void scale8(const float *in, float k, float *out)
 {
-    return make_uint2(e4m3x4_rn(__fmul_rn(xw[0], k), __fmul_rn(xw[1], k), __fmul_rn(xw[2], k),
-                                __fmul_rn(xw[3], k)),
-                      e4m3x4_rn(__fmul_rn(xw[4], k), __fmul_rn(xw[5], k), __fmul_rn(xw[6], k),
-                                __fmul_rn(xw[7], k)));
+    if constexpr (!kPacked) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            out[i] = __fmul_rn(in[i], k);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %4};\n\t"
+                "mul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+                : "=f"(out[2 * i]), "=f"(out[2 * i + 1])
+                : "f"(in[2 * i]), "f"(in[2 * i + 1]), "f"(k));
+    }
 }
 
+// E4M3 of the payload of 8 values of one block: xw * k in one rounding, or for
+// two_step (s < kTwoStepBelow) fp32(xw * r) * k2 with k2 = 2^-s
+template <bool kPacked = true>
+__device__ __forceinline__ uint2 e4m3x8_of(const float *xw, float k)
+{
+    float v[8];
+    scale8<kPacked>(xw, k, v);
+    return make_uint2(e4m3x4_rn(v[0], v[1], v[2], v[3]), e4m3x4_rn(v[4], v[5], v[6], v[7]));
+}
+
+template <bool kPacked = true>
 __device__ __forceinline__ uint2 e4m3x8_two_step(const float *xw, float r, float k2)
 {
     float v[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-        v[k] = __fmul_rn(__fmul_rn(xw[k], r), k2);
+    scale8<kPacked>(xw, r, v);
+    scale8<kPacked>(v, k2, v);
     return make_uint2(e4m3x4_rn(v[0], v[1], v[2], v[3]), e4m3x4_rn(v[4], v[5], v[6], v[7]));
 }
 
 // the payload of a block, either form (callers take this path only when some
 // lane of the warp has a block below kTwoStepBelow; the others use e4m3x8_of
 // with r * 2^-s directly, so the common path carries no select)
+template <bool kPacked = true>
 __device__ __forceinline__ uint2 e4m3x8_block(const float *xw, float r, int s)
 {
-    return s < kTwoStepBelow ? e4m3x8_two_step(xw, r, pow2_neg(s))
-                             : e4m3x8_of(xw, __fmul_rn(r, pow2_neg(s)));
+    return s < kTwoStepBelow ? e4m3x8_two_step<kPacked>(xw, r, pow2_neg(s))
+                             : e4m3x8_of<kPacked>(xw, __fmul_rn(r, pow2_neg(s)));
 }
 
 // bf16 of fp32(xw * r) for 8 values
 __device__ __forceinline__ uint4 bf16x8_scaled(const float *xw, float r)
 {
     float v[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-        v[k] = __fmul_rn(xw[k], r);
+    scale8(xw, r, v);
     return bf16x8_rn(v);
 }
 
-// max |xw| of 8 values
+// max(|a|, |b|, |c|) in one three-input max (sm_100 and later)
+__device__ __forceinline__ float max3_abs(float a, float b, float c)
+{
+    float d;
+    asm("max.abs.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// max |xw| of 8 values (+0 when all are zeros)
 __device__ __forceinline__ float absmax8(const float *xw)
 {
-    float t = 0.0f;
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-        t = fmaxf(t, fabsf(xw[k]));
-    return t;
+    const float a = max3_abs(xw[0], xw[1], xw[2]);
+    const float b = max3_abs(xw[3], xw[4], xw[5]);
+    const float c = max3_abs(xw[6], xw[7], a);
+    return fmaxf(fabsf(b), fabsf(c));
 }
 
 // The lane's products for the KV row of token tok in the whole-warp layout
@@ -670,7 +722,7 @@ __device__ __forceinline__ void kv_row(const KParams &p, int lane, int64_t t, in
     ScaleGuess g1 = ue8m0_guess(__fmul_rn(group8_max(tmax[1]), r));  // lanes 24..31: never near
     // with no norm, v = x exactly and the guess is already exact
     if (kKvNorm && __any_sync(kFull, g0.near || g1.near)) {
-        const int bumps = exact_scale_bumps(p, lane, t, g0.e, g0.near, g1.e, g1.near);
+        const int bumps = exact_scale_bumps(kv_src(p), lane, t, g0.e, g0.near, g1.e, g1.near);
         if (g0.near)
             g0.s = clamp_s(g0.e - 8 + (bumps & 1));
         if (g1.near)
@@ -761,13 +813,9 @@ __device__ __forceinline__ void q_row_out(int lane, uint4 a, uint4 b, float r, f
     float y[16];
     widen8(a, y);
     widen8(b, y + 8);
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-        y[k] = __fmul_rn(y[k], r);
+    scale8(y, r, y);
     if (lane < 24) {
-#pragma unroll
-        for (int k = 8; k < 16; ++k)
-            y[k] = __fmul_rn(y[k], r);
+        scale8(y + 8, r, y + 8);
     } else {
         float u[8];
 #pragma unroll
