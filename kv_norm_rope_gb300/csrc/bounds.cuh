@@ -94,6 +94,12 @@ __device__ __forceinline__ void st_stream16_in(void *p, uint4 v, Span s, int32_t
         __stcs(reinterpret_cast<uint4 *>(p), v);
 }
 
+__device__ __forceinline__ void st16_in(void *p, uint4 v, Span s, int32_t *err)
+{
+    if (in_span(p, 16, s, err))
+        *reinterpret_cast<uint4 *>(p) = v;
+}
+
 __device__ __forceinline__ void st_stream8_in(void *p, uint2 v, Span s, int32_t *err)
 {
     if (in_span(p, 8, s, err))

@@ -44,21 +44,30 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
+// one try_wait on the phase with the given parity: true once it has completed
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(done)
+                 : "r"(smem_addr(bar)), "r"(parity)
+                 : "memory");
+    return done != 0;
+}
+
 // wait for the completion of the phase with the given parity; false once
-// max_cycles SM clock cycles have passed without it
+// max_cycles SM clock cycles have passed without it (the clock is read only
+// when the first try does not succeed)
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
                                           long long max_cycles = kWaitCycles)
 {
+    if (mbar_try_wait(bar, parity))
+        return true;
     const long long t0 = clock64();
     for (;;) {
-        uint32_t done;
-        asm volatile("{\n\t.reg .pred p;\n\t"
-                     "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-                     "selp.u32 %0, 1, 0, p;\n\t}"
-                     : "=r"(done)
-                     : "r"(smem_addr(bar)), "r"(parity)
-                     : "memory");
-        if (done)
+        if (mbar_try_wait(bar, parity))
             return true;
         if (clock64() - t0 > max_cycles)
             return false;

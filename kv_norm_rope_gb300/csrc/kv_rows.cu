@@ -390,9 +390,15 @@ __global__ void __launch_bounds__(kKvThreads, kKvCtasPerSm) kv_rows_kernel(const
         }
         const uint4 *row = reinterpret_cast<const uint4 *>(stages + s * kItemBytes) + c * 64;
         uint4 x[8];
+        if (t - c + 4 <= T) {  // the whole item is live (warp-uniform): no selects
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-            x[u] = t < T ? row[8 * u + g] : make_uint4(0u, 0u, 0u, 0u);
+            for (int u = 0; u < 8; ++u)
+                x[u] = row[8 * u + g];
+        } else {
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                x[u] = t < T ? row[8 * u + g] : make_uint4(0u, 0u, 0u, 0u);
+        }
         // every lane has read the stage: it may be refilled
         fence_proxy_async_smem();
         __syncwarp();
