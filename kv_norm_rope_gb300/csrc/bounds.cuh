@@ -9,9 +9,9 @@
 // The pages record two faults of this operator on other hardware, both
 // address faults: a 32-bit index that wrapped past 2^31 q elements and a KV
 // store that wrote into the rope region of the row (FlagGems-vllm PR #684,
-// "Performance against a baseline").  No memory checker runs on this GPU
-// pool, so the checked build is how every computed address is held against
-// its buffer while the GPU tests run.
+// "Performance against a baseline").  The checked build holds every computed
+// address against its buffer while the GPU tests run, with no memory checker
+// needed.
 #pragma once
 
 #include <cuda_runtime.h>
