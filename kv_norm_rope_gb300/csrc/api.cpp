@@ -204,17 +204,18 @@ int dsv4_launch_plan(int64_t num_tokens, int32_t num_heads, int32_t sm_count, in
     const int stream_warps = dsv4::kStreamThreads / 32;
     const int64_t warp_slots = int64_t(sm_count) * ctas_per_sm * stream_warps;
     if (variant == DSV4_VARIANT_AUTO) {
-        // Measured on GB300 (graph-timed, cold L2): one row per warp is fastest
-        // below about a quarter of the warp slots; from there, with q heads, the
-        // half-warp kernel beats both the others up to 12 rounds of the stream
-        // kernel's 3-row groups (3-35% at 2K-100K rows, a tie near 130K-200K);
-        // beyond, the whole-warp stream (2.5% ahead from ~260K rows).  With no q
-        // heads, STREAM runs the KV-row kernel, whose bulk-copy pipeline costs
-        // ~1.7 us more to start: SMALL is ahead up to ~2.4K rows (two thirds of
-        // the warp slots), the KV-row kernel from there (by 20% at 4K rows, 2x at
-        // 64K).
+        // Measured on GB300 (graph-timed, cold L2): with q heads, one row per warp
+        // is fastest up to about the warp slots of the stream kernel (10-13% ahead
+        // of the half-warp kernel at 0.5K-2K rows, 4% at 3.1K; 18-22% behind from
+        // 4.1K); from there the half-warp kernel beats both the others up to 12
+        // rounds of the stream kernel's 3-row groups (3-10% ahead of STREAM at
+        // 16K-66K rows, a tie near 130K); beyond, the whole-warp stream (2-3% ahead
+        // at 264K rows).  With no q heads, STREAM runs the KV-row kernel, whose
+        // bulk-copy pipeline costs ~1.7 us more to start: SMALL is ahead up to
+        // ~2.4K rows (two thirds of the warp slots), the KV-row kernel from there
+        // (by 20% at 4K rows, 2x at 64K).
         const int64_t round = warp_slots * dsv4::kStreamRowsPerWarp;
-        const int64_t small_below = num_heads > 0 ? warp_slots / 4 : 2 * warp_slots / 3;
+        const int64_t small_below = num_heads > 0 ? warp_slots : 2 * warp_slots / 3;
         variant = rows < small_below                      ? DSV4_VARIANT_SMALL
                   : num_heads > 0 && rows < 12 * round    ? DSV4_VARIANT_HALF
                                                           : DSV4_VARIANT_STREAM;

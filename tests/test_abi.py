@@ -108,12 +108,12 @@ def test_launch_plan_small_and_stream():
     # 131072 x 129 rows: persistent grid, 4 CTAs on each of 152 SMs
     p = k.launch_plan(131072, 128, 152, 4)
     assert (p.variant, p.threads, p.ctas, p.rows) == (k.VARIANT_STREAM, 256, 608, 131072 * 129)
-    # the crossovers: rows below a quarter of the warp slots go SMALL; with q heads,
-    # below 12 rounds of 3-row groups HALF; beyond, STREAM
+    # the crossovers: with q heads, rows below the warp slots go SMALL, below 12
+    # rounds of 3-row groups HALF; beyond, STREAM
     warp_slots = 152 * 4 * 8
     rnd = warp_slots * p.rows_per_warp
-    assert k.launch_plan(warp_slots // 4 // 9 - 1, 8, 152, 4).variant == k.VARIANT_SMALL
-    assert k.launch_plan(warp_slots // 4 // 9 + 1, 8, 152, 4).variant == k.VARIANT_HALF
+    assert k.launch_plan(warp_slots // 9 - 1, 8, 152, 4).variant == k.VARIANT_SMALL
+    assert k.launch_plan(warp_slots // 9 + 1, 8, 152, 4).variant == k.VARIANT_HALF
     assert k.launch_plan(12 * rnd // 65 - 1, 64, 152, 4).variant == k.VARIANT_HALF
     assert k.launch_plan(12 * rnd // 65 + 1, 64, 152, 4).variant == k.VARIANT_STREAM
     # KV rows only: never HALF (they have their own kernel behind STREAM)
