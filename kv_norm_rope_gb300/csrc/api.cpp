@@ -211,11 +211,11 @@ int dsv4_launch_plan(int64_t num_tokens, int32_t num_heads, int32_t sm_count, in
         // rounds of the stream kernel's 3-row groups (3-10% ahead of STREAM at
         // 16K-66K rows, a tie near 130K); beyond, the whole-warp stream (2-3% ahead
         // at 264K rows).  With no q heads, STREAM runs the KV-row kernel, whose
-        // bulk-copy pipeline costs ~1.7 us more to start: SMALL is ahead up to
-        // ~2.4K rows (two thirds of the warp slots), the KV-row kernel from there
-        // (by 20% at 4K rows, 2x at 64K).
+        // bulk-copy pipeline costs more to start: SMALL is 8-14% ahead at 1K-3K
+        // rows, the KV-row kernel 15-33% ahead from 4K rows, so the switch is at
+        // the warp slots there too.
         const int64_t round = warp_slots * dsv4::kStreamRowsPerWarp;
-        const int64_t small_below = num_heads > 0 ? warp_slots : 2 * warp_slots / 3;
+        const int64_t small_below = warp_slots;
         variant = rows < small_below                      ? DSV4_VARIANT_SMALL
                   : num_heads > 0 && rows < 12 * round    ? DSV4_VARIANT_HALF
                                                           : DSV4_VARIANT_STREAM;

@@ -116,10 +116,10 @@ def test_launch_plan_small_and_stream():
     assert k.launch_plan(warp_slots // 9 + 1, 8, 152, 4).variant == k.VARIANT_HALF
     assert k.launch_plan(12 * rnd // 65 - 1, 64, 152, 4).variant == k.VARIANT_HALF
     assert k.launch_plan(12 * rnd // 65 + 1, 64, 152, 4).variant == k.VARIANT_STREAM
-    # KV rows only: never HALF (they have their own kernel behind STREAM)
-    # with no q heads the KV-row kernel's start-up cost moves the switch to 2/3 of the slots
-    assert k.launch_plan(2 * warp_slots // 3 - 1, 0, 152, 4).variant == k.VARIANT_SMALL
-    assert k.launch_plan(2 * warp_slots // 3 + 1, 0, 152, 4).variant == k.VARIANT_STREAM
+    # KV rows only: never HALF (they have their own kernel behind STREAM); the same
+    # switch at the warp slots
+    assert k.launch_plan(warp_slots - 1, 0, 152, 4).variant == k.VARIANT_SMALL
+    assert k.launch_plan(warp_slots + 1, 0, 152, 4).variant == k.VARIANT_STREAM
     # forced variants
     assert k.launch_plan(131072, 128, 152, 4, k.VARIANT_SMALL).ctas == 131072 * 129 // 2
     p = k.launch_plan(3, 1, 152, 4, k.VARIANT_STREAM)
