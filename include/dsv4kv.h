@@ -273,9 +273,9 @@ typedef struct {
 /*
  * Fill *plan for T tokens, H heads on a GPU with sm_count SMs where
  * ctas_per_sm CTAs of the streaming kernel fit per SM.  variant AUTO picks
- * SMALL when there are fewer rows than a quarter of the GPU's warp slots (two
- * thirds of them with num_heads 0) (SGLang PR #33358, "Modifications" item 3: a
- * grid-starved multi-token layout loses at small N); with q heads, HALF below 12
+ * SMALL when there are fewer rows than the GPU's warp slots (sm_count x
+ * ctas_per_sm x 8) (SGLang PR #33358, "Modifications" item 3: a grid-starved
+ * multi-token layout loses at small N); with q heads, HALF below 12
  * rounds of the streaming kernel's groups
  * (warp slots x rows_per_warp x 12; decode- to mid-sized batches, where HALF
  * measured faster); else STREAM (for num_heads 0, the KV-row kernel).  HALF: ceil(T/2) KV row pairs and
