@@ -30,6 +30,17 @@ def test_variants_bit_identical(wl):
         assert o.err == outs[0].err
 
 
+@pytest.mark.parametrize("T,H", [(405, 8), (406, 8), (3647, 0), (3649, 0)])
+def test_auto_at_its_small_switch(T, H):
+    """Rows just below and just above the warp slots of a 152-SM GB300 (3648), where AUTO
+    switches from one row per warp to the half-warp or KV-row kernel: the same bytes as
+    the streaming kernel on either side."""
+    inp = harness.make_inputs(configs.generic(T, H, seed=16 + T))
+    a = harness.run_gpu(inp, k.VARIANT_AUTO)
+    b = harness.run_gpu(inp, k.VARIANT_STREAM)
+    assert np.array_equal(a.q, b.q) and np.array_equal(a.cache, b.cache) and a.err == b.err
+
+
 def test_repeat_is_deterministic():
     wl = configs.generic(3000, 32, seed=15)
     inp = harness.make_inputs(wl)
