@@ -347,7 +347,8 @@ int dsv4_dequant_gather(const uint8_t *kv_cache, int64_t num_blocks, int32_t blo
         return DSV4_ERR_CUDA;
     const int64_t groups = (num_rows + dsv4::gather_rows_per_warp() - 1) /
                            dsv4::gather_rows_per_warp();
-    const int64_t need = (groups + 7) / 8;  // 8 warps per CTA
+    const int64_t warps = dsv4::gather_warps_per_cta();
+    const int64_t need = (groups + warps - 1) / warps;
     return dsv4::launch_gather(kv_cache, num_blocks, block_size, slots, num_rows,
                                static_cast<uint16_t *>(out), device_error,
                                need < resident ? need : resident,

@@ -20,6 +20,10 @@ int kv_rows_ctas_per_sm(int *ctas_per_sm);
 int kv_rows_per_warp();
 int launch_kv_rows(int store_mode, const LaunchArgs &a, int64_t max_ctas, cudaStream_t stream);
 
+// Warps per CTA of the FP8 cache reader (dequant_gather.cu; its other entry points
+// are in launch.h).
+int gather_warps_per_cta();
+
 // The fused step with one row per half-warp (qnorm_rope_kv_insert_half.cu).
 int half_ctas_per_sm(int *ctas_per_sm);
 int half_q_rows_per_warp();
