@@ -879,6 +879,67 @@ def run_reference(args):
     return 0
 
 
+def other_configs(lib, dev, names, steps: int, warmup: int):
+    """The fused step on the other named workloads, in the same process after the main
+    measurement, each timed like it (warm-up launches, CUDA events around every launch,
+    a 256 MB L2 flush before each launch of a step that moves less than 4x the L2, plus
+    its graph-replay time), so that one run of the default command records every
+    configuration.  Returns one dict per workload."""
+    import torch
+
+    import kv_norm_rope_gb300 as k
+    peak, _ = measured_peaks()
+    out = []
+    for name in names:
+        batch = DeviceBatch(configs.WORKLOADS[name], dev)
+        wl = batch.wl
+        stream = torch.cuda.current_stream(dev)
+        fn, call_args = batch.call(lib, stream.cuda_stream)
+        for _ in range(warmup):
+            st = fn(*call_args)
+            if st != 0:
+                raise RuntimeError(f"launch failed: {k.status_string(st)}")
+        torch.cuda.synchronize(dev)
+        if int(batch.err.item()) != 0:
+            raise RuntimeError(f"device error bits {int(batch.err.item())} on {name}")
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) \
+            if batch.bytes < 4 * (129 << 20) else None
+        events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * steps)]
+        torch.cuda.synchronize(dev)
+        for i in range(steps):
+            if flush is not None:
+                flush.fill_(i & 0xFF)
+            events[2 * i].record(stream)
+            fn(*call_args)
+            events[2 * i + 1].record(stream)
+        torch.cuda.synchronize(dev)
+        per_launch = [events[2 * i].elapsed_time(events[2 * i + 1]) / 1e3 for i in range(steps)]
+        step_s = (statistics.mean(per_launch) if flush is not None
+                  else events[0].elapsed_time(events[-1]) / 1e3 / steps)
+        plan = k.launch_plan(wl.T, wl.H,
+                             torch.cuda.get_device_properties(dev).multi_processor_count, 3)
+        row = {"workload": name, "T": wl.T, "H": wl.H, "store": wl.store,
+               "variant": {k.VARIANT_STREAM: "stream", k.VARIANT_SMALL: "small",
+                           k.VARIANT_HALF: "half"}[plan.variant],
+               "bytes_per_step": batch.bytes, "steps": steps,
+               "ms_per_step": round(step_s * 1e3, 4),
+               "GB/s": round(batch.bytes / step_s / 1e9, 1),
+               "frac_of_measured_peak": round(batch.bytes / step_s / 1e9 / peak, 4),
+               "tokens_per_s": round(wl.T / step_s, 1),
+               "l2": "flushed before every launch (256 MB write)" if flush is not None
+               else "inputs larger than L2"}
+        if flush is not None:
+            g_us = graph_device_us(batch, lib, dev, flush)
+            row["graph_us_per_launch"] = round(g_us, 3)
+            row["graph_GB/s"] = round(batch.bytes / g_us / 1e3, 1)
+        if int(batch.err.item()) != 0:
+            raise RuntimeError(f"device error bits {int(batch.err.item())} on {name}")
+        out.append(row)
+        del batch, flush, events
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     import torch
 
@@ -980,6 +1041,12 @@ def run_ours(args):
     kac_after = known_answer_check() if rank == 0 else "skipped"
     if rank != 0:
         return 0
+    # the other configurations of the operator, when this is the default stress run
+    others = None
+    if (world == 1 and args.op == "fused" and args.workload == "stress" and not args.tokens
+            and args.variant == "auto" and not args.no_other_configs):
+        others = other_configs(lib, dev, ("prefill", "bf16_store", "decode", "tiny"),
+                               min(args.steps, 30), args.warmup)
 
     peak, peak_kind = measured_peaks()
     achieved = batch.bytes / mean_launch / 1e9
@@ -1041,6 +1108,8 @@ def run_ours(args):
     }
     if e2e is not None:
         line["e2e"] = e2e
+    if others is not None:
+        line["other_configs"] = others
     if not args.no_cpu_baseline and args.op == "fused":
         line["cpu_baseline"] = cpu_baseline(configs.WORKLOADS[args.workload], args.cpu_seconds)
     print(json.dumps(line), flush=True)
@@ -1071,6 +1140,8 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=6)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-configs", action="store_true",
+                    help="skip the other workloads that the default stress run also times")
     ap.add_argument("--cpu-seconds", type=float, default=2.0,
                     help="wall seconds of oracle work on all host cores for cpu_baseline")
     args = ap.parse_args(argv)
