@@ -263,7 +263,8 @@ __device__ __forceinline__ void quarter_row_fp8(const KParams &p, int lane, bool
 // arithmetic.
 template <int kStore, bool kKvNorm>
 __device__ __forceinline__ void kv_quad_row(const KParams &p, int lane, int64_t t, int64_t pos,
-                                            int64_t slot, uint4 *x, const uint4 *w_smem)
+                                            int64_t slot, uint4 *x, const uint4 *w_smem, float4 cv,
+                                            float4 sv)
 {
     const int g = lane & 7;
     const bool live = t < p.num_tokens;
@@ -277,11 +278,13 @@ __device__ __forceinline__ void kv_quad_row(const KParams &p, int lane, int64_t 
     const bool active = live && pos_ok && slot >= 0 && slot < p.num_slots;
     if (!__any_sync(kFull, active))
         return;
-    float4 cv = make_float4(0.f, 0.f, 0.f, 0.f), sv = cv;
-    if (active) {
-        const float *cs = p.cs + pos * DSV4_ROPE_DIM + 4 * g;
-        cv = ldg_f4_in(cs, cs_span(p), p.err);
-        sv = ldg_f4_in(cs + DSV4_ROPE_DIM / 2, cs_span(p), p.err);
+    if constexpr (kStore == DSV4_STORE_FP8) {
+        // (the bf16 kernel has its cos/sin from the caller, loaded before the kv wait)
+        if (active) {
+            const float *cs = p.cs + pos * DSV4_ROPE_DIM + 4 * g;
+            cv = ldg_f4_in(cs, cs_span(p), p.err);
+            sv = ldg_f4_in(cs + DSV4_ROPE_DIM / 2, cs_span(p), p.err);
+        }
     }
     float tmax[8];
     const float r = quarter_pass1<kKvNorm>(p, g, x, w_smem, tmax);
@@ -299,10 +302,9 @@ __device__ __forceinline__ void kv_quad_row(const KParams &p, int lane, int64_t 
             for (int u = 0; u < 7; ++u) {
                 float xw[8];
                 quarter_vec<kKvNorm>(x, w_smem, g, u, xw);
-                st_stream16_in(row + 64 * u + 8 * g, bf16x8_scaled(xw, r), cache_span<kStore>(p),
-                               p.err);
+                st16_in(row + 64 * u + 8 * g, bf16x8_scaled(xw, r), cache_span<kStore>(p), p.err);
             }
-            st_stream16_in(row + 64 * 7 + 8 * g, bf16x8_rn(rope), cache_span<kStore>(p), p.err);
+            st16_in(row + 64 * 7 + 8 * g, bf16x8_rn(rope), cache_span<kStore>(p), p.err);
         }
     } else {
         quarter_row_fp8<kKvNorm>(p, lane, active, t, slot, x, w_smem, tmax, r, rope);
@@ -379,6 +381,17 @@ __global__ void __launch_bounds__(kKvThreads, kKvCtasPerSm) kv_rows_kernel(const
         const int64_t pos_n = next_live ? ldg_i64_in(p.pos + tn, pos_span(p), p.err) : 0;
         const int64_t slot_n = next_live ? ldg_i64_in(p.slot + tn, slot_span(p), p.err) : -1;
 
+        // the bf16 kernel, with registers to spare, issues this item's cos/sin loads
+        // before the wait for its kv (the position is known an item ahead); the FP8
+        // kernel, at its register limit, loads them after (measured faster each way)
+        float4 cv = make_float4(0.f, 0.f, 0.f, 0.f), sv = cv;
+        if constexpr (kStore == DSV4_STORE_BF16) {
+            if (t < T && pos >= 0 && pos < p.max_pos && slot >= 0 && slot < p.num_slots) {
+                const float *cs = p.cs + pos * DSV4_ROPE_DIM + 4 * g;
+                cv = ldg_f4_in(cs, cs_span(p), p.err);
+                sv = ldg_f4_in(cs + DSV4_ROPE_DIM / 2, cs_span(p), p.err);
+            }
+        }
         const int s = int(j % kKvStages);
         if (!mbar_wait(&bars[s], uint32_t(j / kKvStages) & 1)) {
             if (lane == 0)
@@ -407,7 +420,7 @@ __global__ void __launch_bounds__(kKvThreads, kKvCtasPerSm) kv_rows_kernel(const
                 issue(issued);
             ++issued;
         }
-        kv_quad_row<kStore, kKvNorm>(p, lane, t, pos, slot, x, w_smem);
+        kv_quad_row<kStore, kKvNorm>(p, lane, t, pos, slot, x, w_smem, cv, sv);
         t = tn;
         pos = pos_n;
         slot = slot_n;
